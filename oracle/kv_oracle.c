@@ -1,0 +1,306 @@
+/*
+ * kv_oracle.c -- plain fp64 CPU oracle for decode attention over a paged KV
+ * cache with Quest-style page selection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg load this file's library.  It shares no
+ * code, header or constant with the CUDA path, and the CUDA path never calls
+ * it.  Every loop below is written for a reader checking it against the
+ * definitions, not for speed.
+ *
+ * Sources (page title, section):
+ *  - KVDrive: A Holistic Multi-Tier KV Cache Management System for
+ *    Long-Context LLM Inference, section 2.2 "Sparse attention": keys are split
+ *    into blocks; a block's importance is estimated by multiplying the query
+ *    with the channel-wise minimum and maximum of its keys; only the Top-K
+ *    blocks per query are retrieved.
+ *  - same page, section 2.3 "KV cache offloading": each decode token (1)
+ *    selects critical entries through an index held in GPU memory, (2) fetches
+ *    them, (3) computes sparse attention over them.
+ *  - Dual-Blade: Dual-Path NVMe-Direct KV-Cache Offloading for Edge LLM
+ *    Inference, "Background and key observations": every decode step loads all
+ *    previous KV pairs of the cache (dense decode attention).
+ *  - DirectKV (No Buffer, No Bottleneck), core method 2-3: decode keeps the
+ *    single query and the output resident and scans every K/V once with a
+ *    streaming softmax.  The streaming form is an evaluation order; the value
+ *    it computes is plain softmax attention, which is what this file writes.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - score = sum over channels of max(q_c * min_c, q_c * max_c), no 1/sqrt(d);
+ *  - min/max order is IEEE totalOrder on non-NaN values, so -0.0 < +0.0;
+ *  - top-K ties go to the lower page index; output pages ascending, padded
+ *    with -1 when fewer than K pages exist;
+ *  - query head h reads kv head h / (Hq / Hkv);
+ *  - only the valid tokens of the last, partial page take part.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OKV_F32 0
+#define OKV_F16 1
+#define OKV_BF16 2
+
+/* ------------------------------------------------------------------------- */
+/* element decode: exact value of a stored element                            */
+/* ------------------------------------------------------------------------- */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double dec_f16(uint16_t h) {
+  int sign = h >> 15;
+  int e = (h >> 10) & 31;
+  int m = h & 1023;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -24); /* subnormal: m * 2^(1-15-10) */
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(1024 + m), e - 25); /* (1 + m/2^10) * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32. */
+static double dec_bf16(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+double okv_decode(int dtype, const void *base, int64_t i) {
+  if (dtype == OKV_F32) return (double)((const float *)base)[i];
+  if (dtype == OKV_F16) return dec_f16(((const uint16_t *)base)[i]);
+  return dec_bf16(((const uint16_t *)base)[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* index build: channel-wise key min / max of one page                        */
+/* ------------------------------------------------------------------------- */
+
+/* a < b in IEEE totalOrder restricted to non-NaN values (-0.0 < +0.0). */
+static int total_less(double a, double b) {
+  if (a < b) return 1;
+  if (a > b) return 0;
+  return signbit(a) && !signbit(b);
+}
+
+/* Page of n valid tokens starting at element `off` of `k` ([n][d] row-major).
+ * mn[c] = min over t < n of k[t][c]; mx[c] = max.  (KVDrive, section 2.2.) */
+void okv_page_minmax(int dtype, int d, int n, const void *k, int64_t off, double *mn,
+                     double *mx) {
+  for (int c = 0; c < d; ++c) {
+    double lo = okv_decode(dtype, k, off + c);
+    double hi = lo;
+    for (int t = 1; t < n; ++t) {
+      double x = okv_decode(dtype, k, off + (int64_t)t * d + c);
+      if (total_less(x, lo)) lo = x;
+      if (total_less(hi, x)) hi = x;
+    }
+    mn[c] = lo;
+    mx[c] = hi;
+  }
+}
+
+/* Walk every (sequence, valid logical page, kv head) and write the page's
+ * min/max at its physical page: mn/mx are [num_phys][Hkv][d].  Entries of
+ * physical pages no row references are left untouched. */
+void okv_minmax_build(int dtype, int B, int Hkv, int d, int ps, int max_pages,
+                      const void *k_cache, const int32_t *block_table,
+                      const int32_t *context_lens, double *mn, double *mx) {
+  for (int b = 0; b < B; ++b) {
+    int len = context_lens[b];
+    int P = (len + ps - 1) / ps;
+    for (int p = 0; p < P; ++p) {
+      int n = len - p * ps < ps ? len - p * ps : ps;
+      int64_t phys = block_table[(int64_t)b * max_pages + p];
+      for (int kvh = 0; kvh < Hkv; ++kvh) {
+        int64_t off = ((phys * Hkv + kvh) * ps) * (int64_t)d;
+        int64_t o = (phys * Hkv + kvh) * (int64_t)d;
+        okv_page_minmax(dtype, d, n, k_cache, off, mn + o, mx + o);
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* page score: upper bound of q . k over the page                              */
+/* ------------------------------------------------------------------------- */
+
+/* sum_c max(q_c * mn_c, q_c * mx_c): for every key k in the page,
+ * q_c * k_c <= max(q_c * mn_c, q_c * mx_c) channel by channel, so the sum
+ * bounds q . k from above.  (KVDrive, section 2.2.) */
+double okv_page_score(int d, const double *q, const double *mn, const double *mx) {
+  double s = 0.0;
+  for (int c = 0; c < d; ++c) {
+    double a = q[c] * mn[c];
+    double b = q[c] * mx[c];
+    s += a > b ? a : b;
+  }
+  return s;
+}
+
+/* scores[b][h][p] for p < P_b, -inf for p >= P_b.  q is stored ([B][Hq][d]),
+ * mn/mx are the fp64 tables of okv_minmax_build. */
+void okv_scores(int dtype, int B, int Hq, int Hkv, int d, int ps, int max_pages, const void *q,
+                const double *mn, const double *mx, const int32_t *block_table,
+                const int32_t *context_lens, double *scores) {
+  int G = Hq / Hkv;
+  double *qd = (double *)malloc(sizeof(double) * d);
+  for (int b = 0; b < B; ++b) {
+    int P = (context_lens[b] + ps - 1) / ps;
+    for (int h = 0; h < Hq; ++h) {
+      int kvh = h / G;
+      for (int c = 0; c < d; ++c) qd[c] = okv_decode(dtype, q, ((int64_t)b * Hq + h) * d + c);
+      double *row = scores + ((int64_t)b * Hq + h) * max_pages;
+      for (int p = 0; p < max_pages; ++p) {
+        if (p >= P) {
+          row[p] = -INFINITY;
+          continue;
+        }
+        int64_t phys = block_table[(int64_t)b * max_pages + p];
+        int64_t o = (phys * Hkv + kvh) * (int64_t)d;
+        row[p] = okv_page_score(d, qd, mn + o, mx + o);
+      }
+    }
+  }
+  free(qd);
+}
+
+/* ------------------------------------------------------------------------- */
+/* top-K page selection                                                        */
+/* ------------------------------------------------------------------------- */
+
+static const double *g_sort_scores; /* comparator context (single-threaded use) */
+
+/* order: higher score first; equal scores -> lower page index first */
+static int by_score_desc(const void *pa, const void *pb) {
+  int a = *(const int *)pa, b = *(const int *)pb;
+  double sa = g_sort_scores[a], sb = g_sort_scores[b];
+  if (sa > sb) return -1;
+  if (sa < sb) return 1;
+  return (a > b) - (a < b);
+}
+
+static int by_index_asc(const void *pa, const void *pb) {
+  int a = *(const int *)pa, b = *(const int *)pb;
+  return (a > b) - (a < b);
+}
+
+/* The K pages with the largest scores among pages 0..P-1, returned in
+ * ascending page order; slots past min(K, P) hold -1.  (KVDrive, section 2.2:
+ * only the Top-K blocks per query are retrieved.) */
+void okv_topk_row(int P, const double *scores, int K, int32_t *out) {
+  int *order = (int *)malloc(sizeof(int) * (P > 0 ? P : 1));
+  for (int p = 0; p < P; ++p) order[p] = p;
+  g_sort_scores = scores;
+  qsort(order, P, sizeof(int), by_score_desc);
+  int keff = K < P ? K : P;
+  qsort(order, keff, sizeof(int), by_index_asc);
+  for (int i = 0; i < K; ++i) out[i] = i < keff ? order[i] : -1;
+  free(order);
+}
+
+void okv_topk(int B, int Hq, int ps, int max_pages, const int32_t *context_lens,
+              const double *scores, int K, int32_t *out) {
+  for (int b = 0; b < B; ++b) {
+    int P = (context_lens[b] + ps - 1) / ps;
+    for (int h = 0; h < Hq; ++h)
+      okv_topk_row(P, scores + ((int64_t)b * Hq + h) * max_pages, K,
+                   out + ((int64_t)b * Hq + h) * K);
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* attention of one query head over a set of pages                             */
+/* ------------------------------------------------------------------------- */
+
+/* out[c] = sum_t e^{z_t - m} v_t[c] / sum_t e^{z_t - m},  z_t = scale * q . k_t,
+ * m = max_t z_t, over the valid tokens of the listed logical pages (all pages
+ * 0..P-1 when pages == NULL; entries < 0 are skipped).  Two passes in fp64. */
+void okv_attention_row(int dtype, int Hkv, int d, int ps, int max_pages, double scale,
+                       const void *q, int64_t q_off, const void *k_cache, const void *v_cache,
+                       int kvh, const int32_t *bt_row, int len, const int32_t *pages,
+                       int npages, double *out) {
+  int P = (len + ps - 1) / ps;
+  if (pages == NULL) npages = P;
+  double *qd = (double *)malloc(sizeof(double) * d);
+  double *z = (double *)malloc(sizeof(double) * ((int64_t)npages * ps + 1));
+  for (int c = 0; c < d; ++c) qd[c] = okv_decode(dtype, q, q_off + c);
+
+  /* pass 1: logits of every taking-part token, and their maximum */
+  int64_t nt = 0;
+  double m = -INFINITY;
+  for (int i = 0; i < npages; ++i) {
+    int p = pages ? pages[i] : i;
+    if (p < 0 || p >= P) continue;
+    int n = len - p * ps < ps ? len - p * ps : ps;
+    int64_t phys = bt_row[p];
+    for (int t = 0; t < n; ++t) {
+      int64_t off = (((phys * Hkv + kvh) * ps) + t) * (int64_t)d;
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c) dot += qd[c] * okv_decode(dtype, k_cache, off + c);
+      z[nt] = scale * dot;
+      if (z[nt] > m) m = z[nt];
+      ++nt;
+    }
+  }
+
+  /* pass 2: normalised weighted sum of values */
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  double den = 0.0;
+  nt = 0;
+  for (int i = 0; i < npages; ++i) {
+    int p = pages ? pages[i] : i;
+    if (p < 0 || p >= P) continue;
+    int n = len - p * ps < ps ? len - p * ps : ps;
+    int64_t phys = bt_row[p];
+    for (int t = 0; t < n; ++t) {
+      int64_t off = (((phys * Hkv + kvh) * ps) + t) * (int64_t)d;
+      double w = exp(z[nt] - m);
+      den += w;
+      for (int c = 0; c < d; ++c) out[c] += w * okv_decode(dtype, v_cache, off + c);
+      ++nt;
+    }
+  }
+  for (int c = 0; c < d; ++c) out[c] = den > 0.0 ? out[c] / den : 0.0;
+  free(z);
+  free(qd);
+}
+
+/* Attention for a list of rows r = b * Hq + h (all B*Hq rows when rows ==
+ * NULL).  indices == NULL: dense over all pages; else indices is [B][Hq][K]
+ * (logical pages, -1 padded).  out is [B][Hq][d]; only listed rows are
+ * written.  nthreads > 0 sets the OpenMP thread count (ignored without it). */
+void okv_attention(int dtype, int B, int Hq, int Hkv, int d, int ps, int max_pages,
+                   double scale, const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_table, const int32_t *context_lens,
+                   const int32_t *indices, int K, const int32_t *rows, int nrows,
+                   int nthreads, double *out) {
+  int G = Hq / Hkv;
+  if (rows == NULL) nrows = B * Hq;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int i = 0; i < nrows; ++i) {
+    int r = rows ? rows[i] : i;
+    int b = r / Hq, h = r % Hq;
+    const int32_t *sel = indices ? indices + (int64_t)r * K : NULL;
+    okv_attention_row(dtype, Hkv, d, ps, max_pages, scale, q, (int64_t)r * d, k_cache, v_cache,
+                      h / G, block_table + (int64_t)b * max_pages, context_lens[b], sel,
+                      indices ? K : 0, out + (int64_t)r * d);
+  }
+}
+
+int okv_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
