@@ -1,0 +1,173 @@
+/*
+ * kvsparse.h -- C ABI of decode-phase attention over a paged KV cache with
+ * Quest-style page selection, for one GB300 (sm_103a) GPU.
+ *
+ * The path, per decode token and layer (KVDrive: A Holistic Multi-Tier KV
+ * Cache Management System for Long-Context LLM Inference, section 2.3 "KV
+ * cache offloading", steps (1)-(3); section 2.2 "Sparse attention" for the
+ * Quest index):
+ *   kv_page_minmax_build  -> per-page channel-wise key min/max (the index)
+ *   kv_page_score         -> q against the index: an upper bound on q.k
+ *   kv_topk_select        -> the K highest-scoring pages per query head
+ *   kv_sparse_decode_attn -> softmax attention over only those pages
+ *   kv_dense_decode_attn  -> the same over every page (Dual-Blade, "Background
+ *                            and key observations": decode reads all prior KV)
+ * K/V pages live in device memory (HBM) or in pinned host memory that the GPU
+ * reads in place, with no staging copy (DirectKV -- No Buffer, No Bottleneck:
+ * Efficient Zero-Copy KV Cache Offloading for Long-Context LLMs, core method 1
+ * "KV Cache Manager", core method 2 decode order).
+ *
+ * Conventions for every call:
+ *  - All pointers are plain addresses.  Device arrays are device pointers; for
+ *    KV_LOC_HOST_PINNED the K/V caches are host pointers from cudaHostAlloc
+ *    (or cudaHostRegister) that the device can map.  Everything else is always
+ *    in device memory.
+ *  - The caller owns and allocates every buffer (outputs and workspaces).  The
+ *    library allocates nothing, frees nothing and never synchronises, except
+ *    kv_device_status, which synchronises the given stream.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on it and write only their named outputs and
+ *    their workspace.
+ *  - Return value: KV_OK, or a negative kv_status.  Argument checks run on the
+ *    host before any launch; a call that fails them launches nothing.  Checks
+ *    on device-resident data (context lengths, block-table entries, selected
+ *    page ids) run inside the kernels: a bad entry is skipped and recorded in a
+ *    device status word that kv_device_status returns.
+ *  - Alignment: q, K/V caches, minmax, scores, out and workspaces 16 bytes;
+ *    int32 arrays 4 bytes.
+ *
+ * Shapes: B = batch, Hq = query heads, Hkv = kv heads (Hq % Hkv == 0,
+ * G = Hq / Hkv), d = head_dim (128), ps = page_size (16 or 64), maxP =
+ * max_pages_per_seq, N = num_phys_pages.  Sequence b holds context_lens[b]
+ * tokens in pages 0 .. P_b - 1, P_b = ceil(context_lens[b] / ps); the last page
+ * may be partial and only its first valid tokens take part anywhere.
+ *
+ * Layouts (row-major, innermost last):
+ *   q            [B][Hq][d]          dtype
+ *   k_cache      [N][Hkv][ps][d]     dtype   (v_cache the same)
+ *   block_table  [B][maxP]           int32   logical page -> physical page
+ *   context_lens [B]                 int32   1 <= len <= maxP * ps
+ *   minmax       [N][Hkv][2][d]      dtype   [..][0][c] = min, [..][1][c] = max
+ *   scores       [B][Hq][maxP]       float   -inf for p >= P_b
+ *   indices      [B][Hq][k]          int32   ascending logical pages, -1 padded
+ *   out          [B][Hq][d]          float
+ * Query head h reads kv head h / G.
+ */
+#ifndef KVSPARSE_H
+#define KVSPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { KV_F32 = 0, KV_F16 = 1, KV_BF16 = 2 } kv_dtype;
+typedef enum { KV_LOC_HBM = 0, KV_LOC_HOST_PINNED = 1 } kv_location;
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad shape, k < 1      */
+  KV_ERR_UNSUPPORTED = -2,    /* d != 128, ps not in {16, 64}, unknown dtype    */
+  KV_ERR_LOCATION = -3,       /* K/V memory does not match kv_loc               */
+  KV_ERR_WORKSPACE = -4,      /* workspace null or smaller than required        */
+  KV_ERR_CUDA = -5,           /* a CUDA runtime call or launch failed           */
+  KV_ERR_DEVICE_TIMEOUT = -6, /* a bounded device-side wait gave up             */
+  KV_ERR_BOUNDS = -7          /* device data out of range (len, page id)        */
+} kv_status;
+
+typedef struct {
+  int32_t batch;             /* B   >= 1                                      */
+  int32_t num_q_heads;       /* Hq  >= 1                                      */
+  int32_t num_kv_heads;      /* Hkv >= 1, divides Hq                          */
+  int32_t head_dim;          /* d, must be 128                                */
+  int32_t page_size;         /* ps, 16 or 64 tokens                           */
+  int32_t max_pages_per_seq; /* maxP >= 1                                     */
+  int64_t num_phys_pages;    /* N >= 1: pages in k_cache / v_cache / minmax   */
+  int32_t dtype;             /* kv_dtype of q, K, V and minmax                */
+  int32_t kv_loc;            /* kv_location of k_cache / v_cache              */
+} kv_shape;
+
+/* Index build.  For every sequence b and valid logical page p < P_b, and every
+ * kv head, writes the channel-wise minimum and maximum of the page's keys
+ * over its valid tokens into minmax[block_table[b][p]][kvh] (KVDrive, section
+ * 2.2: Quest keeps per-block channel-wise key min and max).  Exact: the
+ * outputs are elements of K, compared in IEEE totalOrder (so -0.0 < +0.0).
+ * Reads k_cache from kv_loc; minmax is in device memory.  Entries of physical
+ * pages no row references are not written.  A physical page shared by several
+ * rows must be full in each. */
+int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                         const int32_t *context_lens, void *minmax, void *stream);
+
+/* Page criticality (KVDrive, section 2.2): scores[b][h][p] =
+ * sum_c max(q_c * min_c, q_c * max_c) over the minmax entry of page
+ * block_table[b][p], kv head h / G -- an upper bound on q . k for every key of
+ * the page.  fp32 arithmetic (the products of 16-bit inputs are exact); no
+ * 1/sqrt(d) factor, since it does not change the ranking.  p >= P_b -> -inf. */
+int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
+                  const int32_t *block_table, const int32_t *context_lens, float *scores,
+                  void *stream);
+
+/* Bytes of workspace kv_topk_select needs for this shape and k (may be 0). */
+size_t kv_topk_workspace_bytes(const kv_shape *shape, int32_t k);
+
+/* Top-K selection (KVDrive, section 2.2: only the Top-K blocks per query are
+ * retrieved).  For each (b, h): the min(k, P_b) pages with the largest scores
+ * over p < P_b, ties to the lower page index, written ascending into
+ * indices[b][h][0 ..]; the remaining slots get -1.  -0.0 and +0.0 rank equal.
+ * workspace may be NULL when kv_topk_workspace_bytes returns 0. */
+int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
+                   int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Bytes of workspace the attention calls need for this shape on the current
+ * device; k = 0 for kv_dense_decode_attn, the selection size for
+ * kv_sparse_decode_attn.  Split-K partial results and the per-group union of
+ * selected pages live there. */
+size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k);
+
+/* Sparse decode attention (KVDrive, section 2.3 step (3); DirectKV, core
+ * method 2-3: the query and the output stay on chip and each K/V tile is read
+ * once, with a streaming softmax).  For each (b, h):
+ *   out[b][h] = sum_t softmax_t(scale * q . k_t) v_t
+ * over the valid tokens of the pages listed in indices[b][h][0 .. k) (entries
+ * < 0 skipped; ids >= P_b are a bounds error).  Pages selected by several
+ * heads of one GQA group are read once.  scale is typically 1/sqrt(d). */
+int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table,
+                          const int32_t *context_lens, const int32_t *indices, int32_t k,
+                          float scale, float *out, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* Dense decode attention: as kv_sparse_decode_attn over every page p < P_b
+ * (Dual-Blade, "Background and key observations"). */
+int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *block_table,
+                         const int32_t *context_lens, float scale, float *out, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: KV_OK, KV_ERR_DEVICE_TIMEOUT or KV_ERR_BOUNDS (the
+ * first error recorded since the last call), or KV_ERR_CUDA if the
+ * synchronisation itself failed. */
+int kv_device_status(void *stream);
+
+/* Static, NUL-terminated name of a kv_status value. */
+const char *kv_status_string(int status);
+
+/* Testing hook for the bounded device-side waits (failure detection without
+ * a GPU fault).  wait_limit_ns (1 ns .. 60 s; default 2 s) bounds every
+ * pipeline wait of the attention kernels; skip_page >= 0 makes the producer
+ * of every attention CTA leave its skip_page-th page unfilled, so the consumer
+ * waiting for it gives up after the limit, the call's kernels finish, and
+ * kv_device_status reports KV_ERR_DEVICE_TIMEOUT.  skip_page < 0 restores
+ * normal operation.  Process-wide; not for concurrent use with other calls.
+ * Returns KV_OK or KV_ERR_INVALID_ARG. */
+int kv_debug_config(int32_t skip_page, uint64_t wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVSPARSE_H */

@@ -1,0 +1,437 @@
+// kv_api.cu -- the extern "C" boundary: argument checks, launch planning and
+// launches for the paged decode-attention path.  Declarations and contracts
+// are in include/kvsparse.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kv_internal.cuh"
+
+namespace kvs {
+cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
+                             const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
+                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+}  // namespace kvs
+
+namespace {
+
+using namespace kvs;
+
+// device status word (one per device, zero-initialised at module load)
+__device__ int g_kv_status;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int *> g_status_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+// testing hooks (kv_debug_config)
+std::atomic<int> g_debug_skip_page{-1};
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+int *status_ptr(int dev) {
+  int *p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void *addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_kv_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  g_status_ptr[dev].store(static_cast<int *>(addr), std::memory_order_release);
+  return static_cast<int *>(addr);
+}
+
+int sm_count(int dev) {
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 152;
+  }
+  g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool al16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
+bool al4(const void *p) { return p && ((uintptr_t)p & 3u) == 0; }
+int elem_bytes(int dtype) { return dtype == KV_F32 ? 4 : 2; }
+
+int check_shape(const kv_shape *s) {
+  if (!s) return KV_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 ||
+      s->num_q_heads % s->num_kv_heads != 0 || s->max_pages_per_seq < 1 ||
+      s->num_phys_pages < 1)
+    return KV_ERR_INVALID_ARG;
+  if (s->kv_loc != KV_LOC_HBM && s->kv_loc != KV_LOC_HOST_PINNED) return KV_ERR_INVALID_ARG;
+  if (s->dtype != KV_F32 && s->dtype != KV_F16 && s->dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
+  if (s->head_dim != kHeadDim) return KV_ERR_UNSUPPORTED;
+  if (s->page_size != 16 && s->page_size != 64) return KV_ERR_UNSUPPORTED;
+  // index arithmetic limits: tokens per row and K/V rows fit in int32
+  if ((long long)s->max_pages_per_seq * s->page_size > INT_MAX) return KV_ERR_UNSUPPORTED;
+  if (s->num_phys_pages * (long long)s->num_kv_heads * s->page_size > INT_MAX)
+    return KV_ERR_UNSUPPORTED;
+  if ((long long)s->batch * s->num_q_heads > INT_MAX) return KV_ERR_UNSUPPORTED;
+  return KV_OK;
+}
+
+// Device-visible address of a K or V cache, checked against kv_loc.
+int resolve_kv(const kv_shape *s, const void *p, const void **dev_ptr) {
+  if (!al16(p)) return KV_ERR_INVALID_ARG;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  if (s->kv_loc == KV_LOC_HBM) {
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+      return KV_ERR_LOCATION;
+    *dev_ptr = p;
+  } else {
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return KV_ERR_LOCATION;
+    *dev_ptr = at.devicePointer;
+  }
+  return KV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// attention launch plan: head chunking, split count, pipeline depth, workspace
+// ---------------------------------------------------------------------------
+struct Plan {
+  int gc = 1, nchunk = 1, groups = 1;
+  bool mma = false;
+  int S = 1, umax = 0, nstages = 4;
+  size_t smem = 0;
+  size_t off_part_o = 0, off_part_ml = 0, off_upages = 0, off_umasks = 0, off_ucount = 0;
+  size_t total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Plan make_plan(const kv_shape *s, int k, int sms) {
+  Plan pl;
+  const int G = s->num_q_heads / s->num_kv_heads;
+  if (s->dtype == KV_F32) {
+    pl.gc = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  } else if (G % 8 == 0) {
+    pl.gc = 8;
+    pl.mma = true;
+  } else if (G % 4 == 0) {
+    pl.gc = 4;
+    pl.mma = true;
+  } else {
+    pl.gc = (G % 2 == 0) ? 2 : 1;
+  }
+  pl.nchunk = G / pl.gc;
+  pl.groups = s->num_kv_heads * pl.nchunk;
+  const int stage = 2 * s->page_size * kHeadDim * elem_bytes(s->dtype);
+  int ns = (64 * 1024 / stage) / kConsumerWarps * kConsumerWarps;
+  if (ns < kConsumerWarps) ns = kConsumerWarps;
+  if (ns > 16) ns = 16;
+  pl.nstages = ns;
+  pl.smem = 1024 + 4096 + (size_t)ns * stage;
+  int per_sm = (int)((228 * 1024) / (pl.smem + 1024));
+  if (per_sm > 2048 / kAttnThreads) per_sm = 2048 / kAttnThreads;
+  if (per_sm < 1) per_sm = 1;
+  const long long slots = (long long)sms * per_sm;
+  const long long maxP = s->max_pages_per_seq;
+  const long long work = k > 0 ? std::min<long long>((long long)pl.gc * k, maxP) : maxP;
+  const long long units = (long long)s->batch * pl.groups;
+  // split count minimising (waves x pages per CTA), with ~4 pages of fixed
+  // cost per CTA (prologue, pipeline fill, merge)
+  long long best = LLONG_MAX;
+  int bestS = 1;
+  const int smax = (int)std::min<long long>(1024, std::max<long long>(1, (work + 3) / 4));
+  for (int S = 1; S <= smax; ++S) {
+    const long long waves = (units * S + slots - 1) / slots;
+    const long long cost = waves * ((work + S - 1) / S + 4);
+    if (cost < best) {
+      best = cost;
+      bestS = S;
+    }
+  }
+  pl.S = bestS;
+  pl.umax = k > 0 ? (int)work : 0;
+  size_t off = 0;
+  const size_t rows = (size_t)s->batch * s->num_q_heads;
+  if (pl.S > 1) {
+    pl.off_part_o = off;
+    off = align256(off + (size_t)pl.S * rows * kHeadDim * 4);
+    pl.off_part_ml = off;
+    off = align256(off + (size_t)pl.S * rows * 2 * 4);
+  }
+  if (k > 0) {
+    const size_t ng = (size_t)s->batch * pl.groups;
+    pl.off_upages = off;
+    off = align256(off + ng * pl.umax * 4);
+    pl.off_umasks = off;
+    off = align256(off + ng * pl.umax * 4);
+    pl.off_ucount = off;
+    off = align256(off + ng * 4);
+  }
+  pl.total = off;
+  return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D view [rows = N * Hkv * ps][128 elements]; box = one 128-byte slab x ps
+// rows, 128-byte swizzle (matching the kernel's shared-memory layout).
+int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
+  auto fn = encode_fn();
+  if (!fn) return KV_ERR_CUDA;
+  const CUtensorMapDataType dt = s->dtype == KV_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : s->dtype == KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int eb = elem_bytes(s->dtype);
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim,
+                        (cuuint64_t)(s->num_phys_pages * s->num_kv_heads * s->page_size)};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * eb};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)s->page_size};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
+}
+
+int attn_common(const kv_shape *s, const void *q, const void *k_cache, const void *v_cache,
+                const int32_t *bt, const int32_t *ctx, const int32_t *indices, int32_t k,
+                float scale, float *out, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!al16(q) || !al16(out) || !al4(bt) || !al4(ctx)) return KV_ERR_INVALID_ARG;
+  if (indices && (!al4(indices) || k < 1)) return KV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+  if (indices && (long long)(s->max_pages_per_seq + 3) / 4 * 4 > 200 * 1024)
+    return KV_ERR_UNSUPPORTED;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  const void *kd = nullptr, *vd = nullptr;
+  if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
+  if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
+  const Plan pl = make_plan(s, indices ? k : 0, sm_count(dev));
+  if (pl.total > 0 && (ws == nullptr || ws_bytes < pl.total || !al16(ws))) return KV_ERR_WORKSPACE;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(ws);
+
+  AttnArgs a{};
+  a.q = q;
+  a.k = kd;
+  a.v = vd;
+  a.block_table = bt;
+  a.context_lens = ctx;
+  a.out = out;
+  a.status = status;
+  a.nphys = s->num_phys_pages;
+  a.B = s->batch;
+  a.Hq = s->num_q_heads;
+  a.Hkv = s->num_kv_heads;
+  a.G = s->num_q_heads / s->num_kv_heads;
+  a.ps = s->page_size;
+  a.maxP = s->max_pages_per_seq;
+  a.nchunk = pl.nchunk;
+  a.num_splits = pl.S;
+  a.nstages = pl.nstages;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.debug_skip_page = g_debug_skip_page.load();
+  if (pl.S > 1) {
+    a.part_o = reinterpret_cast<float *>(w + pl.off_part_o);
+    a.part_ml = reinterpret_cast<float *>(w + pl.off_part_ml);
+  }
+  if (indices) {
+    a.union_pages = reinterpret_cast<int32_t *>(w + pl.off_upages);
+    a.union_masks = reinterpret_cast<uint32_t *>(w + pl.off_umasks);
+    a.union_count = reinterpret_cast<int32_t *>(w + pl.off_ucount);
+    a.umax = pl.umax;
+    cudaError_t e = launch_union(indices, ctx, s->batch, s->num_q_heads, s->num_kv_heads, pl.gc,
+                                 s->page_size, s->max_pages_per_seq, k, pl.umax,
+                                 const_cast<int32_t *>(a.union_pages),
+                                 const_cast<uint32_t *>(a.union_masks),
+                                 const_cast<int32_t *>(a.union_count), status, st);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+  }
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof tk);
+  memset(&tv, 0, sizeof tv);
+  a.use_tma = s->kv_loc == KV_LOC_HBM ? 1 : 0;
+  if (a.use_tma) {
+    if ((rc = make_kv_map(s, kd, &tk)) != KV_OK) return rc;
+    if ((rc = make_kv_map(s, vd, &tv)) != KV_OK) return rc;
+  }
+  dim3 grid(pl.S, pl.groups, s->batch);
+  cudaError_t e = pl.mma ? launch_attn_mma(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st)
+                         : launch_attn_core(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st);
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  if (pl.S > 1) {
+    e = launch_combine(a.part_o, a.part_ml, out, pl.S, s->batch, s->num_q_heads, st);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                         const int32_t *context_lens, void *minmax, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!al16(minmax) || !al4(block_table) || !al4(context_lens)) return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  const void *kd = nullptr;
+  if ((rc = resolve_kv(shape, k_cache, &kd)) != KV_OK) return rc;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_minmax_build(shape->dtype, kd, block_table, context_lens, minmax,
+                                      shape->batch, shape->num_kv_heads, shape->page_size,
+                                      shape->max_pages_per_seq, shape->num_phys_pages, status,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
+                  const int32_t *block_table, const int32_t *context_lens, float *scores,
+                  void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!al16(q) || !al16(minmax) || !al16(scores) || !al4(block_table) || !al4(context_lens))
+    return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_page_score(shape->dtype, q, minmax, block_table, context_lens, scores,
+                                    shape->batch, shape->num_q_heads, shape->num_kv_heads,
+                                    shape->page_size, shape->max_pages_per_seq,
+                                    shape->num_phys_pages, status,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+size_t kv_topk_workspace_bytes(const kv_shape *shape, int32_t k) {
+  (void)shape;
+  (void)k;
+  return 0;
+}
+
+int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
+                   int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (k < 1 || !al16(scores) || !al4(indices) || !al4(context_lens)) return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_topk(scores, context_lens, shape->batch, shape->num_q_heads,
+                              shape->page_size, shape->max_pages_per_seq, k, indices, status,
+                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k) {
+  if (check_shape(shape) != KV_OK || k < 0) return 0;
+  const int dev = current_device();
+  const int sms = dev >= 0 ? sm_count(dev) : 152;
+  return make_plan(shape, k, sms).total;
+}
+
+int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table,
+                          const int32_t *context_lens, const int32_t *indices, int32_t k,
+                          float scale, float *out, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+  if (!indices) return KV_ERR_INVALID_ARG;
+  return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, indices, k, scale, out,
+                     workspace, workspace_bytes, stream);
+}
+
+int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *block_table,
+                         const int32_t *context_lens, float scale, float *out, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, nullptr, 0, scale,
+                     out, workspace, workspace_bytes, stream);
+}
+
+int kv_device_status(void *stream) {
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  int *p = status_ptr(dev);
+  if (!p) return KV_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return KV_ERR_CUDA;
+    }
+  }
+  return v;
+}
+
+const char *kv_status_string(int status) {
+  switch (status) {
+    case KV_OK: return "KV_OK";
+    case KV_ERR_INVALID_ARG: return "KV_ERR_INVALID_ARG";
+    case KV_ERR_UNSUPPORTED: return "KV_ERR_UNSUPPORTED";
+    case KV_ERR_LOCATION: return "KV_ERR_LOCATION";
+    case KV_ERR_WORKSPACE: return "KV_ERR_WORKSPACE";
+    case KV_ERR_CUDA: return "KV_ERR_CUDA";
+    case KV_ERR_DEVICE_TIMEOUT: return "KV_ERR_DEVICE_TIMEOUT";
+    case KV_ERR_BOUNDS: return "KV_ERR_BOUNDS";
+    default: return "KV_ERR_UNKNOWN";
+  }
+}
+
+int kv_debug_config(int32_t skip_page, uint64_t wait_limit_ns) {
+  if (wait_limit_ns == 0 || wait_limit_ns > 60000000000ull) return KV_ERR_INVALID_ARG;
+  g_debug_skip_page.store(skip_page < 0 ? -1 : skip_page);
+  g_wait_limit_ns.store(wait_limit_ns);
+  return KV_OK;
+}
+
+}  // extern "C"

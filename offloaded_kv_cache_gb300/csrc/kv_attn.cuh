@@ -1,0 +1,560 @@
+// kv_attn.cuh -- paged decode attention (dense or over selected pages) for
+// sm_103a: one producer warp streams K/V pages into a ring of shared-memory
+// stages, consumer warps run a streaming softmax over them.
+//
+// What it computes, per query head h of sequence b:
+//   out = sum_t softmax_t(scale * q . k_t) v_t
+// over the valid tokens of every page (dense) or of the pages head h selected
+// (sparse).  Sources: KVDrive (A Holistic Multi-Tier KV Cache Management
+// System for Long-Context LLM Inference), section 2.3 step (3), attention over
+// the selected entries; DirectKV (No Buffer, No Bottleneck: Efficient
+// Zero-Copy KV Cache Offloading for Long-Context LLMs), core method 2-3: in
+// decode the query and the output stay on chip, every K/V tile is scanned
+// once, a producer warp prefetches the next tile while consumers compute the
+// current one, and the softmax is streamed.
+//
+// Design on GB300:
+//  * CTA = (split, kv head x head chunk, sequence).  All GC query heads of
+//    the chunk share one pass over the K/V bytes; in the sparse path the CTA
+//    walks the union of their selected pages once and masks per head.
+//  * Stage = one page of one kv head: K then V, each `ps` rows x 128 elements,
+//    stored as 128-byte slabs in the 128B-swizzled layout, so ldmatrix and
+//    16-byte shared loads are bank-conflict free.
+//  * Producer: HBM -> TMA tiled loads (cp.async.bulk.tensor) completing on
+//    a full mbarrier with a transaction count; pinned host memory -> 16-byte
+//    cp.async issued by the 32 producer lanes (same layout, same barrier).
+//    Stage s always belongs to consumer warp s % kConsumerWarps, which arrives
+//    on the stage's empty mbarrier when done.
+//  * Consumers: GQA groups of >= 4 heads on 16-bit data use mma.sync
+//    m16n8k16 (tokens x heads tile of q.K^T, then V^T . P^T with P split in a
+//    high and a low 16-bit part so the weights keep ~16 bits); otherwise
+//    CUDA-core FMAs with lanes over (token, slab) for q.k and over channels
+//    for p.v.  Max/sum reductions are warp shuffles.
+//  * Every mbarrier wait is bounded in wall time; a wait that gives up
+//    records KV_ERR_DEVICE_TIMEOUT and the CTA winds down.
+#pragma once
+
+#include "kv_internal.cuh"
+
+namespace kvs {
+
+constexpr int kMaxStages = 16;
+constexpr int kHeaderBytes = 4096;  // barriers + per-CTA q / weight buffers
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, __nv_bfloat16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, __half) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (hi, lo) 16-bit pairs with x ~= hi + lo to ~16 significant bits
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo,
+                                           __nv_bfloat16) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo,
+                                           __half) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// per-CTA page list: the j-th page of this CTA's share
+struct PageRange {
+  int lo, n;  // first index into the (dense or union) list, count
+};
+
+template <class T, int GC, bool MMA>
+__global__ void __launch_bounds__(kAttnThreads)
+    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv) {
+  constexpr int SL = (int)sizeof(T);        // 128-byte slabs per 128-element row
+  constexpr int EPS = 128 / (int)sizeof(T); // elements per slab
+  constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+  constexpr int TP = 32 / SL;               // tokens per CUDA-core pass
+  constexpr int QSTR = EPS + 4;             // padded q slab stride (floats)
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + kMaxStages;
+  float *q_s = reinterpret_cast<float *>(smem + 256);  // CUDA core: [GC][SL][QSTR]
+  float *pbuf = q_s + GC * SL * QSTR;                  // CUDA core: [warps][GC][TP]
+  uint8_t *stages = smem + kHeaderBytes;
+
+  const int ps = a.ps;
+  const int slab_bytes = ps * 128;
+  const int kv_off = ps * 128 * SL;  // V follows K inside a stage
+  const int stage_bytes = 2 * kv_off;
+  const int NS = a.nstages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, grp = blockIdx.y, b = blockIdx.z;
+  const int kvh = grp / a.nchunk, chunk = grp % a.nchunk;
+  const int head0 = kvh * a.G + chunk * GC;
+  const bool sparse = a.union_pages != nullptr;
+  const long long gidx = (long long)b * gridDim.y + grp;
+
+  // ---- this CTA's share of the page list ---------------------------------
+  const int len = a.context_lens[b];
+  const bool bad_len = len < 1 || len > a.maxP * ps;
+  const int P = bad_len ? 0 : (len + ps - 1) / ps;
+  int total = P;
+  if (sparse) total = bad_len ? 0 : min(a.union_count[gidx], a.umax);
+  const int per = (total + a.num_splits - 1) / a.num_splits;
+  PageRange rng;
+  rng.lo = min(total, split * per);
+  rng.n = max(0, min(total, rng.lo + per) - rng.lo);
+  if (bad_len && split == 0 && threadIdx.x == 0 && chunk == 0) flag_error(a.status, KV_ERR_BOUNDS);
+
+  // logical page, head mask and physical page of list entry j (-1 phys = bad)
+  auto page_of = [&](int j, int &p, uint32_t &mask, long long &phys) {
+    const int e = rng.lo + j;
+    if (sparse) {
+      p = a.union_pages[gidx * a.umax + e];
+      mask = a.union_masks[gidx * a.umax + e];
+    } else {
+      p = e;
+      mask = (1u << GC) - 1u;
+    }
+    phys = -1;
+    if (p >= 0 && p < P) {
+      const long long ph = a.block_table[(long long)b * a.maxP + p];
+      if (ph >= 0 && ph < a.nphys) phys = ph;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full[s]), a.use_tma ? 1u : 32u);
+      mbar_init(smem_u32(&empty[s]), 1u);
+    }
+    fence_mbar_init();
+  }
+  if constexpr (!MMA) {
+    for (int i = threadIdx.x; i < GC * kHeadDim; i += blockDim.x) {
+      const int g = i / kHeadDim, c = i % kHeadDim;
+      const T *qrow = static_cast<const T *>(a.q) + ((long long)b * a.Hq + head0 + g) * kHeadDim;
+      q_s[(g * SL + c / EPS) * QSTR + (c % EPS)] = Elem<T>::to_f32(qrow[c]);
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ======================= producer =====================================
+    int issued = 0;
+    bool ok = true;
+    if (a.use_tma) {
+      if (lane == 0) {
+        for (int j = 0; j < rng.n; ++j) {
+          const int s = j % NS;
+          if (j >= NS && !mbar_wait(smem_u32(&empty[s]), ((j / NS) - 1) & 1, a.wait_limit_ns)) {
+            flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+          }
+          int p;
+          uint32_t mask;
+          long long phys;
+          page_of(j, p, mask, phys);
+          if (phys < 0) phys = 0;  // still fill the stage; the consumer skips it
+          issued = j + 1;
+          if (j == a.debug_skip_page) continue;
+          const uint32_t fb = smem_u32(&full[s]);
+          const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
+          const int row0 = (int)((phys * a.Hkv + kvh) * ps);
+          mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+#pragma unroll
+          for (int h = 0; h < SL; ++h) tma_load_2d(dst + h * slab_bytes, &tk, h * EPS, row0, fb);
+#pragma unroll
+          for (int h = 0; h < SL; ++h)
+            tma_load_2d(dst + kv_off + h * slab_bytes, &tv, h * EPS, row0, fb);
+        }
+      }
+    } else {
+      const char *kbase = static_cast<const char *>(a.k);
+      const char *vbase = static_cast<const char *>(a.v);
+      const int chunks = ps * SL * 8;  // 16-byte chunks per K (or V) page
+      for (int j = 0; j < rng.n; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(smem_u32(&empty[s]), ((j / NS) - 1) & 1, a.wait_limit_ns)) {
+          if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
+          ok = false;
+          break;
+        }
+        int p;
+        uint32_t mask;
+        long long phys;
+        page_of(j, p, mask, phys);
+        if (phys < 0) phys = 0;
+        issued = j + 1;
+        if (j == a.debug_skip_page) continue;
+        const size_t src0 = (size_t)((phys * a.Hkv + kvh) * ps) * (SL * 128);
+        const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
+        for (int i = lane; i < chunks; i += 32) {
+          const int row = i / (SL * 8), rem = i % (SL * 8);
+          const int h = rem >> 3, c = rem & 7;
+          const size_t off = src0 + (size_t)row * (SL * 128) + rem * 16;
+          const uint32_t d = dst + h * slab_bytes + swz(row, c);
+          cp_async16(d, kbase + off);
+          cp_async16(d + kv_off, vbase + off);
+        }
+        cp_async_arrive_noinc(smem_u32(&full[s]));
+      }
+    }
+    (void)ok;
+    // Drain: wait (bounded) until the last fill of every stage has landed, so
+    // no asynchronous copy targets this CTA's shared memory after it moves on.
+    if (lane == 0 || !a.use_tma) {
+      for (int s = 0; s < NS && s < issued; ++s) {
+        int jl = s + ((issued - 1 - s) / NS) * NS;  // last page issued into stage s
+        if (jl == a.debug_skip_page) jl -= NS;
+        if (jl < 0) continue;
+        if (!mbar_wait(smem_u32(&full[s]), (jl / NS) & 1, a.wait_limit_ns))
+          flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ======================= consumers ======================================
+  const int cw = warp - 1;
+  float m_run[MMA ? 2 : GC], l_run[MMA ? 2 : GC];
+  float acc[MMA ? 8 : GC][4];
+#pragma unroll
+  for (int i = 0; i < (MMA ? 2 : GC); ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < (MMA ? 8 : GC); ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  const int gid = lane >> 2, tig = lane & 3;
+  if (warp > 0) {
+    uint32_t qb[8][2];
+    if constexpr (MMA) {
+      // q as the B operand (k = channel, n = head): b0 = channels 16j+2tig..+1,
+      // b1 = channels 16j+8+2tig..+1 of head gid; heads >= GC are zero.
+#pragma unroll
+      for (int j8 = 0; j8 < 8; ++j8) {
+        qb[j8][0] = qb[j8][1] = 0u;
+        if (gid < GC) {
+          const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+              static_cast<const T *>(a.q) + ((long long)b * a.Hq + head0 + gid) * kHeadDim);
+          qb[j8][0] = qrow[(16 * j8 + 2 * tig) >> 1];
+          qb[j8][1] = qrow[(16 * j8 + 8 + 2 * tig) >> 1];
+        }
+      }
+    }
+    const float sl = a.scale_log2;
+#pragma unroll 1
+    for (int j = cw; j < rng.n; j += kConsumerWarps) {
+      const int s = j % NS;
+      if (!mbar_wait(smem_u32(&full[s]), (j / NS) & 1, a.wait_limit_ns)) {
+        if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      int p;
+      uint32_t msk;
+      long long phys;
+      page_of(j, p, msk, phys);
+      int nv = 0;
+      if (phys >= 0) {
+        nv = min(ps, len - p * ps);
+      } else if (lane == 0) {
+        flag_error(a.status, KV_ERR_BOUNDS);
+      }
+      uint8_t *st = stages + (size_t)s * stage_bytes;
+      if constexpr (MMA) {
+        const uint32_t kb = smem_u32(st), vb = kb + kv_off;
+        if (nv > 0 && nv < ps) {
+          // zero V rows past the last valid token of the 16-token tile they
+          // share with valid ones (P is 0 there, but 0 * NaN would not be)
+          const int hi_row = min(ps, (nv + 15) & ~15);
+          for (int i = lane; i < (hi_row - nv) * SL * 8; i += 32) {
+            const int row = nv + i / (SL * 8), rem = i % (SL * 8);
+            *reinterpret_cast<uint4 *>(st + kv_off + (rem >> 3) * slab_bytes + swz(row, rem & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+#pragma unroll 1
+        for (int sub = 0; sub * 16 < nv; ++sub) {
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int tok = sub * 16 + r;
+#pragma unroll
+            for (int j8 = 0; j8 < 8; ++j8) {
+              const int ch = 2 * j8 + (lane >> 4);
+              uint32_t af[4];
+              ldsm_x4(kb + (ch >> 3) * slab_bytes + swz(tok, ch & 7), af);
+              mma16816(c, af, qb[j8][0], qb[j8][1], T());
+            }
+          }
+          const int t0 = sub * 16 + gid, t1 = t0 + 8;
+          const bool v0 = t0 < nv, v1 = t1 < nv;
+          const bool s0 = (msk >> (2 * tig)) & 1u, s1 = (msk >> (2 * tig + 1)) & 1u;
+          const float z00 = (v0 && s0) ? c[0] * sl : -INFINITY;
+          const float z01 = (v0 && s1) ? c[1] * sl : -INFINITY;
+          const float z10 = (v1 && s0) ? c[2] * sl : -INFINITY;
+          const float z11 = (v1 && s1) ? c[3] * sl : -INFINITY;
+          float tm0 = fmaxf(z00, z10), tm1 = fmaxf(z01, z11);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            tm0 = fmaxf(tm0, __shfl_xor_sync(0xFFFFFFFFu, tm0, off));
+            tm1 = fmaxf(tm1, __shfl_xor_sync(0xFFFFFFFFu, tm1, off));
+          }
+          const float mn0 = fmaxf(m_run[0], tm0), mn1 = fmaxf(m_run[1], tm1);
+          const float bs0 = mn0 == -INFINITY ? 0.f : mn0;
+          const float bs1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = ex2(m_run[0] - bs0), al1 = ex2(m_run[1] - bs1);
+          const float p00 = ex2(z00 - bs0), p10 = ex2(z10 - bs0);
+          const float p01 = ex2(z01 - bs1), p11 = ex2(z11 - bs1);
+          l_run[0] = fmaf(l_run[0], al0, p00 + p10);
+          l_run[1] = fmaf(l_run[1], al1, p01 + p11);
+          m_run[0] = mn0;
+          m_run[1] = mn1;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            acc[mt][0] *= al0; acc[mt][2] *= al0;
+            acc[mt][1] *= al1; acc[mt][3] *= al1;
+          }
+          // P^T as the B operand (k = token, n = head) via 8x8 transposes
+          uint32_t x0h, x0l, x1h, x1l;
+          split_pack(p00, p01, x0h, x0l, T());
+          split_pack(p10, p11, x1h, x1l, T());
+          const uint32_t bh0 = movm_t(x0h), bh1 = movm_t(x1h);
+          const uint32_t bl0 = movm_t(x0l), bl1 = movm_t(x1l);
+          {
+            const int mi = lane >> 3;
+            const int tok = sub * 16 + (lane & 7) + (mi >> 1) * 8;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              const int ch = 2 * mt + (mi & 1);
+              uint32_t af[4];
+              ldsm_x4_t(vb + (ch >> 3) * slab_bytes + swz(tok, ch & 7), af);
+              mma16816(acc[mt], af, bh0, bh1, T());
+              mma16816(acc[mt], af, bl0, bl1, T());
+            }
+          }
+        }
+        if (nv > 0 && nv < ps) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      } else {
+        // ---- CUDA-core consumer ----
+        const int tt = lane / SL, hh = lane % SL;
+        float *pb = pbuf + cw * GC * TP;
+        // this lane's 4 output channels 4*lane .. 4*lane+3 inside a V row
+        const int vslab = (4 * lane * SL) / 128;
+        const int vbyte = (4 * lane * SL) % 128;
+        const uint8_t *kst = st;
+        const uint8_t *vst = st + kv_off + vslab * slab_bytes;
+#pragma unroll 1
+        for (int pass = 0; pass * TP < nv; ++pass) {
+          const int t = pass * TP + tt;
+          float dot[GC];
+#pragma unroll
+          for (int g = 0; g < GC; ++g) dot[g] = 0.f;
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int lc = (c8 + hh * (8 / SL)) & 7;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(kst + hh * slab_bytes + swz(t, lc));
+            float kf[EPC];
+            if constexpr (SL == 2) {
+              const float2 f0 = unpack2(kw.x, T()), f1 = unpack2(kw.y, T());
+              const float2 f2 = unpack2(kw.z, T()), f3 = unpack2(kw.w, T());
+              kf[0] = f0.x; kf[1] = f0.y; kf[2] = f1.x; kf[3] = f1.y;
+              kf[4] = f2.x; kf[5] = f2.y; kf[6] = f3.x; kf[7] = f3.y;
+            } else {
+              kf[0] = __uint_as_float(kw.x); kf[1] = __uint_as_float(kw.y);
+              kf[2] = __uint_as_float(kw.z); kf[3] = __uint_as_float(kw.w);
+            }
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+              const float4 *qp =
+                  reinterpret_cast<const float4 *>(q_s + (g * SL + hh) * QSTR + lc * EPC);
+#pragma unroll
+              for (int e4 = 0; e4 < EPC / 4; ++e4) {
+                const float4 qv = qp[e4];
+                dot[g] = fmaf(qv.x, kf[4 * e4 + 0], dot[g]);
+                dot[g] = fmaf(qv.y, kf[4 * e4 + 1], dot[g]);
+                dot[g] = fmaf(qv.z, kf[4 * e4 + 2], dot[g]);
+                dot[g] = fmaf(qv.w, kf[4 * e4 + 3], dot[g]);
+              }
+            }
+          }
+          const bool valid = t < nv;
+#pragma unroll
+          for (int g = 0; g < GC; ++g) {
+#pragma unroll
+            for (int off = 1; off < SL; off <<= 1)
+              dot[g] += __shfl_xor_sync(0xFFFFFFFFu, dot[g], off);
+            const float z = (valid && ((msk >> g) & 1u)) ? dot[g] * sl : -INFINITY;
+            float tm = z;
+#pragma unroll
+            for (int off = SL; off < 32; off <<= 1)
+              tm = fmaxf(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, off));
+            const float mn = fmaxf(m_run[g], tm);
+            const float bs = mn == -INFINITY ? 0.f : mn;
+            const float al = ex2(m_run[g] - bs);
+            const float pz = ex2(z - bs);
+            l_run[g] = fmaf(l_run[g], al, hh == 0 ? pz : 0.f);
+            acc[g][0] *= al; acc[g][1] *= al; acc[g][2] *= al; acc[g][3] *= al;
+            m_run[g] = mn;
+            if (hh == 0) pb[g * TP + tt] = pz;
+          }
+          __syncwarp();
+          const int ntok = min(TP, nv - pass * TP);
+#pragma unroll 4
+          for (int tk2 = 0; tk2 < ntok; ++tk2) {
+            const int row = pass * TP + tk2;
+            float vv[4];
+            if constexpr (SL == 2) {
+              const int chk = vbyte >> 4;
+              const uint2 w = *reinterpret_cast<const uint2 *>(vst + swz(row, chk) + (vbyte & 15));
+              const float2 f0 = unpack2(w.x, T()), f1 = unpack2(w.y, T());
+              vv[0] = f0.x; vv[1] = f0.y; vv[2] = f1.x; vv[3] = f1.y;
+            } else {
+              const float4 w = *reinterpret_cast<const float4 *>(vst + swz(row, vbyte >> 4));
+              vv[0] = w.x; vv[1] = w.y; vv[2] = w.z; vv[3] = w.w;
+            }
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+              const float pz = pb[g * TP + tk2];
+              acc[g][0] = fmaf(pz, vv[0], acc[g][0]);
+              acc[g][1] = fmaf(pz, vv[1], acc[g][1]);
+              acc[g][2] = fmaf(pz, vv[2], acc[g][2]);
+              acc[g][3] = fmaf(pz, vv[3], acc[g][3]);
+            }
+          }
+          __syncwarp();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+  }
+
+  // ======================= merge the consumer warps =======================
+  __syncthreads();  // every stage is consumed (or abandoned): reuse the ring
+  float *mw = reinterpret_cast<float *>(stages);  // [warps][GC]
+  float *lw = mw + kConsumerWarps * GC;           // [warps][GC]
+  float *ow = lw + kConsumerWarps * GC;           // [warps][GC][128]
+  if (warp > 0) {
+    if constexpr (MMA) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1)
+          l_run[i] += __shfl_xor_sync(0xFFFFFFFFu, l_run[i], off);
+      const int h0 = 2 * tig, h1 = h0 + 1;
+      if (gid == 0) {
+        if (h0 < GC) { mw[cw * GC + h0] = m_run[0]; lw[cw * GC + h0] = l_run[0]; }
+        if (h1 < GC) { mw[cw * GC + h1] = m_run[1]; lw[cw * GC + h1] = l_run[1]; }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d0 = 16 * mt + gid, d1 = d0 + 8;
+        if (h0 < GC) {
+          ow[(cw * GC + h0) * kHeadDim + d0] = acc[mt][0];
+          ow[(cw * GC + h0) * kHeadDim + d1] = acc[mt][2];
+        }
+        if (h1 < GC) {
+          ow[(cw * GC + h1) * kHeadDim + d0] = acc[mt][1];
+          ow[(cw * GC + h1) * kHeadDim + d1] = acc[mt][3];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < GC; ++g) {
+        float l = l_run[g];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
+        if (lane == 0) { mw[cw * GC + g] = m_run[g]; lw[cw * GC + g] = l; }
+        float4 o4 = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+        *reinterpret_cast<float4 *>(ow + (cw * GC + g) * kHeadDim + 4 * lane) = o4;
+      }
+    }
+  }
+  __syncthreads();
+  const long long rows = (long long)a.B * a.Hq;
+  for (int i = threadIdx.x; i < GC * kHeadDim; i += blockDim.x) {
+    const int g = i / kHeadDim, dd = i % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * GC + g]);
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float m = mw[w * GC + g];
+        const float f = m == -INFINITY ? 0.f : ex2(m - M);
+        o = fmaf(f, ow[(w * GC + g) * kHeadDim + dd], o);
+        l = fmaf(f, lw[w * GC + g], l);
+      }
+    }
+    const long long r = (long long)b * a.Hq + head0 + g;
+    if (a.num_splits == 1) {
+      a.out[r * kHeadDim + dd] = l > 0.f ? o / l : 0.f;
+    } else {
+      a.part_o[((long long)split * rows + r) * kHeadDim + dd] = o;
+      if (dd == 0) {
+        a.part_ml[((long long)split * rows + r) * 2] = M;
+        a.part_ml[((long long)split * rows + r) * 2 + 1] = l;
+      }
+    }
+  }
+}
+
+template <class T, int GC, bool MMA>
+cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                          dim3 grid, size_t smem, cudaStream_t st) {
+  auto kern = attn_kernel<T, GC, MMA>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+  }
+  kern<<<grid, kAttnThreads, smem, st>>>(a, *tk, *tv);
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

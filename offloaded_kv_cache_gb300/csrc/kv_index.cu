@@ -1,0 +1,249 @@
+// kv_index.cu -- the Quest index: per-page channel-wise key min/max, and the
+// page score q . (min, max) that bounds q . k from above.
+//
+// KVDrive: A Holistic Multi-Tier KV Cache Management System for Long-Context
+// LLM Inference, section 2.2 "Sparse attention": keys are split into blocks
+// and a block's importance is estimated by multiplying the query with the
+// channel-wise minimum and maximum of its keys.
+//
+// Both kernels stream their input once with coalesced 16-byte loads; they are
+// HBM-bound (or host-link bound for a host-resident K cache in the build).
+#include "kv_internal.cuh"
+
+namespace kvs {
+namespace {
+
+// ---------------------------------------------------------------------------
+// minmax build: one warp per (sequence, logical page, kv head)
+// ---------------------------------------------------------------------------
+// A page of one kv head is ps rows of d = 128 elements (256 or 512 bytes).
+// Lane = (16-byte column chunk, row group); rows are strided by the number of
+// row groups.  Values become IEEE totalOrder keys, so an unsigned min/max is
+// exact and does not depend on the order of the reduction (-0.0 < +0.0).
+template <class T>
+__global__ void __launch_bounds__(256)
+    minmax_build_kernel(const T *__restrict__ k, const int32_t *__restrict__ bt,
+                        const int32_t *__restrict__ ctx, T *__restrict__ mm, int B, int Hkv,
+                        int ps, int maxP, long long nphys, int *status) {
+  constexpr int C = kHeadDim * (int)sizeof(T) / 16;  // 16-byte chunks per row
+  constexpr int RG = 32 / C;                          // row groups per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * 8 + warp;
+  if (item >= (long long)B * maxP * Hkv) return;
+  const int kvh = (int)(item % Hkv);
+  const long long bp = item / Hkv;
+  const int p = (int)(bp % maxP);
+  const int b = (int)(bp / maxP);
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if (p == 0 && kvh == 0 && lane == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  if (p * ps >= len) return;
+  const int n = min(ps, len - p * ps);
+  const long long phys = bt[(long long)b * maxP + p];
+  if (phys < 0 || phys >= nphys) {
+    if (lane == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int chunk = lane % C, rg = lane / C;
+  const uint4 *src = reinterpret_cast<const uint4 *>(k) + ((phys * Hkv + kvh) * ps) * C + chunk;
+  uint4 lo = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 8
+  for (int r = rg; r < n; r += RG) {
+    uint4 x = src[(long long)r * C];
+    if constexpr (sizeof(T) == 2) {
+      x.x = key16x2(x.x); x.y = key16x2(x.y); x.z = key16x2(x.z); x.w = key16x2(x.w);
+      lo.x = __vminu2(lo.x, x.x); lo.y = __vminu2(lo.y, x.y);
+      lo.z = __vminu2(lo.z, x.z); lo.w = __vminu2(lo.w, x.w);
+      hi.x = __vmaxu2(hi.x, x.x); hi.y = __vmaxu2(hi.y, x.y);
+      hi.z = __vmaxu2(hi.z, x.z); hi.w = __vmaxu2(hi.w, x.w);
+    } else {
+      x.x = key32(x.x); x.y = key32(x.y); x.z = key32(x.z); x.w = key32(x.w);
+      lo.x = min(lo.x, x.x); lo.y = min(lo.y, x.y); lo.z = min(lo.z, x.z); lo.w = min(lo.w, x.w);
+      hi.x = max(hi.x, x.x); hi.y = max(hi.y, x.y); hi.z = max(hi.z, x.z); hi.w = max(hi.w, x.w);
+    }
+  }
+  if constexpr (RG == 2) {
+    // merge the two row groups (lanes l and l ^ 16 hold the same chunk)
+    uint4 lo2, hi2;
+    lo2.x = __shfl_xor_sync(0xFFFFFFFFu, lo.x, 16); lo2.y = __shfl_xor_sync(0xFFFFFFFFu, lo.y, 16);
+    lo2.z = __shfl_xor_sync(0xFFFFFFFFu, lo.z, 16); lo2.w = __shfl_xor_sync(0xFFFFFFFFu, lo.w, 16);
+    hi2.x = __shfl_xor_sync(0xFFFFFFFFu, hi.x, 16); hi2.y = __shfl_xor_sync(0xFFFFFFFFu, hi.y, 16);
+    hi2.z = __shfl_xor_sync(0xFFFFFFFFu, hi.z, 16); hi2.w = __shfl_xor_sync(0xFFFFFFFFu, hi.w, 16);
+    lo.x = __vminu2(lo.x, lo2.x); lo.y = __vminu2(lo.y, lo2.y);
+    lo.z = __vminu2(lo.z, lo2.z); lo.w = __vminu2(lo.w, lo2.w);
+    hi.x = __vmaxu2(hi.x, hi2.x); hi.y = __vmaxu2(hi.y, hi2.y);
+    hi.z = __vmaxu2(hi.z, hi2.z); hi.w = __vmaxu2(hi.w, hi2.w);
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(mm) + ((phys * Hkv + kvh) * 2) * C + chunk;
+  if constexpr (sizeof(T) == 2) {
+    // row group 0 writes the minimum, row group 1 the maximum
+    uint4 kk = rg == 0 ? lo : hi;
+    kk.x = unkey16x2(kk.x); kk.y = unkey16x2(kk.y); kk.z = unkey16x2(kk.z); kk.w = unkey16x2(kk.w);
+    dst[rg * C] = kk;
+  } else {
+    lo.x = unkey32(lo.x); lo.y = unkey32(lo.y); lo.z = unkey32(lo.z); lo.w = unkey32(lo.w);
+    hi.x = unkey32(hi.x); hi.y = unkey32(hi.y); hi.z = unkey32(hi.z); hi.w = unkey32(hi.w);
+    dst[0] = lo;
+    dst[C] = hi;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// page score: one warp per page, lane = 4 channels, GS query heads at once
+// ---------------------------------------------------------------------------
+// Sum over G per-lane partials across the warp with halving exchanges: after
+// the call lane l holds the full sum of head l / (32 / G).
+template <int G>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane) {
+  int bit = 16;
+#pragma unroll
+  for (int n = G; n > 1; n >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, bit);
+    }
+  }
+#pragma unroll
+  for (; bit >= 1; bit >>= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], bit);
+  return v[0];
+}
+
+template <class T>
+__device__ __forceinline__ void load4(const T *p, float (&x)[4]) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 f = *reinterpret_cast<const float4 *>(p);
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = unpack2(w.x, T()), c = unpack2(w.y, T());
+    x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+  }
+}
+
+constexpr int kScoreWarps = 8;
+constexpr int kScorePagesPerWarp = 4;
+
+template <class T, int GS>
+__global__ void __launch_bounds__(32 * kScoreWarps)
+    page_score_kernel(const T *__restrict__ q, const T *__restrict__ mm,
+                      const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
+                      float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
+                      long long nphys, int nchunk, int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int kvh = blockIdx.y / nchunk, chunk = blockIdx.y % nchunk;
+  const int G = Hq / Hkv;
+  const int head0 = kvh * G + chunk * GS;
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int P = (len + ps - 1) / ps;
+  float qf[GS][4];
+#pragma unroll
+  for (int g = 0; g < GS; ++g) load4(q + ((long long)b * Hq + head0 + g) * kHeadDim + 4 * lane, qf[g]);
+
+  constexpr int kSpan = 32 / GS;        // lanes per head after the reduction
+  const int my_head = lane / kSpan;     // the head whose total this lane ends with
+  const bool writer = (lane % kSpan) == 0;
+  float *srow = scores + ((long long)b * Hq + head0 + my_head) * maxP;
+
+  const int p0 = blockIdx.x * (kScoreWarps * kScorePagesPerWarp) + warp;
+#pragma unroll
+  for (int i = 0; i < kScorePagesPerWarp; ++i) {
+    const int p = p0 + i * kScoreWarps;
+    if (p >= maxP) break;
+    if (p >= P) {
+      if (writer) srow[p] = -INFINITY;
+      continue;
+    }
+    const long long phys = bt[(long long)b * maxP + p];
+    if (phys < 0 || phys >= nphys) {
+      if (lane == 0) flag_error(status, KV_ERR_BOUNDS);
+      if (writer) srow[p] = -INFINITY;
+      continue;
+    }
+    const T *row = mm + ((phys * Hkv + kvh) * 2) * kHeadDim + 4 * lane;
+    float mn[4], mx[4];
+    load4(row, mn);
+    load4(row + kHeadDim, mx);
+    float part[GS];
+#pragma unroll
+    for (int g = 0; g < GS; ++g) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // max(q*mn, q*mx) == q * (q >= 0 ? mx : mn) because mx >= mn
+        const float bound = qf[g][e] >= 0.f ? mx[e] : mn[e];
+        s = fmaf(qf[g][e], bound, s);
+      }
+      part[g] = s;
+    }
+    const float tot = reduce_heads<GS>(part, lane);
+    if (writer) srow[p] = tot;
+  }
+}
+
+template <class T>
+cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, const int32_t *ctx,
+                           float *scores, int B, int Hq, int Hkv, int ps, int maxP,
+                           long long nphys, int *status, cudaStream_t st) {
+  const int G = Hq / Hkv;
+  const int gs = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  const int nchunk = G / gs;
+  dim3 grid((maxP + kScoreWarps * kScorePagesPerWarp - 1) / (kScoreWarps * kScorePagesPerWarp),
+            Hkv * nchunk, B);
+  const T *qq = static_cast<const T *>(q);
+  const T *m = static_cast<const T *>(mm);
+  switch (gs) {
+    case 8: page_score_kernel<T, 8><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
+    case 4: page_score_kernel<T, 4><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
+    case 2: page_score_kernel<T, 2><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
+    default: page_score_kernel<T, 1><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
+                                void *minmax, int B, int Hkv, int ps, int maxP, long long nphys,
+                                int *status, cudaStream_t st) {
+  const long long items = (long long)B * maxP * Hkv;
+  const unsigned blocks = (unsigned)((items + 7) / 8);
+  switch (dtype) {
+    case KV_F32:
+      minmax_build_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float *>(k), bt, ctx,
+          static_cast<float *>(minmax), B, Hkv, ps, maxP, nphys, status);
+      break;
+    case KV_F16:
+      minmax_build_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half *>(k), bt, ctx,
+          static_cast<__half *>(minmax), B, Hkv, ps, maxP, nphys, status);
+      break;
+    default:
+      minmax_build_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(k), bt, ctx, static_cast<__nv_bfloat16 *>(minmax), B,
+          Hkv, ps, maxP, nphys, status);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,
+                              const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
+                              int maxP, long long nphys, int *status, cudaStream_t st) {
+  switch (dtype) {
+    case KV_F32: return score_dispatch<float>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
+    case KV_F16: return score_dispatch<__half>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
+    default: return score_dispatch<__nv_bfloat16>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
+  }
+}
+
+}  // namespace kvs

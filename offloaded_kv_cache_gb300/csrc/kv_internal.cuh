@@ -1,0 +1,208 @@
+// kv_internal.cuh -- device helpers and launcher declarations shared by the
+// kvsparse translation units (sm_103a only).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvsparse.h"
+
+namespace kvs {
+
+constexpr int kHeadDim = 128;
+
+// ---------------------------------------------------------------------------
+// device status word: the first error a kernel records wins
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void flag_error(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// element types
+// ---------------------------------------------------------------------------
+template <class T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kBytes = 4;
+  __device__ __forceinline__ static float to_f32(float x) { return x; }
+};
+template <> struct Elem<__half> {
+  static constexpr int kBytes = 2;
+  __device__ __forceinline__ static float to_f32(__half x) { return __half2float(x); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+// two packed 16-bit elements -> two floats
+__device__ __forceinline__ float2 unpack2(uint32_t w, __half) {
+  return __half22float2(*reinterpret_cast<__half2 *>(&w));
+}
+__device__ __forceinline__ float2 unpack2(uint32_t w, __nv_bfloat16) {
+  // bf16 is the upper half of an fp32: widening is a shift / mask
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ---------------------------------------------------------------------------
+// IEEE totalOrder keys (non-NaN): unsigned order of the key == totalOrder of
+// the value, so -0.0 < +0.0 and min/max are exact and order independent
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key16x2(uint32_t x) {
+  uint32_t s = (x >> 15) & 0x00010001u;  // sign bit of each half
+  return x ^ (0x80008000u | (s * 0x7FFFu));
+}
+__device__ __forceinline__ uint32_t unkey16x2(uint32_t k) {
+  uint32_t s = ((~k) >> 15) & 0x00010001u;  // halves that were negative
+  return k ^ (0x80008000u | (s * 0x7FFFu));
+}
+__device__ __forceinline__ uint32_t key32(uint32_t x) {
+  return x ^ (uint32_t)(((int32_t)x >> 31) | (int32_t)0x80000000);
+}
+__device__ __forceinline__ uint32_t unkey32(uint32_t k) {
+  return k ^ (uint32_t)(((int32_t)~k >> 31) | (int32_t)0x80000000);
+}
+
+// ---------------------------------------------------------------------------
+// fast exp2 (PTX ex2.approx: relative error ~2^-22; ex2(-inf) = +0)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (CTA scope) with bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of `parity` to complete; gives up after limit_ns of
+// wall time and returns false (the caller records KV_ERR_DEVICE_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// async copies into shared memory
+// ---------------------------------------------------------------------------
+// TMA tiled load of a 2-D box (x = element column, y = row) completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// 16-byte asynchronous global->shared copy (L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once all prior cp.async of this thread have landed; the
+// barrier's expected count already includes this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// 128-byte swizzle: inside each 1024-byte block of eight 128-byte rows, the
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7).  This is the layout TMA
+// writes with CU_TENSOR_MAP_SWIZZLE_128B into a 1024-byte aligned box; the
+// cp.async producer writes the same layout by hand.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// launch parameter blocks (host fills, kernels read)
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  const void *q;
+  const void *k;  // device-visible K cache
+  const void *v;  // device-visible V cache
+  const int32_t *block_table;
+  const int32_t *context_lens;
+  const int32_t *union_pages;   // sparse: [B][groups][umax], else null
+  const uint32_t *union_masks;  // sparse: [B][groups][umax]
+  const int32_t *union_count;   // sparse: [B][groups]
+  float *out;                   // [B][Hq][d]      (num_splits == 1)
+  float *part_o;                // [S][B][Hq][d]   (num_splits > 1)
+  float *part_ml;               // [S][B][Hq][2]   (log2-domain max, sum)
+  int *status;
+  long long nphys;
+  int B, Hq, Hkv, G, ps, maxP;
+  int nchunk;      // head chunks per kv head (G / heads-per-CTA)
+  int num_splits;  // CTAs per (b, head chunk)
+  int umax;        // union capacity per group (sparse)
+  int nstages;     // pipeline depth, a multiple of kConsumerWarps
+  int use_tma;     // 1: TMA producer, 0: cp.async producer
+  float scale_log2;
+  unsigned long long wait_limit_ns;
+  int debug_skip_page;  // >= 0: the producer never fills that page (timeout test)
+};
+
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = 32 * (1 + kConsumerWarps);
+
+// launchers (return a cudaError_t)
+cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
+                                void *minmax, int B, int Hkv, int ps, int maxP, long long nphys,
+                                int *status, cudaStream_t st);
+cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,
+                              const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
+                              int maxP, long long nphys, int *status, cudaStream_t st);
+cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
+                        int k, int32_t *indices, int *status, cudaStream_t st);
+cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,
+                         int gc, int ps, int maxP, int k, int umax, int32_t *upages,
+                         uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st);
+size_t attn_smem_bytes(int dtype, int gc, bool mma, int ps, int nstages);
+cudaError_t launch_attn(int dtype, int gc, bool mma, const AttnArgs &a, const CUtensorMap *tk,
+                        const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
+                           int Hq, cudaStream_t st);
+
+}  // namespace kvs

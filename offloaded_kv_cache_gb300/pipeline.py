@@ -1,0 +1,126 @@
+"""Device buffers and the decode steps of one paged-attention layer.
+
+`DecodeLayer` owns the device (or pinned host) copies of one workload and the
+outputs and workspaces the C ABI needs, and runs the path through the ctypes
+binding:
+
+    build_index()  -> kv_page_minmax_build
+    sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
+    dense_step()   -> kv_dense_decode_attn
+
+PyTorch is used for allocation, host<->device copies and streams only; every
+step of the computation runs in libkvsparse's kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import kvsparse as kv
+from .workloads import Workload
+
+TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def storage_to_torch(a: np.ndarray, dtype: str) -> torch.Tensor:
+    """Host tensor with exactly the stored bits of `a`."""
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
+def torch_to_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw element bits of a tensor as an unsigned numpy array."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy().view(np.uint32)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+class DecodeLayer:
+    def __init__(self, wl: Workload, kv_loc: str | None = None, topk: int | None = None,
+                 device: str = "cuda", kv_copies: int = 1):
+        spec = wl.spec
+        self.wl = wl
+        self.spec = spec
+        self.kv_loc = kv_loc or spec.kv_loc
+        self.topk = spec.topk if topk is None else topk
+        self.device = torch.device(device)
+        self.scale = wl.scale
+        self.shape = kv.make_shape(spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                   spec.page_size, spec.max_pages, spec.num_phys_pages, spec.dtype,
+                                   self.kv_loc)
+        dev = self.device
+        self.q = storage_to_torch(wl.q, spec.dtype).to(dev)
+        self.block_table = torch.from_numpy(wl.block_table).to(dev)
+        self.context_lens = torch.from_numpy(wl.context_lens).to(dev)
+        # kv_copies > 1 keeps rotated copies of the caches so that a timing
+        # loop can cycle through more bytes than the L2 holds
+        self.k_copies, self.v_copies = [], []
+        kt = storage_to_torch(wl.k_cache, spec.dtype)
+        vt = storage_to_torch(wl.v_cache, spec.dtype)
+        for _ in range(kv_copies):
+            if self.kv_loc == "host":
+                kh = torch.empty(kt.shape, dtype=kt.dtype, pin_memory=True)
+                vh = torch.empty(vt.shape, dtype=vt.dtype, pin_memory=True)
+                kh.copy_(kt)
+                vh.copy_(vt)
+                self.k_copies.append(kh)
+                self.v_copies.append(vh)
+            else:
+                self.k_copies.append(kt.to(dev))
+                self.v_copies.append(vt.to(dev))
+        self.k_cache, self.v_cache = self.k_copies[0], self.v_copies[0]
+        tdt = TORCH_DTYPE[spec.dtype]
+        self.minmax = torch.zeros((spec.num_phys_pages, spec.num_kv_heads, 2, spec.head_dim),
+                                  dtype=tdt, device=dev)
+        self.scores = torch.empty((spec.batch, spec.num_q_heads, spec.max_pages),
+                                  dtype=torch.float32, device=dev)
+        k = max(1, self.topk)
+        self.indices = torch.empty((spec.batch, spec.num_q_heads, k), dtype=torch.int32,
+                                   device=dev)
+        self.out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim),
+                               dtype=torch.float32, device=dev)
+        self.ws_dense_bytes = kv.kv_attn_workspace_bytes(self.shape, 0)
+        self.ws_sparse_bytes = kv.kv_attn_workspace_bytes(self.shape, k) if self.topk else 0
+        self.ws_topk_bytes = kv.kv_topk_workspace_bytes(self.shape, k)
+        nbytes = max(self.ws_dense_bytes, self.ws_sparse_bytes, self.ws_topk_bytes, 16)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def use_copy(self, i: int):
+        self.k_cache = self.k_copies[i % len(self.k_copies)]
+        self.v_cache = self.v_copies[i % len(self.v_copies)]
+
+    # --- steps -------------------------------------------------------------
+    def build_index(self, stream=None):
+        kv.kv_page_minmax_build(self.shape, self.k_cache, self.block_table, self.context_lens,
+                                self.minmax, stream)
+
+    def score(self, stream=None):
+        kv.kv_page_score(self.shape, self.q, self.minmax, self.block_table, self.context_lens,
+                         self.scores, stream)
+
+    def select(self, stream=None):
+        kv.kv_topk_select(self.shape, self.scores, self.context_lens, self.topk, self.indices,
+                          self.workspace, self.workspace.numel(), stream)
+
+    def sparse_attn(self, indices=None, stream=None):
+        idx = self.indices if indices is None else indices
+        kv.kv_sparse_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
+                                 self.context_lens, idx, idx.shape[-1], self.scale, self.out,
+                                 self.workspace, self.workspace.numel(), stream)
+
+    def sparse_step(self, stream=None):
+        self.score(stream)
+        self.select(stream)
+        self.sparse_attn(stream=stream)
+
+    def dense_step(self, stream=None):
+        kv.kv_dense_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
+                                self.context_lens, self.scale, self.out, self.workspace,
+                                self.workspace.numel(), stream)
+
+    # --- host views --------------------------------------------------------
+    def minmax_bits(self) -> np.ndarray:
+        return torch_to_bits(self.minmax)

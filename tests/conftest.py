@@ -21,3 +21,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def kvlib():
+    """libkvsparse, built in-tree if stale (nvcc cross-compiles without a GPU)."""
+    from offloaded_kv_cache_gb300 import build, kvsparse
+    build.build()
+    return kvsparse.load()
