@@ -1,0 +1,498 @@
+"""Decode-attention benchmark: KV GB/s, % of the bandwidth roofline, queries/s.
+
+One step = one pass of the decode path of one layer over one batch of the
+workload: dense attention for a dense-only workload; page scoring, top-K
+selection and sparse attention for a workload with a page budget (the dense
+pass and the index build are timed beside it and reported as sub-objects).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (the path has no exchange step); the job value is the units all ranks
+processed over the slowest rank's time.  `--impl reference` times the fp64 CPU
+oracle on this machine's host cores, as it stands, on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+DEFAULT_WORKLOAD = "opt6.7b-b32-ctx544"
+METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/sec"
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
+# hash of the kernel sources it was taken on; a changed kernel reports null.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("kv_attn.cuh", "kv_attn_core.cu", "kv_attn_mma.cu", "kv_internal.cuh"):
+        with open(os.path.join(ROOT, "offloaded_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def dense_bytes(spec, ctx):
+    e = spec.elem_bytes
+    kv = 2 * spec.num_kv_heads * int(np.sum(ctx)) * spec.head_dim * e
+    q = spec.batch * spec.num_q_heads * spec.head_dim * e
+    out = spec.batch * spec.num_q_heads * spec.head_dim * 4
+    pages = int(np.sum(-(-np.asarray(ctx) // spec.page_size)))
+    return kv + q + out + 4 * pages + 4 * spec.batch
+
+
+def sparse_bytes(spec, ctx, indices):
+    """(step bytes, attention bytes): score + select + attention over the union
+    of each (sequence, kv head) group's selected pages."""
+    e = spec.elem_bytes
+    B, Hq, Hkv, d, ps = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
+    G = spec.group
+    P = -(-np.asarray(ctx) // ps)
+    table = int(np.sum(P)) * Hkv * 2 * d * e                 # minmax read by page_score
+    scores = 2 * B * Hq * spec.max_pages * 4                 # written, then read by top-K
+    idx_w = B * Hq * indices.shape[-1] * 4                   # written by top-K
+    idx_r = B * Hq * indices.shape[-1] * 4                   # read by the union step
+    kv = 0
+    for b in range(B):
+        for kvh in range(Hkv):
+            sel = indices[b, kvh * G:(kvh + 1) * G].reshape(-1)
+            for p in np.unique(sel[sel >= 0]):
+                n = min(ps, int(ctx[b]) - int(p) * ps)
+                kv += 2 * n * d * e
+    q = B * Hq * d * e
+    out = B * Hq * d * 4
+    attn = idx_r + kv + q + out
+    return table + q + scores + idx_w + attn, attn
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+        sel = None
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            bus = getattr(props, "pci_bus_id", None)
+            dom = getattr(props, "pci_domain_id", 0)
+            dev = getattr(props, "pci_device_id", 0)
+            if bus is not None:
+                sel = f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+        except Exception:
+            sel = None
+        self.sel = sel
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.sel:
+            cmd += ["-i", self.sel]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if self.t_on and self.t_off and self.t_on <= t <= self.t_off]
+        use = inside or [r for _, r in self.rows]
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in use:
+            parts = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names[1:], parts[4:8]):
+                if v.lower() in ("active", "yes", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed region" if inside else "whole run (timed region shorter than "
+                                                        "the 100 ms sampling period)"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(spec, wl, target_s: float, nthreads: int):
+    """Times the oracle over whole (b, kv-head group) row sets, enough rows
+    for about target_s seconds; returns (GB/s, queries/s, seconds, sample)."""
+    import oracle
+    dtype = spec.dtype
+    G = spec.group
+    groups = [(b, kvh) for b in range(spec.batch) for kvh in range(spec.num_kv_heads)]
+
+    def rows_of(gs):
+        return [b * spec.num_q_heads + kvh * G + g for b, kvh in gs for g in range(G)]
+
+    def run(gs):
+        rows = rows_of(gs)
+        t0 = time.perf_counter()
+        if spec.topk:
+            bs = sorted({b for b, _ in gs})
+            for b in bs:
+                mn, mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table[b:b + 1],
+                                             wl.context_lens[b:b + 1])
+                s = oracle.scores(dtype, wl.q[b:b + 1], mn, mx, wl.block_table[b:b + 1],
+                                  wl.context_lens[b:b + 1], spec.page_size)
+                idx = oracle.topk(s, wl.context_lens[b:b + 1], spec.page_size, spec.topk)
+                rb = [r - b * spec.num_q_heads for r in rows if r // spec.num_q_heads == b]
+                oracle.attention(dtype, wl.q[b:b + 1], wl.k_cache, wl.v_cache,
+                                 wl.block_table[b:b + 1], wl.context_lens[b:b + 1], wl.scale,
+                                 indices=idx, rows=rb, nthreads=nthreads)
+        else:
+            oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                             wl.context_lens, wl.scale, rows=rows, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    n = 1
+    dt = run(groups[:1])
+    while dt < target_s / 4 and n < len(groups):
+        n = min(len(groups), max(n + 1, int(n * max(2.0, (target_s / 2) / max(dt, 1e-3)))))
+        dt = run(groups[:n])
+    gs = groups[:n]
+    ctx = wl.context_lens
+    kv = sum(2 * int(ctx[b]) * spec.head_dim * spec.elem_bytes for b, _ in gs)
+    gbs = kv / dt / 1e9
+    qps = len(rows_of(gs)) / dt
+    what = (f"{n} of {len(groups)} (sequence, kv head) groups = {len(rows_of(gs))} query heads, "
+            f"{'score+top-K+sparse attention' if spec.topk else 'dense attention'}, "
+            f"fp64 oracle, {nthreads} threads")
+    return gbs, qps, dt, what
+
+
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, spec_name):
+    from offloaded_kv_cache_gb300 import workloads as W
+    import oracle
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    spec = W.WORKLOADS[spec_name]
+    wl = W.generate(spec)
+    oracle.build()
+    cores = os.cpu_count() or 1
+    budget = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    what = ""
+    for i in range(args.warmup + args.steps):
+        gbs, qps, dt, what = oracle_sample(spec, wl, budget, cores)
+        if i >= args.warmup:
+            vals.append((gbs, qps, dt))
+    gbs = statistics.median(v[0] for v in vals)
+    qps = statistics.median(v[1] for v in vals)
+    line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.median(v[2] for v in vals), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "batch": spec.batch, "q_heads": spec.num_q_heads,
+                       "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                       "context": spec.context, "page_size": spec.page_size,
+                       "topk": spec.topk, "kv_loc": spec.kv_loc, "parallelism": "replicas"},
+            "queries_per_s": round(qps, 2),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": what},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+
+    import torch
+    import torch.distributed as dist
+    from offloaded_kv_cache_gb300 import build as kbuild
+    from offloaded_kv_cache_gb300 import kvsparse as kv
+    from offloaded_kv_cache_gb300 import workloads as W
+    from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    if rank == 0:
+        kbuild.build()
+    if ws > 1:
+        dist.barrier()
+    kv.load()
+
+    spec = W.WORKLOADS[args.workload]
+    wl = W.generate(spec)
+    ctx = wl.context_lens
+    l2_bytes = 129 * 2**20
+    copies = 1
+    if spec.kv_loc == "hbm":
+        copies = max(1, min(8, math.ceil(4 * l2_bytes / spec.kv_bytes())))
+    layer = DecodeLayer(wl, kv_copies=copies)
+    stream = torch.cuda.current_stream()
+    sparse = spec.topk > 0
+
+    # index (built once per page; timed separately below)
+    layer.build_index()
+    if sparse:
+        layer.score()
+        layer.select()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+
+    splits = kv.kv_attn_num_splits(layer.shape, spec.topk if sparse else 0)
+    if sparse:
+        step = layer.sparse_step
+        idx_np = layer.indices.cpu().numpy()
+        step_bytes, attn_bytes = sparse_bytes(spec, ctx, idx_np)
+        launches_per_step = 2 + 1 + 1 + (1 if splits > 1 else 0)   # score, top-K, union, attn, combine
+    else:
+        step = layer.dense_step
+        step_bytes = dense_bytes(spec, ctx)
+        launches_per_step = 1 + (1 if splits > 1 else 0)
+        attn_bytes = step_bytes
+
+    def timed(fn, k, warm, attn_fn=None):
+        for i in range(warm):
+            layer.use_copy(i)
+            fn()
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ka = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        kb = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        ev0.record(stream)
+        for i in range(k):
+            layer.use_copy(i)
+            if attn_fn is None:
+                ka[i].record(stream)
+                fn()
+                kb[i].record(stream)
+            else:
+                attn_fn(i, ka[i], kb[i])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        total_ms = ev0.elapsed_time(ev1)
+        kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ka, kb))
+        return total_ms, kern_ms
+
+    def sparse_with_events(i, a, b):
+        layer.score()
+        layer.select()
+        a.record(stream)
+        layer.sparse_attn()
+        b.record(stream)
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    clocks.mark_on()
+    total_ms, kern_ms = timed(step, args.steps, args.warmup,
+                              sparse_with_events if sparse else None)
+    clocks.mark_off()
+    t_local = total_ms
+    if ws > 1:
+        t = torch.tensor([t_local], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_local = float(t.item())
+    ms_per_step = t_local / args.steps
+    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
+    qps = ws * spec.batch * spec.num_q_heads / (ms_per_step * 1e-3)
+
+    # sustained window for the clock record when the timed region is short
+    if rank == 0 and total_ms < 500:
+        clocks.mark_on()
+        t_end = time.time() + 1.0
+        i = 0
+        while time.time() < t_end:
+            for _ in range(50):
+                layer.use_copy(i)
+                step()
+                i += 1
+            torch.cuda.synchronize()
+        clocks.mark_off()
+    clocks.stop()
+
+    # side measurements: dense pass for sparse workloads, index build
+    extra = {}
+    if sparse:
+        d_total, _ = timed(layer.dense_step, max(3, args.steps // 4), 3)
+        d_ms = d_total / max(3, args.steps // 4)
+        db = dense_bytes(spec, ctx)
+        extra["dense"] = {"ms_per_step": round(d_ms, 4), "GB_s": round(db / (d_ms * 1e-3) / 1e9, 2)}
+    ib_total, _ = timed(layer.build_index, max(3, args.steps // 4), 3)
+    ib_ms = ib_total / max(3, args.steps // 4)
+    kbytes = spec.num_kv_heads * int(np.sum(ctx)) * spec.head_dim * spec.elem_bytes
+    table_bytes = int(np.sum(-(-ctx // spec.page_size))) * spec.num_kv_heads * 2 * spec.head_dim * spec.elem_bytes
+    extra["index_build"] = {"ms": round(ib_ms, 4),
+                            "GB_s": round((kbytes + table_bytes) / (ib_ms * 1e-3) / 1e9, 2)}
+
+    # end to end through the public API with host buffers: q and context
+    # lengths copied in, the output copied out, every step
+    q_host = layer.q.cpu().pin_memory()
+    ctx_host = layer.context_lens.cpu().pin_memory()
+    out_host = torch.empty(layer.out.shape, dtype=torch.float32, pin_memory=True)
+    h2d = q_host.numel() * q_host.element_size() + ctx_host.numel() * 4
+    d2h = out_host.numel() * 4
+
+    def e2e_step():
+        layer.q.copy_(q_host, non_blocking=True)
+        layer.context_lens.copy_(ctx_host, non_blocking=True)
+        step()
+        out_host.copy_(layer.out, non_blocking=True)
+
+    e_total, _ = timed(e2e_step, args.steps, args.warmup)
+    e_ms = e_total / args.steps
+    if ws > 1:
+        t = torch.tensor([e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = ws * step_bytes / (e_ms * 1e-3) / 1e9
+    assert kv.kv_device_status() == kv.KV_OK
+
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = None
+    rec = NCU_TRAFFIC.get(spec.name)
+    if rec and rec.get("src") == kernel_source_hash():
+        traffic = rec["bytes"]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        gbs, cq, dt, what = oracle_sample(spec, wl, 2.0, cores)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": what, "seconds": round(dt, 3), "queries_per_s": round(cq, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": spec.dtype, "data": "synthetic",
+            "config": {"workload": spec.name, "batch": spec.batch, "q_heads": spec.num_q_heads,
+                       "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+                       "context": spec.context, "page_size": spec.page_size,
+                       "topk": spec.topk, "kv_loc": spec.kv_loc, "accumulate": "f32",
+                       "step": ("score + top-K + sparse attention" if sparse
+                                else "dense attention"),
+                       "l2": (f"{copies} rotating K/V copies of {spec.kv_bytes() / 2**20:.0f} MiB "
+                              f"each (> 4x the 129 MB L2 in total)" if copies > 1 else
+                              "K/V larger than L2"),
+                       "splits": splits, "parallelism": f"replicas x{ws}"},
+            "queries_per_s": round(qps, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": ("kv_sparse_decode_attn (union + attention + combine)" if sparse
+                                    else "kv_dense_decode_attn (attention"
+                                    + (" + combine)" if splits > 1 else ")")),
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+            "clocks": clocks.summary(),
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 5)},
+            "gpu_launches": launches_per_step * args.steps,
+            "cpu_baseline": cpu,
+            **extra,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -127,6 +127,12 @@ int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *co
  * selected pages live there. */
 size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k);
 
+/* Launch plan of the attention calls on the current device: the number of
+ * CTAs each (sequence, kv head, head chunk) is split over (k as for
+ * kv_attn_workspace_bytes).  With more than one split, the call launches a
+ * combine kernel after the attention kernel.  0 for an invalid shape. */
+int32_t kv_attn_num_splits(const kv_shape *shape, int32_t k);
+
 /* Sparse decode attention (KVDrive, section 2.3 step (3); DirectKV, core
  * method 2-3: the query and the output stay on chip and each K/V tile is read
  * once, with a streaming softmax).  For each (b, h):
@@ -159,8 +165,8 @@ const char *kv_status_string(int status);
 /* Testing hook for the bounded device-side waits (failure detection without
  * a GPU fault).  wait_limit_ns (1 ns .. 60 s; default 2 s) bounds every
  * pipeline wait of the attention kernels; skip_page >= 0 makes the producer
- * of every attention CTA leave its skip_page-th page unfilled, so the consumer
- * waiting for it gives up after the limit, the call's kernels finish, and
+ * of every attention CTA leave its skip_page-th 16-token K/V tile unfilled, so
+ * the consumer waiting for it gives up after the limit, the call's kernels finish, and
  * kv_device_status reports KV_ERR_DEVICE_TIMEOUT.  skip_page < 0 restores
  * normal operation.  Process-wide; not for concurrent use with other calls.
  * Returns KV_OK or KV_ERR_INVALID_ARG. */

@@ -136,7 +136,7 @@ Plan make_plan(const kv_shape *s, int k, int sms) {
   }
   pl.nchunk = G / pl.gc;
   pl.groups = s->num_kv_heads * pl.nchunk;
-  const int stage = 2 * s->page_size * kHeadDim * elem_bytes(s->dtype);
+  const int stage = 2 * kTileTokens * kHeadDim * elem_bytes(s->dtype);  // one K+V tile
   int ns = (64 * 1024 / stage) / kConsumerWarps * kConsumerWarps;
   if (ns < kConsumerWarps) ns = kConsumerWarps;
   if (ns > 16) ns = 16;
@@ -149,14 +149,16 @@ Plan make_plan(const kv_shape *s, int k, int sms) {
   const long long maxP = s->max_pages_per_seq;
   const long long work = k > 0 ? std::min<long long>((long long)pl.gc * k, maxP) : maxP;
   const long long units = (long long)s->batch * pl.groups;
-  // split count minimising (waves x pages per CTA), with ~4 pages of fixed
-  // cost per CTA (prologue, pipeline fill, merge)
+  // split count minimising (waves x 16-token tiles per CTA), with ~4 tiles of
+  // fixed cost per CTA (prologue, pipeline fill, merge); a split keeps at
+  // least one page
+  const long long upp = s->page_size / kTileTokens;
   long long best = LLONG_MAX;
   int bestS = 1;
-  const int smax = (int)std::min<long long>(1024, std::max<long long>(1, (work + 3) / 4));
-  for (int S = 1; S <= smax; ++S) {
+  const int smax = (int)std::min<long long>(1024, std::max<long long>(1, work * upp / 4));
+  for (int S = 1; S <= smax && S <= work; ++S) {
     const long long waves = (units * S + slots - 1) / slots;
-    const long long cost = waves * ((work + S - 1) / S + 4);
+    const long long cost = waves * (((work + S - 1) / S) * upp + 4);
     if (cost < best) {
       best = cost;
       bestS = S;
@@ -201,8 +203,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [rows = N * Hkv * ps][128 elements]; box = one 128-byte slab x ps
-// rows, 128-byte swizzle (matching the kernel's shared-memory layout).
+// 2-D view [rows = N * Hkv * ps][128 elements]; box = one 128-byte slab x
+// kTileTokens rows (one stage of the kernel's ring), 128-byte swizzle
+// (matching the kernel's shared-memory layout).
 int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
   auto fn = encode_fn();
   if (!fn) return KV_ERR_CUDA;
@@ -213,7 +216,7 @@ int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
   cuuint64_t dims[2] = {(cuuint64_t)kHeadDim,
                         (cuuint64_t)(s->num_phys_pages * s->num_kv_heads * s->page_size)};
   cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * eb};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)s->page_size};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)kTileTokens};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -369,6 +372,13 @@ size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k) {
   const int dev = current_device();
   const int sms = dev >= 0 ? sm_count(dev) : 152;
   return make_plan(shape, k, sms).total;
+}
+
+int32_t kv_attn_num_splits(const kv_shape *shape, int32_t k) {
+  if (check_shape(shape) != KV_OK || k < 0) return 0;
+  const int dev = current_device();
+  const int sms = dev >= 0 ? sm_count(dev) : 152;
+  return make_plan(shape, k, sms).S;
 }
 
 int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,

@@ -17,9 +17,10 @@
 //  * CTA = (split, kv head x head chunk, sequence).  All GC query heads of
 //    the chunk share one pass over the K/V bytes; in the sparse path the CTA
 //    walks the union of their selected pages once and masks per head.
-//  * Stage = one page of one kv head: K then V, each `ps` rows x 128 elements,
-//    stored as 128-byte slabs in the 128B-swizzled layout, so ldmatrix and
-//    16-byte shared loads are bank-conflict free.
+//  * Stage = one 16-token tile of one page of one kv head: K then V, each 16
+//    rows x 128 elements, stored as 128-byte slabs in the 128B-swizzled
+//    layout, so ldmatrix and 16-byte shared loads are bank-conflict free.  A
+//    page of ps tokens is ps / 16 consecutive tiles.
 //  * Producer: HBM -> TMA tiled loads (cp.async.bulk.tensor) completing on
 //    a full mbarrier with a transaction count; pinned host memory -> 16-byte
 //    cp.async issued by the 32 producer lanes (same layout, same barrier).
@@ -116,10 +117,12 @@ __global__ void __launch_bounds__(kAttnThreads)
   float *pbuf = q_s + GC * SL * QSTR;                  // CUDA core: [warps][GC][TP]
   uint8_t *stages = smem + kHeaderBytes;
 
+  constexpr int TT = kTileTokens;            // tokens per tile (stage)
+  constexpr int slab_bytes = TT * 128;
+  constexpr int kv_off = TT * 128 * SL;      // V follows K inside a stage
+  constexpr int stage_bytes = 2 * kv_off;
   const int ps = a.ps;
-  const int slab_bytes = ps * 128;
-  const int kv_off = ps * 128 * SL;  // V follows K inside a stage
-  const int stage_bytes = 2 * kv_off;
+  const int UPP = ps / TT;                   // tiles per page
   const int NS = a.nstages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   PageRange rng;
   rng.lo = min(total, split * per);
   rng.n = max(0, min(total, rng.lo + per) - rng.lo);
+  const int ntiles = rng.n * UPP;
   if (bad_len && split == 0 && threadIdx.x == 0 && chunk == 0) flag_error(a.status, KV_ERR_BOUNDS);
 
   // logical page, head mask and physical page of list entry j (-1 phys = bad)
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     bool ok = true;
     if (a.use_tma) {
       if (lane == 0) {
-        for (int j = 0; j < rng.n; ++j) {
+        for (int j = 0; j < ntiles; ++j) {
           const int s = j % NS;
           if (j >= NS && !mbar_wait(smem_u32(&empty[s]), ((j / NS) - 1) & 1, a.wait_limit_ns)) {
             flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
@@ -190,13 +194,13 @@ __global__ void __launch_bounds__(kAttnThreads)
           int p;
           uint32_t mask;
           long long phys;
-          page_of(j, p, mask, phys);
+          page_of(j / UPP, p, mask, phys);
           if (phys < 0) phys = 0;  // still fill the stage; the consumer skips it
           issued = j + 1;
           if (j == a.debug_skip_page) continue;
           const uint32_t fb = smem_u32(&full[s]);
           const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
-          const int row0 = (int)((phys * a.Hkv + kvh) * ps);
+          const int row0 = (int)((phys * a.Hkv + kvh) * ps) + (j % UPP) * TT;
           mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
 #pragma unroll
           for (int h = 0; h < SL; ++h) tma_load_2d(dst + h * slab_bytes, &tk, h * EPS, row0, fb);
@@ -208,8 +212,8 @@ __global__ void __launch_bounds__(kAttnThreads)
     } else {
       const char *kbase = static_cast<const char *>(a.k);
       const char *vbase = static_cast<const char *>(a.v);
-      const int chunks = ps * SL * 8;  // 16-byte chunks per K (or V) page
-      for (int j = 0; j < rng.n; ++j) {
+      constexpr int chunks = TT * SL * 8;  // 16-byte chunks per K (or V) tile
+      for (int j = 0; j < ntiles; ++j) {
         const int s = j % NS;
         if (j >= NS && !mbar_wait(smem_u32(&empty[s]), ((j / NS) - 1) & 1, a.wait_limit_ns)) {
           if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
@@ -219,11 +223,12 @@ __global__ void __launch_bounds__(kAttnThreads)
         int p;
         uint32_t mask;
         long long phys;
-        page_of(j, p, mask, phys);
+        page_of(j / UPP, p, mask, phys);
         if (phys < 0) phys = 0;
         issued = j + 1;
         if (j == a.debug_skip_page) continue;
-        const size_t src0 = (size_t)((phys * a.Hkv + kvh) * ps) * (SL * 128);
+        const size_t src0 =
+            ((size_t)((phys * a.Hkv + kvh) * ps) + (size_t)(j % UPP) * TT) * (SL * 128);
         const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
         for (int i = lane; i < chunks; i += 32) {
           const int row = i / (SL * 8), rem = i % (SL * 8);
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     const float sl = a.scale_log2;
 #pragma unroll 1
-    for (int j = cw; j < rng.n; j += kConsumerWarps) {
+    for (int j = cw; j < ntiles; j += kConsumerWarps) {
       const int s = j % NS;
       if (!mbar_wait(smem_u32(&full[s]), (j / NS) & 1, a.wait_limit_ns)) {
         if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
@@ -291,21 +296,20 @@ __global__ void __launch_bounds__(kAttnThreads)
       int p;
       uint32_t msk;
       long long phys;
-      page_of(j, p, msk, phys);
-      int nv = 0;
+      page_of(j / UPP, p, msk, phys);
+      int nv = 0;  // valid tokens of this tile
       if (phys >= 0) {
-        nv = min(ps, len - p * ps);
-      } else if (lane == 0) {
+        nv = max(0, min(TT, len - p * ps - (j % UPP) * TT));
+      } else if (lane == 0 && (j % UPP) == 0) {
         flag_error(a.status, KV_ERR_BOUNDS);
       }
       uint8_t *st = stages + (size_t)s * stage_bytes;
       if constexpr (MMA) {
         const uint32_t kb = smem_u32(st), vb = kb + kv_off;
-        if (nv > 0 && nv < ps) {
-          // zero V rows past the last valid token of the 16-token tile they
-          // share with valid ones (P is 0 there, but 0 * NaN would not be)
-          const int hi_row = min(ps, (nv + 15) & ~15);
-          for (int i = lane; i < (hi_row - nv) * SL * 8; i += 32) {
+        if (nv > 0 && nv < TT) {
+          // zero the V rows past the last valid token (P is 0 there, but
+          // 0 * NaN would not be)
+          for (int i = lane; i < (TT - nv) * SL * 8; i += 32) {
             const int row = nv + i / (SL * 8), rem = i % (SL * 8);
             *reinterpret_cast<uint4 *>(st + kv_off + (rem >> 3) * slab_bytes + swz(row, rem & 7)) =
                 make_uint4(0u, 0u, 0u, 0u);
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads)
             }
           }
         }
-        if (nv > 0 && nv < ps) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (nv > 0 && nv < TT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       } else {
         // ---- CUDA-core consumer ----
         const int tt = lane / SL, hh = lane % SL;

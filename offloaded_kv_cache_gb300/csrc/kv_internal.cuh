@@ -13,6 +13,8 @@
 namespace kvs {
 
 constexpr int kHeadDim = 128;
+// tokens per K/V tile: one pipeline stage, one TMA box height
+constexpr int kTileTokens = 16;
 
 // ---------------------------------------------------------------------------
 // device status word: the first error a kernel records wins

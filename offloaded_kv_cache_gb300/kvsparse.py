@@ -65,6 +65,7 @@ def load(path: str = LIB_PATH):
         "kv_topk_workspace_bytes": (sz, [S, i32]),
         "kv_topk_select": (ctypes.c_int, [S, P, P, i32, P, P, sz, P]),
         "kv_attn_workspace_bytes": (sz, [S, i32]),
+        "kv_attn_num_splits": (i32, [S, i32]),
         "kv_sparse_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, P, i32, f32, P, P, sz, P]),
         "kv_dense_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, f32, P, P, sz, P]),
         "kv_device_status": (ctypes.c_int, [P]),
@@ -140,6 +141,10 @@ def kv_topk_select(shape, scores, context_lens, k, indices, workspace=None, work
 
 def kv_attn_workspace_bytes(shape, k) -> int:
     return int(load().kv_attn_workspace_bytes(ctypes.byref(shape), int(k)))
+
+
+def kv_attn_num_splits(shape, k) -> int:
+    return int(load().kv_attn_num_splits(ctypes.byref(shape), int(k)))
 
 
 def kv_sparse_decode_attn(shape, q, k_cache, v_cache, block_table, context_lens, indices, k,
