@@ -153,6 +153,30 @@ int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cac
                          const int32_t *context_lens, float scale, float *out, void *workspace,
                          size_t workspace_bytes, void *stream);
 
+/* Dense decode attention for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a convenience of this library.
+ * Callers such as a plugin that a host framework hands only its input and
+ * output buffers, or a latency-critical loop where cudaMalloc would
+ * synchronise the device, have no workspace to pass.  This call computes
+ * exactly what kv_dense_decode_attn computes, with the split-K partials kept
+ * in a fixed 1 MiB scratch array inside the library's device image, which
+ * every GPU that loads the library holds until the process exits.  It
+ * allocates nothing and calls no allocating routine.
+ *  - Limit: shapes whose partials need more than 1 MiB (see
+ *    kv_attn_workspace_bytes(shape, 0)) are refused with KV_ERR_WORKSPACE
+ *    before anything is launched; use kv_dense_decode_attn for them.
+ *  - The first call on each device looks up the scratch array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents; nothing in it needs to start at zero.  Calls that overlap on
+ *    the GPU (concurrent streams, or several host threads) race on it.
+ * Other arguments and return codes as kv_dense_decode_attn. */
+int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_table,
+                                 const int32_t *context_lens, float scale, float *out,
+                                 void *stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: KV_OK, KV_ERR_DEVICE_TIMEOUT or KV_ERR_BOUNDS (the
  * first error recorded since the last call), or KV_ERR_CUDA if the
