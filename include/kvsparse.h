@@ -177,6 +177,16 @@ int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q, const voi
                                  const int32_t *context_lens, float scale, float *out,
                                  void *stream);
 
+/* Streaming-read bandwidth probe (DirectKV, observation 4: host-resident
+ * long-context attention is bound by the link's sustained bandwidth; this
+ * measures that bandwidth).  Reads `bytes` (a multiple of 16) from `src` --
+ * device memory, or pinned host memory read in place through its device
+ * mapping -- with 16-byte loads from every SM, and writes one XOR word per
+ * thread block into `sink` (device memory, sink_words >= 1 words; up to 4
+ * blocks per SM are used).  Time it with events on `stream`. */
+int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
+                         int32_t sink_words, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: KV_OK, KV_ERR_DEVICE_TIMEOUT or KV_ERR_BOUNDS (the
  * first error recorded since the last call), or KV_ERR_CUDA if the

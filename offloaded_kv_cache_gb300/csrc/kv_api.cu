@@ -11,13 +11,6 @@
 
 #include "kv_internal.cuh"
 
-namespace kvs {
-cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
-                             const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
-cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
-                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
-}  // namespace kvs
-
 namespace {
 
 using namespace kvs;
@@ -112,7 +105,7 @@ int resolve_kv(const kv_shape *s, const void *p, const void **dev_ptr) {
 struct Plan {
   int gc = 1, nchunk = 1, groups = 1;
   bool mma = false;
-  int S = 1, umax = 0, nstages = 4;
+  int S = 1, umax = 0, nstages = 4, nw = 4, header = 8192;
   size_t smem = 0;
   size_t off_part_o = 0, off_part_ml = 0, off_upages = 0, off_umasks = 0, off_ucount = 0;
   size_t total = 0;
@@ -120,7 +113,48 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-Plan make_plan(const kv_shape *s, int k, int sms) {
+// CTA shapes the planner chooses between (consumer warps, stages):
+//  * wide: small CTAs, many resident per SM, for many short (b, head) units
+//    that fit one wave without splitting;
+//  * deep: four consumer warps double-buffered over an 8-stage ring (4 for
+//    fp32), split along the context when there are few long units.
+#ifndef KVS_WIDE_NW
+#define KVS_WIDE_NW 2
+#endif
+#ifndef KVS_WIDE_NS
+#define KVS_WIDE_NS 2
+#endif
+#ifndef KVS_DEEP_NW
+#define KVS_DEEP_NW 4
+#endif
+#ifndef KVS_DEEP_RING_BYTES
+#define KVS_DEEP_RING_BYTES (64 * 1024)
+#endif
+#ifndef KVS_SPLIT_OVERHEAD_TILES
+#define KVS_SPLIT_OVERHEAD_TILES 4  // fixed cost of a CTA, in tiles, for the split choice
+#endif
+
+int header_bytes(long long list_pages) {
+  const long long b = 4096 + 8 * std::min<long long>(list_pages, kMaxListPages);
+  return (int)((b + 1023) / 1024 * 1024);
+}
+
+// resident CTAs per SM: the occupancy calculator on the real kernel when a
+// device is present, else an estimate from shared memory and threads
+int resident_ctas(const Plan &pl, int dtype, bool have_device) {
+  const int threads = 32 * (1 + pl.nw);
+  int n = 0;
+  if (have_device)
+    n = pl.mma ? attn_occupancy_mma(dtype, pl.gc, threads, pl.smem)
+               : attn_occupancy_core(dtype, pl.gc, threads, pl.smem);
+  if (n <= 0) {
+    n = (int)((228 * 1024) / (pl.smem + 1024));
+    n = std::min(n, 2048 / threads);
+  }
+  return std::max(n, 1);
+}
+
+Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
   Plan pl;
   const int G = s->num_q_heads / s->num_kv_heads;
   if (s->dtype == KV_F32) {
@@ -137,34 +171,60 @@ Plan make_plan(const kv_shape *s, int k, int sms) {
   pl.nchunk = G / pl.gc;
   pl.groups = s->num_kv_heads * pl.nchunk;
   const int stage = 2 * kTileTokens * kHeadDim * elem_bytes(s->dtype);  // one K+V tile
-  int ns = (64 * 1024 / stage) / kConsumerWarps * kConsumerWarps;
-  if (ns < kConsumerWarps) ns = kConsumerWarps;
-  if (ns > 16) ns = 16;
-  pl.nstages = ns;
-  pl.smem = 1024 + 4096 + (size_t)ns * stage;
-  int per_sm = (int)((228 * 1024) / (pl.smem + 1024));
-  if (per_sm > 2048 / kAttnThreads) per_sm = 2048 / kAttnThreads;
-  if (per_sm < 1) per_sm = 1;
-  const long long slots = (long long)sms * per_sm;
   const long long maxP = s->max_pages_per_seq;
   const long long work = k > 0 ? std::min<long long>((long long)pl.gc * k, maxP) : maxP;
   const long long units = (long long)s->batch * pl.groups;
-  // split count minimising (waves x 16-token tiles per CTA), with ~4 tiles of
-  // fixed cost per CTA (prologue, pipeline fill, merge); a split keeps at
-  // least one page
   const long long upp = s->page_size / kTileTokens;
-  long long best = LLONG_MAX;
-  int bestS = 1;
-  const int smax = (int)std::min<long long>(1024, std::max<long long>(1, work * upp / 4));
-  for (int S = 1; S <= smax && S <= work; ++S) {
-    const long long waves = (units * S + slots - 1) / slots;
-    const long long cost = waves * (((work + S - 1) / S) * upp + 4);
-    if (cost < best) {
-      best = cost;
-      bestS = S;
+
+  // wide: one CTA per unit, all resident at once
+  Plan wide = pl;
+  wide.nw = KVS_WIDE_NW;
+  wide.nstages = KVS_WIDE_NS;
+  wide.S = 1;
+  wide.header = header_bytes(work);
+  wide.smem = 1024 + wide.header + (size_t)wide.nstages * stage;
+  // wide when the units alone keep enough K/V bytes in flight on every SM
+  // (about 96 KB) without splitting them
+#ifndef KVS_WIDE_INFLIGHT
+#define KVS_WIDE_INFLIGHT (96 * 1024)
+#endif
+  (void)have_device;
+  const bool use_wide = work <= kMaxListPages &&
+                        units * wide.nstages * stage >= (long long)sms * KVS_WIDE_INFLIGHT;
+
+  if (use_wide) {
+    pl = wide;
+  } else {
+    pl.nw = KVS_DEEP_NW;
+    int ns = (KVS_DEEP_RING_BYTES / stage) / pl.nw * pl.nw;
+    ns = std::max(ns, 2 * pl.nw);
+    ns = std::min(ns, kMaxStages / pl.nw * pl.nw);
+    pl.nstages = ns;
+    pl.header = header_bytes(kMaxListPages);
+    pl.smem = 1024 + pl.header + (size_t)ns * stage;
+    const long long slots = (long long)sms * resident_ctas(pl, s->dtype, have_device);
+    // split count minimising (waves x tiles per CTA) plus a fixed cost per
+    // CTA; a split keeps at least one page and at most kMaxListPages
+    const int smin = (int)std::max<long long>(1, (work + kMaxListPages - 1) / kMaxListPages);
+    const int smax = (int)std::min<long long>(1024, std::max<long long>(smin, work * upp / 4));
+    long long best = LLONG_MAX;
+    int bestS = smin;
+    for (int S = smin; S <= smax && S <= work; ++S) {
+      const long long waves = (units * S + slots - 1) / slots;
+      const long long cost = waves * (((work + S - 1) / S) * upp + KVS_SPLIT_OVERHEAD_TILES);
+      if (cost < best) {
+        best = cost;
+        bestS = S;
+      }
     }
+#ifdef KVS_FORCE_SPLITS
+    bestS = (int)std::min<long long>(std::max(KVS_FORCE_SPLITS, smin), std::max<long long>(work, 1));
+#endif
+    pl.S = bestS;
+    // a smaller page list leaves more shared memory
+    pl.header = header_bytes((work + pl.S - 1) / pl.S);
+    pl.smem = 1024 + pl.header + (size_t)ns * stage;
   }
-  pl.S = bestS;
   pl.umax = k > 0 ? (int)work : 0;
   size_t off = 0;
   const size_t rows = (size_t)s->batch * s->num_q_heads;
@@ -239,7 +299,7 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   const void *kd = nullptr, *vd = nullptr;
   if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
   if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
-  const Plan pl = make_plan(s, indices ? k : 0, sm_count(dev));
+  const Plan pl = make_plan(s, indices ? k : 0, sm_count(dev), true);
   if (pl.total > 0 && (ws == nullptr || ws_bytes < pl.total || !al16(ws))) return KV_ERR_WORKSPACE;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
@@ -264,6 +324,8 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   a.nchunk = pl.nchunk;
   a.num_splits = pl.S;
   a.nstages = pl.nstages;
+  a.nw = pl.nw;
+  a.header_bytes = pl.header;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.debug_skip_page = g_debug_skip_page.load();
@@ -371,14 +433,14 @@ size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k) {
   if (check_shape(shape) != KV_OK || k < 0) return 0;
   const int dev = current_device();
   const int sms = dev >= 0 ? sm_count(dev) : 152;
-  return make_plan(shape, k, sms).total;
+  return make_plan(shape, k, sms, dev >= 0).total;
 }
 
 int32_t kv_attn_num_splits(const kv_shape *shape, int32_t k) {
   if (check_shape(shape) != KV_OK || k < 0) return 0;
   const int dev = current_device();
   const int sms = dev >= 0 ? sm_count(dev) : 152;
-  return make_plan(shape, k, sms).S;
+  return make_plan(shape, k, sms, dev >= 0).S;
 }
 
 int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,

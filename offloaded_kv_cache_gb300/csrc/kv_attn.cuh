@@ -24,8 +24,10 @@
 //  * Producer: HBM -> TMA tiled loads (cp.async.bulk.tensor) completing on
 //    a full mbarrier with a transaction count; pinned host memory -> 16-byte
 //    cp.async issued by the 32 producer lanes (same layout, same barrier).
-//    Stage s always belongs to consumer warp s % kConsumerWarps, which arrives
-//    on the stage's empty mbarrier when done.
+//    Stage s always belongs to consumer warp s % nw, which arrives on the
+//    stage's empty mbarrier when done.  The number of consumer warps nw and
+//    of stages are launch parameters: many short (sequence, head) units run
+//    as small CTAs, all resident in one wave; long units as deep CTAs.
 //  * Consumers: GQA groups of >= 4 heads on 16-bit data use mma.sync
 //    m16n8k16 (tokens x heads tile of q.K^T, then V^T . P^T with P split in a
 //    high and a low 16-bit part so the weights keep ~16 bits); otherwise
@@ -39,8 +41,9 @@
 
 namespace kvs {
 
-constexpr int kMaxStages = 16;
-constexpr int kHeaderBytes = 4096;  // barriers + per-CTA q / weight buffers
+// shared memory before the ring: [0, 4096) barriers, q and weights; then the
+// page list (a.header_bytes in total, a multiple of 1024)
+constexpr int kFixedHeaderBytes = 4096;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -97,9 +100,15 @@ __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uin
 struct PageRange {
   int lo, n;  // first index into the (dense or union) list, count
 };
+// one page of the list, resolved once in the prologue: physical page (-1 when
+// the entry is out of range) and (valid tokens | head mask << 8)
+struct PageEnt {
+  int phys;
+  int info;
+};
 
 template <class T, int GC, bool MMA>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnMaxThreads)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv) {
   constexpr int SL = (int)sizeof(T);        // 128-byte slabs per 128-element row
@@ -115,7 +124,8 @@ __global__ void __launch_bounds__(kAttnThreads)
   uint64_t *empty = full + kMaxStages;
   float *q_s = reinterpret_cast<float *>(smem + 256);  // CUDA core: [GC][SL][QSTR]
   float *pbuf = q_s + GC * SL * QSTR;                  // CUDA core: [warps][GC][TP]
-  uint8_t *stages = smem + kHeaderBytes;
+  PageEnt *plist = reinterpret_cast<PageEnt *>(smem + kFixedHeaderBytes);
+  uint8_t *stages = smem + a.header_bytes;
 
   constexpr int TT = kTileTokens;            // tokens per tile (stage)
   constexpr int slab_bytes = TT * 128;
@@ -141,26 +151,9 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int per = (total + a.num_splits - 1) / a.num_splits;
   PageRange rng;
   rng.lo = min(total, split * per);
-  rng.n = max(0, min(total, rng.lo + per) - rng.lo);
+  rng.n = max(0, min(min(total, rng.lo + per) - rng.lo, kMaxListPages));
   const int ntiles = rng.n * UPP;
   if (bad_len && split == 0 && threadIdx.x == 0 && chunk == 0) flag_error(a.status, KV_ERR_BOUNDS);
-
-  // logical page, head mask and physical page of list entry j (-1 phys = bad)
-  auto page_of = [&](int j, int &p, uint32_t &mask, long long &phys) {
-    const int e = rng.lo + j;
-    if (sparse) {
-      p = a.union_pages[gidx * a.umax + e];
-      mask = a.union_masks[gidx * a.umax + e];
-    } else {
-      p = e;
-      mask = (1u << GC) - 1u;
-    }
-    phys = -1;
-    if (p >= 0 && p < P) {
-      const long long ph = a.block_table[(long long)b * a.maxP + p];
-      if (ph >= 0 && ph < a.nphys) phys = ph;
-    }
-  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -168,6 +161,31 @@ __global__ void __launch_bounds__(kAttnThreads)
       mbar_init(smem_u32(&empty[s]), 1u);
     }
     fence_mbar_init();
+  }
+  // Resolve this CTA's page list once (block table, union list, valid tokens,
+  // head masks), all threads in parallel, so no tile waits on a dependent
+  // global load later.
+  for (int j = threadIdx.x; j < rng.n; j += blockDim.x) {
+    const int e = rng.lo + j;
+    int p;
+    uint32_t mask;
+    if (sparse) {
+      p = a.union_pages[gidx * a.umax + e];
+      mask = a.union_masks[gidx * a.umax + e];
+    } else {
+      p = e;
+      mask = (1u << GC) - 1u;
+    }
+    PageEnt ent{-1, 0};
+    if (p >= 0 && p < P) {
+      const long long ph = a.block_table[(long long)b * a.maxP + p];
+      if (ph >= 0 && ph < a.nphys) {
+        ent.phys = (int)ph;
+        ent.info = min(ps, len - p * ps) | (int)(mask << 8);
+      }
+    }
+    if (ent.phys < 0) flag_error(a.status, KV_ERR_BOUNDS);
+    plist[j] = ent;
   }
   if constexpr (!MMA) {
     for (int i = threadIdx.x; i < GC * kHeadDim; i += blockDim.x) {
@@ -191,11 +209,8 @@ __global__ void __launch_bounds__(kAttnThreads)
             ok = false;
             break;
           }
-          int p;
-          uint32_t mask;
-          long long phys;
-          page_of(j / UPP, p, mask, phys);
-          if (phys < 0) phys = 0;  // still fill the stage; the consumer skips it
+          // a bad entry still fills its stage (from page 0); the consumer skips it
+          const long long phys = max(plist[j / UPP].phys, 0);
           issued = j + 1;
           if (j == a.debug_skip_page) continue;
           const uint32_t fb = smem_u32(&full[s]);
@@ -220,11 +235,7 @@ __global__ void __launch_bounds__(kAttnThreads)
           ok = false;
           break;
         }
-        int p;
-        uint32_t mask;
-        long long phys;
-        page_of(j / UPP, p, mask, phys);
-        if (phys < 0) phys = 0;
+        const long long phys = max(plist[j / UPP].phys, 0);
         issued = j + 1;
         if (j == a.debug_skip_page) continue;
         const size_t src0 =
@@ -287,22 +298,16 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
     const float sl = a.scale_log2;
 #pragma unroll 1
-    for (int j = cw; j < ntiles; j += kConsumerWarps) {
+    for (int j = cw; j < ntiles; j += a.nw) {
       const int s = j % NS;
       if (!mbar_wait(smem_u32(&full[s]), (j / NS) & 1, a.wait_limit_ns)) {
         if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
         break;
       }
-      int p;
-      uint32_t msk;
-      long long phys;
-      page_of(j / UPP, p, msk, phys);
-      int nv = 0;  // valid tokens of this tile
-      if (phys >= 0) {
-        nv = max(0, min(TT, len - p * ps - (j % UPP) * TT));
-      } else if (lane == 0 && (j % UPP) == 0) {
-        flag_error(a.status, KV_ERR_BOUNDS);
-      }
+      const PageEnt ent = plist[j / UPP];
+      const uint32_t msk = (uint32_t)ent.info >> 8;
+      // valid tokens of this tile (0 for a bad entry)
+      const int nv = ent.phys >= 0 ? max(0, min(TT, (ent.info & 0xFF) - (j % UPP) * TT)) : 0;
       uint8_t *st = stages + (size_t)s * stage_bytes;
       if constexpr (MMA) {
         const uint32_t kb = smem_u32(st), vb = kb + kv_off;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kAttnThreads)
       } else {
         // ---- CUDA-core consumer ----
         const int tt = lane / SL, hh = lane % SL;
-        float *pb = pbuf + cw * GC * TP;
+        float *pb = pbuf + cw * GC * TP;  // cw < kMaxConsumerWarps
         // this lane's 4 output channels 4*lane .. 4*lane+3 inside a V row
         const int vslab = (4 * lane * SL) / 128;
         const int vbyte = (4 * lane * SL) % 128;
@@ -475,9 +480,9 @@ __global__ void __launch_bounds__(kAttnThreads)
 
   // ======================= merge the consumer warps =======================
   __syncthreads();  // every stage is consumed (or abandoned): reuse the ring
-  float *mw = reinterpret_cast<float *>(stages);  // [warps][GC]
-  float *lw = mw + kConsumerWarps * GC;           // [warps][GC]
-  float *ow = lw + kConsumerWarps * GC;           // [warps][GC][128]
+  float *mw = reinterpret_cast<float *>(stages);  // [warps][GC] (at most 64)
+  float *lw = mw + 64;                            // [warps][GC]
+  float *ow = mw + 128;                           // [warps][GC][128], 16-byte aligned
   if (warp > 0) {
     if constexpr (MMA) {
 #pragma unroll
@@ -520,11 +525,11 @@ __global__ void __launch_bounds__(kAttnThreads)
     const int g = i / kHeadDim, dd = i % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mw[w * GC + g]);
+    for (int w = 0; w < a.nw; ++w) M = fmaxf(M, mw[w * GC + g]);
     float o = 0.f, l = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < a.nw; ++w) {
         const float m = mw[w * GC + g];
         const float f = m == -INFINITY ? 0.f : ex2(m - M);
         o = fmaf(f, ow[(w * GC + g) * kHeadDim + dd], o);
@@ -557,8 +562,30 @@ cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap *tk, const CUtens
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  kern<<<grid, kAttnThreads, smem, st>>>(a, *tk, *tv);
+  kern<<<grid, 32 * (1 + a.nw), smem, st>>>(a, *tk, *tv);
   return cudaGetLastError();
+}
+
+template <class T, int GC, bool MMA>
+int attn_occupancy_t(int threads, size_t smem) {
+  auto kern = attn_kernel<T, GC, MMA>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int attr_done[64] = {0};
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    attr_done[dev] = 1;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace kvs

@@ -20,4 +20,18 @@ cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtenso
   return launch_attn_t<__nv_bfloat16, 1, false>(a, tk, tv, grid, smem, st);
 }
 
+int attn_occupancy_core(int dtype, int gc, int threads, size_t smem) {
+  if (dtype == KV_F32) {
+    if (gc == 4) return attn_occupancy_t<float, 4, false>(threads, smem);
+    if (gc == 2) return attn_occupancy_t<float, 2, false>(threads, smem);
+    return attn_occupancy_t<float, 1, false>(threads, smem);
+  }
+  if (dtype == KV_F16) {
+    if (gc == 2) return attn_occupancy_t<__half, 2, false>(threads, smem);
+    return attn_occupancy_t<__half, 1, false>(threads, smem);
+  }
+  if (gc == 2) return attn_occupancy_t<__nv_bfloat16, 2, false>(threads, smem);
+  return attn_occupancy_t<__nv_bfloat16, 1, false>(threads, smem);
+}
+
 }  // namespace kvs

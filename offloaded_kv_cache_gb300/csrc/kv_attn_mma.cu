@@ -15,4 +15,13 @@ cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensor
   return launch_attn_t<__nv_bfloat16, 4, true>(a, tk, tv, grid, smem, st);
 }
 
+int attn_occupancy_mma(int dtype, int gc, int threads, size_t smem) {
+  if (dtype == KV_F16) {
+    if (gc == 8) return attn_occupancy_t<__half, 8, true>(threads, smem);
+    return attn_occupancy_t<__half, 4, true>(threads, smem);
+  }
+  if (gc == 8) return attn_occupancy_t<__nv_bfloat16, 8, true>(threads, smem);
+  return attn_occupancy_t<__nv_bfloat16, 4, true>(threads, smem);
+}
+
 }  // namespace kvs

@@ -179,15 +179,21 @@ struct AttnArgs {
   int nchunk;      // head chunks per kv head (G / heads-per-CTA)
   int num_splits;  // CTAs per (b, head chunk)
   int umax;        // union capacity per group (sparse)
-  int nstages;     // pipeline depth, a multiple of kConsumerWarps
+  int nstages;     // pipeline depth, a multiple of nw
+  int nw;          // consumer warps (blockDim.x == 32 * (1 + nw))
+  int header_bytes;  // shared-memory bytes before the stage ring (multiple of 1024)
   int use_tma;     // 1: TMA producer, 0: cp.async producer
   float scale_log2;
   unsigned long long wait_limit_ns;
   int debug_skip_page;  // >= 0: the producer never fills that page (timeout test)
 };
 
-constexpr int kConsumerWarps = 4;
-constexpr int kAttnThreads = 32 * (1 + kConsumerWarps);
+// Attention CTA shape: one producer warp plus 1..kMaxConsumerWarps consumer
+// warps (chosen per launch); a CTA owns at most kMaxListPages pages.
+constexpr int kMaxConsumerWarps = 4;
+constexpr int kAttnMaxThreads = 32 * (1 + kMaxConsumerWarps);
+constexpr int kMaxListPages = 512;
+constexpr int kMaxStages = 16;
 
 // launchers (return a cudaError_t)
 cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
@@ -201,9 +207,13 @@ cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, 
 cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,
                          int gc, int ps, int maxP, int k, int umax, int32_t *upages,
                          uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st);
-size_t attn_smem_bytes(int dtype, int gc, bool mma, int ps, int nstages);
-cudaError_t launch_attn(int dtype, int gc, bool mma, const AttnArgs &a, const CUtensorMap *tk,
-                        const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
+                             const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
+                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+// resident attention CTAs per SM for a launch shape (0 when unknown)
+int attn_occupancy_core(int dtype, int gc, int threads, size_t smem);
+int attn_occupancy_mma(int dtype, int gc, int threads, size_t smem);
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st);
 

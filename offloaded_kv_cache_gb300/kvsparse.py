@@ -71,6 +71,7 @@ def load(path: str = LIB_PATH):
         "kv_device_status": (ctypes.c_int, [P]),
         "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv_debug_config": (ctypes.c_int, [i32, ctypes.c_uint64]),
+        "kv_stream_read_probe": (ctypes.c_int, [P, sz, P, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -177,3 +178,11 @@ def kv_status_string(code: int) -> str:
 def kv_debug_config(skip_page: int, wait_limit_ns: int, check=True):
     rc = load().kv_debug_config(int(skip_page), int(wait_limit_ns))
     return _ret(rc, "kv_debug_config", check)
+
+
+def kv_stream_read_probe(src, nbytes, sink, stream=None, check=True):
+    """Streaming 16-byte reads of `nbytes` from src (device or pinned host);
+    sink is a device int64 tensor with one word per thread block."""
+    rc = load().kv_stream_read_probe(_ptr(src), int(nbytes), _ptr(sink), int(sink.numel()),
+                                     _stream(stream))
+    return _ret(rc, "kv_stream_read_probe", check)
