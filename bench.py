@@ -356,58 +356,71 @@ def main():
 
     splits = kv.kv_attn_num_splits(layer.shape, spec.topk if sparse else 0)
     if sparse:
-        step = layer.sparse_step
         idx_np = layer.indices.cpu().numpy()
         step_bytes, attn_bytes = sparse_bytes(spec, ctx, idx_np)
+        stages = [("page_score", layer.score), ("topk_select", layer.select),
+                  ("sparse_attn", lambda: layer.sparse_attn())]
         launches_per_step = 2 + 1 + 1 + (1 if splits > 1 else 0)   # score, top-K, union, attn, combine
+        dominant = "sparse_attn"
     else:
-        step = layer.dense_step
         step_bytes = dense_bytes(spec, ctx)
+        stages = [("dense_attn", layer.dense_step)]
         launches_per_step = 1 + (1 if splits > 1 else 0)
         attn_bytes = step_bytes
+        dominant = "dense_attn"
 
-    def timed(fn, k, warm, attn_fn=None):
-        for i in range(warm):
-            layer.use_copy(i)
-            fn()
-        torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ka = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
-        kb = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
-        ev0.record(stream)
-        for i in range(k):
-            layer.use_copy(i)
-            if attn_fn is None:
-                ka[i].record(stream)
+    def capture(fns):
+        """One CUDA graph per stage and K/V copy (after eager warm-up calls)."""
+        graphs = {name: [] for name, _ in fns}
+        for c in range(copies):
+            layer.use_copy(c)
+            for name, fn in fns:
                 fn()
-                kb[i].record(stream)
-            else:
-                attn_fn(i, ka[i], kb[i])
-        ev1.record(stream)
+        torch.cuda.synchronize()
+        for c in range(copies):
+            layer.use_copy(c)
+            for name, fn in fns:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                    fn()
+                graphs[name].append(g)
+        torch.cuda.synchronize()
+        return graphs
+
+    def timed(fns, k, warm):
+        """Replays k steps (each step = every stage once, K/V copies rotating);
+        returns (total ms, {stage: mean ms}) from CUDA events on the stream."""
+        graphs = capture(fns)
+        names = [n for n, _ in fns]
+        for i in range(warm):
+            for n in names:
+                graphs[n][i % copies].replay()
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier()
-        total_ms = ev0.elapsed_time(ev1)
-        kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ka, kb))
-        return total_ms, kern_ms
-
-    def sparse_with_events(i, a, b):
-        layer.score()
-        layer.select()
-        a.record(stream)
-        layer.sparse_attn()
-        b.record(stream)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+              for _ in range(k)]
+        for i in range(k):
+            for si, n in enumerate(names):
+                ev[i][si].record(stream)
+                graphs[n][i % copies].replay()
+            ev[i][-1].record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        total = ev[0][0].elapsed_time(ev[-1][-1])
+        per = {n: statistics.mean(ev[i][si].elapsed_time(ev[i][si + 1]) for i in range(k))
+               for si, n in enumerate(names)}
+        return total, per
 
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
     clocks.mark_on()
-    total_ms, kern_ms = timed(step, args.steps, args.warmup,
-                              sparse_with_events if sparse else None)
+    total_ms, per_stage = timed(stages, args.steps, args.warmup)
     clocks.mark_off()
+    kern_ms = per_stage[dominant]
     t_local = total_ms
     if ws > 1:
         t = torch.tensor([t_local], device="cuda")
@@ -420,25 +433,19 @@ def main():
     # sustained window for the clock record when the timed region is short
     if rank == 0 and total_ms < 500:
         clocks.mark_on()
-        t_end = time.time() + 1.0
-        i = 0
-        while time.time() < t_end:
-            for _ in range(50):
-                layer.use_copy(i)
-                step()
-                i += 1
-            torch.cuda.synchronize()
+        timed(stages, max(20, int(args.steps * 600 / max(total_ms, 1e-3))), 3)
         clocks.mark_off()
     clocks.stop()
 
     # side measurements: dense pass for sparse workloads, index build
     extra = {}
     if sparse:
-        d_total, _ = timed(layer.dense_step, max(3, args.steps // 4), 3)
+        extra["stages_ms"] = {n: round(v, 5) for n, v in per_stage.items()}
+        d_total, _ = timed([("dense_attn", layer.dense_step)], max(3, args.steps // 4), 3)
         d_ms = d_total / max(3, args.steps // 4)
         db = dense_bytes(spec, ctx)
         extra["dense"] = {"ms_per_step": round(d_ms, 4), "GB_s": round(db / (d_ms * 1e-3) / 1e9, 2)}
-    ib_total, _ = timed(layer.build_index, max(3, args.steps // 4), 3)
+    ib_total, _ = timed([("index_build", layer.build_index)], max(3, args.steps // 4), 3)
     ib_ms = ib_total / max(3, args.steps // 4)
     kbytes = spec.num_kv_heads * int(np.sum(ctx)) * spec.head_dim * spec.elem_bytes
     table_bytes = int(np.sum(-(-ctx // spec.page_size))) * spec.num_kv_heads * 2 * spec.head_dim * spec.elem_bytes
@@ -453,14 +460,28 @@ def main():
     h2d = q_host.numel() * q_host.element_size() + ctx_host.numel() * 4
     d2h = out_host.numel() * 4
 
+    step = layer.sparse_step if sparse else layer.dense_step
+
     def e2e_step():
         layer.q.copy_(q_host, non_blocking=True)
         layer.context_lens.copy_(ctx_host, non_blocking=True)
         step()
         out_host.copy_(layer.out, non_blocking=True)
 
-    e_total, _ = timed(e2e_step, args.steps, args.warmup)
-    e_ms = e_total / args.steps
+    for i in range(args.warmup):
+        layer.use_copy(i)
+        e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        layer.use_copy(i)
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / args.steps
     if ws > 1:
         t = torch.tensor([e_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -505,7 +526,8 @@ def main():
                        "l2": (f"{copies} rotating K/V copies of {spec.kv_bytes() / 2**20:.0f} MiB "
                               f"each (> 4x the 129 MB L2 in total)" if copies > 1 else
                               "K/V larger than L2"),
-                       "splits": splits, "parallelism": f"replicas x{ws}"},
+                       "splits": splits, "timing": "CUDA-graph replays of each stage, events between",
+                       "parallelism": f"replicas x{ws}"},
             "queries_per_s": round(qps, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,

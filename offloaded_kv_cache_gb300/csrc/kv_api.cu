@@ -139,14 +139,44 @@ int header_bytes(long long list_pages) {
   return (int)((b + 1023) / 1024 * 1024);
 }
 
+// occupancy answers, cached per (device, kernel, threads, shared memory):
+// the calculator costs microseconds of host time per query
+struct OccEntry {
+  int dev, dtype, gc, mma, threads;
+  size_t smem;
+  int n;
+};
+std::mutex g_occ_mutex;
+OccEntry g_occ[64];
+int g_occ_n = 0;
+
+int cached_occupancy(int dtype, int gc, bool mma, int threads, size_t smem) {
+  const int dev = current_device();
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (int i = 0; i < g_occ_n; ++i) {
+      const OccEntry &e = g_occ[i];
+      if (e.dev == dev && e.dtype == dtype && e.gc == gc && e.mma == (int)mma &&
+          e.threads == threads && e.smem == smem)
+        return e.n;
+    }
+  }
+  const int n = mma ? attn_occupancy_mma(dtype, gc, threads, smem)
+                    : attn_occupancy_core(dtype, gc, threads, smem);
+  if (n > 0) {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    g_occ[g_occ_n % 64] = OccEntry{dev, dtype, gc, (int)mma, threads, smem, n};
+    if (g_occ_n < 64) ++g_occ_n;
+  }
+  return n;
+}
+
 // resident CTAs per SM: the occupancy calculator on the real kernel when a
 // device is present, else an estimate from shared memory and threads
 int resident_ctas(const Plan &pl, int dtype, bool have_device) {
   const int threads = 32 * (1 + pl.nw);
   int n = 0;
-  if (have_device)
-    n = pl.mma ? attn_occupancy_mma(dtype, pl.gc, threads, pl.smem)
-               : attn_occupancy_core(dtype, pl.gc, threads, pl.smem);
+  if (have_device) n = cached_occupancy(dtype, pl.gc, pl.mma, threads, pl.smem);
   if (n <= 0) {
     n = (int)((228 * 1024) / (pl.smem + 1024));
     n = std::min(n, 2048 / threads);

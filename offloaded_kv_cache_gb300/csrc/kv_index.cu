@@ -127,14 +127,18 @@ __device__ __forceinline__ void load4(const T *p, float (&x)[4]) {
 }
 
 constexpr int kScoreWarps = 8;
-constexpr int kScorePagesPerWarp = 4;
+constexpr int kScorePagesPerWarp = 8;
 
+// One warp scores kScorePagesPerWarp pages of one (b, kv head, head chunk):
+// the pages' block-table entries arrive in one load, every min/max load is
+// issued before any arithmetic, then each page's GS head sums are reduced.
 template <class T, int GS>
 __global__ void __launch_bounds__(32 * kScoreWarps)
     page_score_kernel(const T *__restrict__ q, const T *__restrict__ mm,
                       const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
                       float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
                       long long nphys, int nchunk, int *status) {
+  constexpr int PPW = kScorePagesPerWarp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z;
   const int kvh = blockIdx.y / nchunk, chunk = blockIdx.y % nchunk;
@@ -146,34 +150,47 @@ __global__ void __launch_bounds__(32 * kScoreWarps)
     return;
   }
   const int P = (len + ps - 1) / ps;
+  const int p0 = (blockIdx.x * kScoreWarps + warp) * PPW;  // this warp's first page
+  if (p0 >= maxP) return;
+
+  constexpr int kSpan = 32 / GS;     // lanes per head after the reduction
+  const int my_head = lane / kSpan;  // the head whose total this lane ends with
+  const bool writer = (lane % kSpan) == 0;
+  float *srow = scores + ((long long)b * Hq + head0 + my_head) * maxP;
+
+  // block-table entries of the warp's pages (lane i < PPW holds page p0 + i)
+  long long my_phys = -1;
+  if (lane < PPW && p0 + lane < P) {
+    const long long ph = bt[(long long)b * maxP + p0 + lane];
+    if (ph >= 0 && ph < nphys) my_phys = ph;
+    else flag_error(status, KV_ERR_BOUNDS);
+  }
+  float mn[PPW][4], mx[PPW][4];
+#pragma unroll
+  for (int i = 0; i < PPW; ++i) {
+    const long long phys = __shfl_sync(0xFFFFFFFFu, my_phys, i);
+    if (phys >= 0) {
+      const T *row = mm + ((phys * Hkv + kvh) * 2) * kHeadDim + 4 * lane;
+      load4(row, mn[i]);
+      load4(row + kHeadDim, mx[i]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mn[i][e] = mx[i][e] = 0.f;
+    }
+  }
   float qf[GS][4];
 #pragma unroll
   for (int g = 0; g < GS; ++g) load4(q + ((long long)b * Hq + head0 + g) * kHeadDim + 4 * lane, qf[g]);
 
-  constexpr int kSpan = 32 / GS;        // lanes per head after the reduction
-  const int my_head = lane / kSpan;     // the head whose total this lane ends with
-  const bool writer = (lane % kSpan) == 0;
-  float *srow = scores + ((long long)b * Hq + head0 + my_head) * maxP;
-
-  const int p0 = blockIdx.x * (kScoreWarps * kScorePagesPerWarp) + warp;
 #pragma unroll
-  for (int i = 0; i < kScorePagesPerWarp; ++i) {
-    const int p = p0 + i * kScoreWarps;
+  for (int i = 0; i < PPW; ++i) {
+    const int p = p0 + i;
     if (p >= maxP) break;
-    if (p >= P) {
+    const long long phys = __shfl_sync(0xFFFFFFFFu, my_phys, i);
+    if (phys < 0) {  // past the row's last page, or a bad entry
       if (writer) srow[p] = -INFINITY;
       continue;
     }
-    const long long phys = bt[(long long)b * maxP + p];
-    if (phys < 0 || phys >= nphys) {
-      if (lane == 0) flag_error(status, KV_ERR_BOUNDS);
-      if (writer) srow[p] = -INFINITY;
-      continue;
-    }
-    const T *row = mm + ((phys * Hkv + kvh) * 2) * kHeadDim + 4 * lane;
-    float mn[4], mx[4];
-    load4(row, mn);
-    load4(row + kHeadDim, mx);
     float part[GS];
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
@@ -181,13 +198,124 @@ __global__ void __launch_bounds__(32 * kScoreWarps)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         // max(q*mn, q*mx) == q * (q >= 0 ? mx : mn) because mx >= mn
-        const float bound = qf[g][e] >= 0.f ? mx[e] : mn[e];
+        const float bound = qf[g][e] >= 0.f ? mx[i][e] : mn[i][e];
         s = fmaf(qf[g][e], bound, s);
       }
       part[g] = s;
     }
     const float tot = reduce_heads<GS>(part, lane);
     if (writer) srow[p] = tot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// page score as a tensor-core contraction (16-bit data, 4 or 8 heads)
+// ---------------------------------------------------------------------------
+// max(q*mn, q*mx) == min(q, 0)*mn + max(q, 0)*mx, so over a group's GS heads
+// the scores of 16 pages are S[page][head] = T[page][0..256) . C[0..256)[head]
+// with T a page's [min | max] row (the table's own layout) and C the
+// [q- | q+] coefficients -- a 16 x 8 x 256 mma.sync contraction.  Products of
+// two 16-bit values are exact in fp32; sums accumulate in fp32.
+//
+// k order: lane (gid, tig) loads 16-byte chunks ch = tig + 4 i (i = 0..7) of
+// rows gid and gid + 8; chunk i supplies k-steps 2i and 2i + 1, whose slots
+// (2tig, 2tig+1, 2tig+8, 2tig+9) take the chunk's elements 0..3 and 4..7.
+// The q coefficients follow the same permutation, so every global load is a
+// coalesced 16-byte load straight into an A fragment.
+__device__ __forceinline__ void mma_score(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1, __nv_bfloat16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_score(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1, __half) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// keep the halves of a packed 16-bit pair whose sign is set (neg) or clear
+__device__ __forceinline__ uint32_t sign_part(uint32_t w, bool neg) {
+  const uint32_t s = (w >> 15) & 0x00010001u;  // 1 per negative half
+  const uint32_t m = (neg ? s : (s ^ 0x00010001u)) * 0xFFFFu;
+  return w & m;
+}
+
+constexpr int kScoreMmaWarps = 8;
+
+template <class T, int GS>
+__global__ void __launch_bounds__(32 * kScoreMmaWarps)
+    page_score_mma_kernel(const T *__restrict__ q, const T *__restrict__ mm,
+                          const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
+                          float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
+                          long long nphys, int nchunk, int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int b = blockIdx.z;
+  const int kvh = blockIdx.y / nchunk, chunk = blockIdx.y % nchunk;
+  const int G = Hq / Hkv;
+  const int head0 = kvh * G + chunk * GS;
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int P = (len + ps - 1) / ps;
+  const int p0 = (blockIdx.x * kScoreMmaWarps + warp) * 16;  // this warp's 16 pages
+  if (p0 >= maxP) return;
+
+  // physical pages of rows gid and gid + 8 (lanes 0..15 load the 16 entries)
+  long long ph_lane = -1;
+  if (lane < 16 && p0 + lane < P) {
+    const long long ph = bt[(long long)b * maxP + p0 + lane];
+    if (ph >= 0 && ph < nphys) ph_lane = ph;
+    else flag_error(status, KV_ERR_BOUNDS);
+  }
+  const long long ph_a = __shfl_sync(0xFFFFFFFFu, ph_lane, gid);
+  const long long ph_b = __shfl_sync(0xFFFFFFFFu, ph_lane, gid + 8);
+  uint4 ra[8], rb[8];
+  const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * 2 * kHeadDim);
+  const uint4 *rowb = reinterpret_cast<const uint4 *>(mm + ((ph_b < 0 ? 0 : ph_b) * Hkv + kvh) * 2 * kHeadDim);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ra[i] = ph_a >= 0 ? rowa[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
+    rb[i] = ph_b >= 0 ? rowb[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // coefficients [q- | q+] of head gid in the same k order
+  uint4 cf[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cf[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (gid < GS) {
+      const int ch = tig + 4 * i;  // chunk of the 256-long [q- | q+] row
+      const uint4 w = reinterpret_cast<const uint4 *>(
+          q + ((long long)b * Hq + head0 + gid) * kHeadDim)[ch & 15];
+      const bool neg = ch < 16;
+      cf[i] = make_uint4(sign_part(w.x, neg), sign_part(w.y, neg), sign_part(w.z, neg),
+                         sign_part(w.w, neg));
+    }
+  }
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a0[4] = {ra[i].x, rb[i].x, ra[i].y, rb[i].y};
+    mma_score(c, a0, cf[i].x, cf[i].y, T());
+    const uint32_t a1[4] = {ra[i].z, rb[i].z, ra[i].w, rb[i].w};
+    mma_score(c, a1, cf[i].z, cf[i].w, T());
+  }
+  // c0/c1: page gid, heads 2tig / 2tig+1; c2/c3: page gid + 8
+  const int pa = p0 + gid, pb = pa + 8;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int h = 2 * tig + (e & 1);
+    const int p = (e < 2) ? pa : pb;
+    const bool ok = (e < 2) ? ph_a >= 0 : ph_b >= 0;
+    if (h < GS && p < maxP)
+      scores[((long long)b * Hq + head0 + h) * maxP + p] = ok ? c[e] : -INFINITY;
   }
 }
 
@@ -198,6 +326,18 @@ cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, con
   const int G = Hq / Hkv;
   const int gs = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
   const int nchunk = G / gs;
+  if constexpr (sizeof(T) == 2) {
+    if (gs >= 4) {  // a tokens-free pages x heads x 256 contraction: tensor cores
+      dim3 g((maxP + 16 * kScoreMmaWarps - 1) / (16 * kScoreMmaWarps), Hkv * nchunk, B);
+      const T *qq = static_cast<const T *>(q);
+      const T *m = static_cast<const T *>(mm);
+      if (gs == 8)
+        page_score_mma_kernel<T, 8><<<g, 32 * kScoreMmaWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status);
+      else
+        page_score_mma_kernel<T, 4><<<g, 32 * kScoreMmaWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status);
+      return cudaGetLastError();
+    }
+  }
   dim3 grid((maxP + kScoreWarps * kScorePagesPerWarp - 1) / (kScoreWarps * kScorePagesPerWarp),
             Hkv * nchunk, B);
   const T *qq = static_cast<const T *>(q);

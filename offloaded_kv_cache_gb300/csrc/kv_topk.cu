@@ -10,7 +10,7 @@
 namespace kvs {
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -18,40 +18,44 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return key32(__float_as_uint(s + 0.0f));
 }
 
-// Exclusive prefix count of `flag` over the block in thread order; *total
-// receives the block-wide count.  Two block barriers.
-__device__ __forceinline__ int block_excl_count(bool flag, int *warp_tot, int *total) {
+// Exclusive prefix sum over the warps of the block of one 64-bit value per
+// warp (lane 0's argument counts); returns the warp's base, *total the sum.
+// Two block barriers; `wsum` holds one slot per warp.
+template <int WARPS>
+__device__ __forceinline__ unsigned long long warp_bases64(unsigned long long v,
+                                                           unsigned long long *wsum,
+                                                           unsigned long long *total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const unsigned bal = __ballot_sync(0xFFFFFFFFu, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[warp] = __popc(bal);
+  if (lane == 0) wsum[warp] = v;
   __syncthreads();
-  int off = 0, tot = 0;
-#pragma unroll 8
-  for (int w = 0; w < kTopkWarps; ++w) {
-    const int t = warp_tot[w];
-    off += w < warp ? t : 0;
+  unsigned long long base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < WARPS; ++w) {
+    const unsigned long long t = wsum[w];
+    base += w < warp ? t : 0ull;
     tot += t;
   }
   __syncthreads();
   *total = tot;
-  return off + in_warp;
+  return base;
 }
 
 // One CTA per (b, h) row.  Radix select of the K-th largest key, 8 bits per
-// pass from the top, over keys cached in shared memory (or re-read from the
-// L2-resident score row when the row does not fit); the digit search is one
-// warp scanning the 256-bin histogram; the final pass compacts the selected
-// pages in index order with ballots.
+// pass from the top (a shared-memory histogram whose threshold digit one warp
+// finds with a shuffle scan), stopping early once every key of the threshold
+// bin is taken.  The output pass splits the pages into one contiguous segment
+// per warp; each warp walks its segment 32 pages at a time and places the
+// selected pages in index order with ballots, after one block scan of the
+// per-warp counts.  Equal keys at the threshold go to the lower page index.
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx, int Hq, int ps,
                 int maxP, int K, int keys_in_smem, int32_t *__restrict__ out, int *status) {
   extern __shared__ uint32_t skeys[];
   __shared__ uint32_t hist[256];
-  __shared__ int warp_tot[kTopkWarps];
+  __shared__ unsigned long long wsum[kTopkWarps];
   __shared__ uint32_t s_digit;
-  __shared__ int s_krem;
-  const int tid = threadIdx.x;
+  __shared__ int s_krem, s_all;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long row = blockIdx.x;
   const int b = (int)(row / Hq);
   int32_t *orow = out + row * K;
@@ -70,17 +74,17 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   if (keys_in_smem) {
     for (int p = tid; p < P; p += kTopkThreads) skeys[p] = score_key(srow[p]);
-    __syncthreads();
   }
   auto key_at = [&](int p) -> uint32_t {
     return keys_in_smem ? skeys[p] : score_key(srow[p]);
   };
 
   uint32_t prefix = 0, pmask = 0;
-  int krem = keff;  // how many of the keys matching `prefix` still have to be taken
+  int krem = keff;  // keys matching `prefix` that still have to be taken
+  bool all_taken = false;
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    hist[tid] = 0;  // kTopkThreads == 256 bins
     __syncthreads();
     for (int p = tid; p < P; p += kTopkThreads) {
       const uint32_t k = key_at(p);
@@ -101,13 +105,14 @@ __global__ void __launch_bounds__(kTopkThreads)
         const int t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
         if (tid >= off) incl += t;
       }
-      int above = incl - sum;  // keys whose digit beats this lane's range
+      int above = incl - sum;
       if (above < krem && krem <= incl) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (above + c[j] >= krem) {
             s_digit = (uint32_t)(255 - 8 * tid - j);
             s_krem = krem - above;
+            s_all = (above + c[j] == krem) ? 1 : 0;
             break;
           }
           above += c[j];
@@ -118,24 +123,43 @@ __global__ void __launch_bounds__(kTopkThreads)
     prefix |= s_digit << shift;
     pmask |= 255u << shift;
     krem = s_krem;
+    if (s_all) {
+      all_taken = true;  // every key with this prefix is selected
+      break;
+    }
   }
-  // prefix is now the K-th largest key; krem keys equal to it are taken,
-  // lowest page index first.
-  const uint32_t tau = prefix;
-  int eq_carry = 0, sel_carry = 0;
-#pragma unroll 1
-  for (int base = 0; base < P; base += kTopkThreads) {
-    const int p = base + tid;
-    const uint32_t k = p < P ? key_at(p) : 0u;
-    const bool eq = p < P && k == tau;
-    const bool gt = p < P && k > tau;
-    int eq_tot, sel_tot;
-    const int eq_rank = block_excl_count(eq, warp_tot, &eq_tot);
-    const bool sel = gt || (eq && eq_carry + eq_rank < krem);
-    const int pos = block_excl_count(sel, warp_tot, &sel_tot);
-    if (sel && sel_carry + pos < K) orow[sel_carry + pos] = p;
-    eq_carry += eq_tot;
-    sel_carry += sel_tot;
+  // selected: keys whose masked value beats the prefix, plus those equal to
+  // it -- all of them when all_taken, else the first krem in page order
+  const int seg = ((P + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;  // pages per warp
+  const int lo = warp * seg, hi = min(P, lo + seg);
+  uint32_t gt_n = 0, eq_n = 0;
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
+    gt_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k > prefix));
+    eq_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k == prefix));
+  }
+  unsigned long long tot;
+  const unsigned long long base =
+      warp_bases64<kTopkWarps>(((unsigned long long)eq_n << 32) | gt_n, wsum, &tot);
+  long long gt_b = (long long)(base & 0xFFFFFFFFull);
+  long long eq_b = (long long)(base >> 32);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
+    const unsigned gtb = __ballot_sync(0xFFFFFFFFu, p < hi && k > prefix);
+    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, p < hi && k == prefix);
+    const long long my_gt = gt_b + __popc(gtb & lt_mask);
+    const long long my_eq = eq_b + __popc(eqb & lt_mask);
+    const bool is_gt = (gtb >> lane) & 1u, is_eq = (eqb >> lane) & 1u;
+    const bool sel = is_gt || (is_eq && (all_taken || my_eq < krem));
+    if (sel) {
+      const long long pos = my_gt + (all_taken ? my_eq : min(my_eq, (long long)krem));
+      if (pos < K) orow[pos] = p;
+    }
+    gt_b += __popc(gtb);
+    eq_b += __popc(eqb);
   }
   for (int i = keff + tid; i < K; i += kTopkThreads) orow[i] = -1;
 }
@@ -143,14 +167,15 @@ __global__ void __launch_bounds__(kTopkThreads)
 // ---------------------------------------------------------------------------
 // union of the selected pages of the gc heads of one (b, kv head, head chunk)
 // ---------------------------------------------------------------------------
-constexpr int kUnionThreads = 512;
+constexpr int kUnionThreads = 256;
+constexpr int kUnionWarps = kUnionThreads / 32;
 
 __global__ void __launch_bounds__(kUnionThreads)
     union_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ ctx, int Hq, int G,
                  int gc, int ps, int maxP, int K, int umax, int32_t *__restrict__ upages,
                  uint32_t *__restrict__ umasks, int32_t *__restrict__ ucount, int *status) {
   extern __shared__ uint32_t words[];  // one byte of head bits per page, 4 pages a word
-  __shared__ int warp_tot[kUnionThreads / 32];
+  __shared__ unsigned long long wsum[kUnionWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = blockIdx.x, b = blockIdx.y;
   const int nchunk = G / gc;
@@ -180,48 +205,88 @@ __global__ void __launch_bounds__(kUnionThreads)
     atomicOr(&words[p >> 2], (1u << g) << ((p & 3) * 8));
   }
   __syncthreads();
-  int carry = 0;
-  for (int base = 0; base < P; base += kUnionThreads) {
-    const int p = base + tid;
-    const uint32_t m = p < P ? (words[p >> 2] >> ((p & 3) * 8)) & 0xFFu : 0u;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, m != 0u);
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    int off = 0, tot = 0;
-    for (int w = 0; w < kUnionThreads / 32; ++w) {
-      off += w < warp ? warp_tot[w] : 0;
-      tot += warp_tot[w];
-    }
-    __syncthreads();
-    const int pos = carry + off + __popc(bal & ((1u << lane) - 1u));
-    if (m != 0u && pos < umax) {
-      upages[gbase * umax + pos] = p;
-      umasks[gbase * umax + pos] = m;
-    }
-    carry += tot;
+  // one contiguous segment of pages per warp, walked 32 pages at a time
+  const int seg = ((P + kUnionWarps - 1) / kUnionWarps + 31) / 32 * 32;
+  const int lo = warp * seg, hi = min(P, lo + seg);
+  unsigned long long n = 0;
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    const uint32_t m = p < hi ? (words[p >> 2] >> ((p & 3) * 8)) & 0xFFu : 0u;
+    n += __popc(__ballot_sync(0xFFFFFFFFu, m != 0u));
   }
-  if (tid == 0) ucount[gbase] = min(carry, umax);
+  unsigned long long tot;
+  unsigned long long pos = warp_bases64<kUnionWarps>(n, wsum, &tot);
+  for (int p0 = lo; p0 < hi; p0 += 32) {
+    const int p = p0 + lane;
+    const uint32_t m = p < hi ? (words[p >> 2] >> ((p & 3) * 8)) & 0xFFu : 0u;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, m != 0u);
+    const unsigned long long my = pos + __popc(bal & ((1u << lane) - 1u));
+    if (m != 0u && my < (unsigned long long)umax) {
+      upages[gbase * umax + my] = p;
+      umasks[gbase * umax + my] = m;
+    }
+    pos += __popc(bal);
+  }
+  if (tid == 0) ucount[gbase] = (int)min(tot, (unsigned long long)umax);
 }
 
 // ---------------------------------------------------------------------------
 // split-K combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
 // ---------------------------------------------------------------------------
+// One CTA per (b, q head), one thread per output channel.  The split maxima
+// and weights are staged once in shared memory; the partial outputs are then
+// read with independent loads.
+constexpr int kMaxCombineSplits = 1024;
+
 __global__ void __launch_bounds__(kHeadDim)
     combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                    float *__restrict__ out, int S, long long rows) {
+  __shared__ float w[kMaxCombineSplits];
+  __shared__ float red[kHeadDim / 32];
+  __shared__ float s_M, s_l;
   const long long r = blockIdx.x;
-  const int c = threadIdx.x;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, part_ml[(s * rows + r) * 2]);
-  float o = 0.f, l = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float m = part_ml[(s * rows + r) * 2];
-      const float w = m == -INFINITY ? 0.f : ex2(m - M);
-      o = fmaf(w, part_o[(s * rows + r) * kHeadDim + c], o);
-      l = fmaf(w, part_ml[(s * rows + r) * 2 + 1], l);
-    }
+  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  float m_loc = -INFINITY;
+  for (int s = c; s < S; s += kHeadDim) {
+    const float m = part_ml[(s * rows + r) * 2];
+    w[s] = m;
+    m_loc = fmaxf(m_loc, m);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m_loc = fmaxf(m_loc, __shfl_xor_sync(0xFFFFFFFFu, m_loc, off));
+  if (lane == 0) red[warp] = m_loc;
+  __syncthreads();
+  if (c == 0) {
+    float M = red[0];
+    for (int i = 1; i < kHeadDim / 32; ++i) M = fmaxf(M, red[i]);
+    s_M = M;
+  }
+  __syncthreads();
+  const float M = s_M;
+  float l_loc = 0.f;
+  for (int s = c; s < S; s += kHeadDim) {
+    const float m = w[s];
+    const float f = (M == -INFINITY || m == -INFINITY) ? 0.f : ex2(m - M);
+    w[s] = f;
+    l_loc = fmaf(f, part_ml[(s * rows + r) * 2 + 1], l_loc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l_loc += __shfl_xor_sync(0xFFFFFFFFu, l_loc, off);
+  __syncthreads();
+  if (lane == 0) red[warp] = l_loc;
+  __syncthreads();
+  if (c == 0) {
+    float l = 0.f;
+    for (int i = 0; i < kHeadDim / 32; ++i) l += red[i];
+    s_l = l;
+  }
+  __syncthreads();
+  float o = 0.f;
+  const float *po = part_o + r * kHeadDim + c;
+  const long long stride = rows * kHeadDim;
+#pragma unroll 8
+  for (int s = 0; s < S; ++s) o = fmaf(w[s], po[s * stride], o);
+  const float l = s_l;
   out[r * kHeadDim + c] = l > 0.f ? o / l : 0.f;
 }
 
@@ -229,7 +294,8 @@ __global__ void __launch_bounds__(kHeadDim)
 
 cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
                         int k, int32_t *indices, int *status, cudaStream_t st) {
-  constexpr size_t kMaxSmemKeys = 48 * 1024 / 4;  // keys cached in shared memory
+  // keys cached in shared memory, within the default 48 KB per block
+  constexpr size_t kMaxSmemKeys = 11264;
   const int in_smem = (size_t)maxP <= kMaxSmemKeys ? 1 : 0;
   const size_t smem = in_smem ? (size_t)maxP * 4 : 0;
   topk_kernel<<<(unsigned)((long long)B * Hq), kTopkThreads, smem, st>>>(scores, ctx, Hq, ps, maxP,

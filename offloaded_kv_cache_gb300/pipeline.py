@@ -92,31 +92,41 @@ class DecodeLayer:
         self.k_cache = self.k_copies[i % len(self.k_copies)]
         self.v_cache = self.v_copies[i % len(self.v_copies)]
 
-    # --- steps -------------------------------------------------------------
+    # --- steps (on torch's current stream unless one is given) ---------------
+    @staticmethod
+    def _st(stream):
+        return torch.cuda.current_stream() if stream is None else stream
+
     def build_index(self, stream=None):
+        stream = self._st(stream)
         kv.kv_page_minmax_build(self.shape, self.k_cache, self.block_table, self.context_lens,
                                 self.minmax, stream)
 
     def score(self, stream=None):
+        stream = self._st(stream)
         kv.kv_page_score(self.shape, self.q, self.minmax, self.block_table, self.context_lens,
                          self.scores, stream)
 
     def select(self, stream=None):
+        stream = self._st(stream)
         kv.kv_topk_select(self.shape, self.scores, self.context_lens, self.topk, self.indices,
                           self.workspace, self.workspace.numel(), stream)
 
     def sparse_attn(self, indices=None, stream=None):
+        stream = self._st(stream)
         idx = self.indices if indices is None else indices
         kv.kv_sparse_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
                                  self.context_lens, idx, idx.shape[-1], self.scale, self.out,
                                  self.workspace, self.workspace.numel(), stream)
 
     def sparse_step(self, stream=None):
+        stream = self._st(stream)
         self.score(stream)
         self.select(stream)
         self.sparse_attn(stream=stream)
 
     def dense_step(self, stream=None):
+        stream = self._st(stream)
         kv.kv_dense_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
                                 self.context_lens, self.scale, self.out, self.workspace,
                                 self.workspace.numel(), stream)
