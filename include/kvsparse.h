@@ -69,7 +69,8 @@ typedef enum { KV_LOC_HBM = 0, KV_LOC_HOST_PINNED = 1 } kv_location;
 typedef enum {
   KV_OK = 0,
   KV_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad shape, k < 1      */
-  KV_ERR_UNSUPPORTED = -2,    /* d != 128, ps not in {16, 64}, unknown dtype    */
+  KV_ERR_UNSUPPORTED = -2,    /* d != 128, ps not in {16, 64}, unknown dtype,
+                                 max_pages_per_seq > 524288 (attention)      */
   KV_ERR_LOCATION = -3,       /* K/V memory does not match kv_loc               */
   KV_ERR_WORKSPACE = -4,      /* workspace null or smaller than required        */
   KV_ERR_CUDA = -5,           /* a CUDA runtime call or launch failed           */

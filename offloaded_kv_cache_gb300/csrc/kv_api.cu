@@ -119,10 +119,10 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 //  * deep: four consumer warps double-buffered over an 8-stage ring (4 for
 //    fp32), split along the context when there are few long units.
 #ifndef KVS_WIDE_NW
-#define KVS_WIDE_NW 2
+#define KVS_WIDE_NW 3
 #endif
 #ifndef KVS_WIDE_NS
-#define KVS_WIDE_NS 2
+#define KVS_WIDE_NS 3
 #endif
 #ifndef KVS_DEEP_NW
 #define KVS_DEEP_NW 4
@@ -134,8 +134,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 #define KVS_SPLIT_OVERHEAD_TILES 4  // fixed cost of a CTA, in tiles, for the split choice
 #endif
 
-int header_bytes(long long list_pages) {
-  const long long b = 4096 + 8 * std::min<long long>(list_pages, kMaxListPages);
+int header_bytes(const Plan &pl, int elem, long long list_pages) {
+  const long long b = attn_fixed_header(elem, pl.gc, pl.mma) +
+                      8 * std::min<long long>(list_pages, kMaxListPages);
   return (int)((b + 1023) / 1024 * 1024);
 }
 
@@ -211,7 +212,7 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
   wide.nw = KVS_WIDE_NW;
   wide.nstages = KVS_WIDE_NS;
   wide.S = 1;
-  wide.header = header_bytes(work);
+  wide.header = header_bytes(wide, elem_bytes(s->dtype), work);
   wide.smem = 1024 + wide.header + (size_t)wide.nstages * stage;
   // wide when the units alone keep enough K/V bytes in flight on every SM
   // (about 96 KB) without splitting them
@@ -230,7 +231,7 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
     ns = std::max(ns, 2 * pl.nw);
     ns = std::min(ns, kMaxStages / pl.nw * pl.nw);
     pl.nstages = ns;
-    pl.header = header_bytes(kMaxListPages);
+    pl.header = header_bytes(pl, elem_bytes(s->dtype), kMaxListPages);
     pl.smem = 1024 + pl.header + (size_t)ns * stage;
     const long long slots = (long long)sms * resident_ctas(pl, s->dtype, have_device);
     // split count minimising (waves x tiles per CTA) plus a fixed cost per
@@ -252,7 +253,7 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
 #endif
     pl.S = bestS;
     // a smaller page list leaves more shared memory
-    pl.header = header_bytes((work + pl.S - 1) / pl.S);
+    pl.header = header_bytes(pl, elem_bytes(s->dtype), (work + pl.S - 1) / pl.S);
     pl.smem = 1024 + pl.header + (size_t)ns * stage;
   }
   pl.umax = k > 0 ? (int)work : 0;
@@ -274,6 +275,41 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
     off = align256(off + ng * 4);
   }
   pl.total = off;
+  return pl;
+}
+
+// Plans depend only on (device, shape, k): cache them, since the split search
+// and the occupancy query cost host time on every call.
+struct PlanEntry {
+  int dev, k;
+  kv_shape shape;
+  Plan plan;
+};
+std::mutex g_plan_mutex;
+PlanEntry g_plans[32];
+int g_plan_n = 0;
+
+bool same_shape(const kv_shape &x, const kv_shape &y) {
+  return x.batch == y.batch && x.num_q_heads == y.num_q_heads &&
+         x.num_kv_heads == y.num_kv_heads && x.head_dim == y.head_dim &&
+         x.page_size == y.page_size && x.max_pages_per_seq == y.max_pages_per_seq &&
+         x.num_phys_pages == y.num_phys_pages && x.dtype == y.dtype && x.kv_loc == y.kv_loc;
+}
+
+Plan cached_plan(const kv_shape *s, int k) {
+  const int dev = current_device();
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    for (int i = 0; i < std::min(g_plan_n, 32); ++i)
+      if (g_plans[i].dev == dev && g_plans[i].k == k && same_shape(g_plans[i].shape, *s))
+        return g_plans[i].plan;
+  }
+  const Plan pl = make_plan(s, k, dev >= 0 ? sm_count(dev) : 152, dev >= 0);
+  if (dev >= 0) {
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    g_plans[g_plan_n % 32] = PlanEntry{dev, k, *s, pl};
+    ++g_plan_n;
+  }
   return pl;
 }
 
@@ -324,12 +360,15 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
   if (indices && (long long)(s->max_pages_per_seq + 3) / 4 * 4 > 200 * 1024)
     return KV_ERR_UNSUPPORTED;
+  // a row's pages are spread over at most 1024 splits of at most
+  // kMaxListPages pages each
+  if ((long long)s->max_pages_per_seq > 1024LL * kMaxListPages) return KV_ERR_UNSUPPORTED;
   const int dev = current_device();
   if (dev < 0) return KV_ERR_CUDA;
   const void *kd = nullptr, *vd = nullptr;
   if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
   if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
-  const Plan pl = make_plan(s, indices ? k : 0, sm_count(dev), true);
+  const Plan pl = cached_plan(s, indices ? k : 0);
   if (pl.total > 0 && (ws == nullptr || ws_bytes < pl.total || !al16(ws))) return KV_ERR_WORKSPACE;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
@@ -461,16 +500,12 @@ int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *co
 
 size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k) {
   if (check_shape(shape) != KV_OK || k < 0) return 0;
-  const int dev = current_device();
-  const int sms = dev >= 0 ? sm_count(dev) : 152;
-  return make_plan(shape, k, sms, dev >= 0).total;
+  return cached_plan(shape, k).total;
 }
 
 int32_t kv_attn_num_splits(const kv_shape *shape, int32_t k) {
   if (check_shape(shape) != KV_OK || k < 0) return 0;
-  const int dev = current_device();
-  const int sms = dev >= 0 ? sm_count(dev) : 152;
-  return make_plan(shape, k, sms, dev >= 0).S;
+  return cached_plan(shape, k).S;
 }
 
 int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,

@@ -41,9 +41,8 @@
 
 namespace kvs {
 
-// shared memory before the ring: [0, 4096) barriers, q and weights; then the
-// page list (a.header_bytes in total, a multiple of 1024)
-constexpr int kFixedHeaderBytes = 4096;
+// shared memory before the ring: barriers, q and weights (attn_fixed_header),
+// then the page list (a.header_bytes in total, a multiple of 1024)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -124,7 +123,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   uint64_t *empty = full + kMaxStages;
   float *q_s = reinterpret_cast<float *>(smem + 256);  // CUDA core: [GC][SL][QSTR]
   float *pbuf = q_s + GC * SL * QSTR;                  // CUDA core: [warps][GC][TP]
-  PageEnt *plist = reinterpret_cast<PageEnt *>(smem + kFixedHeaderBytes);
+  PageEnt *plist = reinterpret_cast<PageEnt *>(smem + attn_fixed_header(SL, GC, MMA));
   uint8_t *stages = smem + a.header_bytes;
 
   constexpr int TT = kTileTokens;            // tokens per tile (stage)

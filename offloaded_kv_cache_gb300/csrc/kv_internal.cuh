@@ -193,6 +193,16 @@ struct AttnArgs {
 constexpr int kMaxConsumerWarps = 4;
 constexpr int kAttnMaxThreads = 32 * (1 + kMaxConsumerWarps);
 constexpr int kMaxListPages = 512;
+
+// Bytes of an attention CTA's shared memory before its page list: mbarriers,
+// then (CUDA-core path) q in fp32 and the per-warp weight buffers.  The page
+// list follows; the stage ring starts at the next 1024-byte boundary.
+__host__ __device__ inline int attn_fixed_header(int elem_bytes, int gc, bool mma) {
+  const int SL = elem_bytes, QSTR = 128 / elem_bytes + 4, TP = 32 / SL;
+  int off = 256;
+  if (!mma) off += gc * SL * QSTR * 4 + 4 * gc * TP * 4;  // q_s + pbuf (<= 4 warps)
+  return (off + 255) & ~255;
+}
 constexpr int kMaxStages = 16;
 
 // launchers (return a cudaError_t)

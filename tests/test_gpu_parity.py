@@ -195,7 +195,7 @@ def test_bounded_wait_times_out_and_context_survives():
                        index=2700)
     wl = W.generate(spec)
     layer = DecodeLayer(wl, topk=4)
-    kv.kv_debug_config(1, 50_000_000)       # page 1 of every CTA is never filled; 50 ms limit
+    kv.kv_debug_config(0, 50_000_000)       # tile 0 of every CTA is never filled; 50 ms limit
     try:
         layer.dense_step()
         assert kv.kv_device_status() == kv.KV_ERR_DEVICE_TIMEOUT
