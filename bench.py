@@ -369,49 +369,55 @@ def main():
         attn_bytes = step_bytes
         dominant = "dense_attn"
 
-    def capture(fns):
-        """One CUDA graph per stage and K/V copy (after eager warm-up calls)."""
-        graphs = {name: [] for name, _ in fns}
+    R = 10  # steps per captured graph (amortises the graph launch itself)
+
+    def capture(fn, n):
+        """A CUDA graph of n consecutive calls of fn, K/V copies rotating
+        (after eager warm-up calls of every copy)."""
         for c in range(copies):
             layer.use_copy(c)
-            for name, fn in fns:
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for i in range(n):
+                layer.use_copy(i)
                 fn()
         torch.cuda.synchronize()
-        for c in range(copies):
-            layer.use_copy(c)
-            for name, fn in fns:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, capture_error_mode="relaxed"):
-                    fn()
-                graphs[name].append(g)
+        return g
+
+    def run_steps(fn, k, warm):
+        """Exactly k calls of fn on the device (graphs of R calls, then single
+        calls), after warm calls; returns device ms for the k calls."""
+        g_r = capture(fn, R)
+        g_1 = capture(fn, 1)
+        for _ in range(max(1, warm // R)):
+            g_r.replay()
         torch.cuda.synchronize()
-        return graphs
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k // R):
+            g_r.replay()
+        for _ in range(k % R):
+            g_1.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        return e0.elapsed_time(e1)
 
     def timed(fns, k, warm):
-        """Replays k steps (each step = every stage once, K/V copies rotating);
-        returns (total ms, {stage: mean ms}) from CUDA events on the stream."""
-        graphs = capture(fns)
-        names = [n for n, _ in fns]
-        for i in range(warm):
-            for n in names:
-                graphs[n][i % copies].replay()
-        torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-              for _ in range(k)]
-        for i in range(k):
-            for si, n in enumerate(names):
-                ev[i][si].record(stream)
-                graphs[n][i % copies].replay()
-            ev[i][-1].record(stream)
-        torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
-        total = ev[0][0].elapsed_time(ev[-1][-1])
-        per = {n: statistics.mean(ev[i][si].elapsed_time(ev[i][si + 1]) for i in range(k))
-               for si, n in enumerate(names)}
+        """The step (every stage once) k times, then each stage alone k times
+        (its mean duration); returns (total ms of the k steps, {stage: ms})."""
+        def step_fn():
+            for _, f in fns:
+                f()
+        total = run_steps(step_fn, k, warm)
+        per = {n: run_steps(f, k, warm) / k for n, f in fns} if len(fns) > 1 else \
+            {fns[0][0]: total / k}
         return total, per
 
     clocks = ClockSampler(local)
@@ -526,7 +532,9 @@ def main():
                        "l2": (f"{copies} rotating K/V copies of {spec.kv_bytes() / 2**20:.0f} MiB "
                               f"each (> 4x the 129 MB L2 in total)" if copies > 1 else
                               "K/V larger than L2"),
-                       "splits": splits, "timing": "CUDA-graph replays of each stage, events between",
+                       "splits": splits,
+                       "timing": ("CUDA events around exactly K steps replayed as CUDA graphs of "
+                                  f"{R} steps; per-kernel times from graphs of each stage alone"),
                        "parallelism": f"replicas x{ws}"},
             "queries_per_s": round(qps, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),

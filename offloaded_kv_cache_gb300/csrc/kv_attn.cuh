@@ -110,6 +110,7 @@ template <class T, int GC, bool MMA>
 __global__ void __launch_bounds__(kAttnMaxThreads)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv) {
+  pdl_wait();
   constexpr int SL = (int)sizeof(T);        // 128-byte slabs per 128-element row
   constexpr int EPS = 128 / (int)sizeof(T); // elements per slab
   constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
@@ -479,6 +480,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
 
   // ======================= merge the consumer warps =======================
   __syncthreads();  // every stage is consumed (or abandoned): reuse the ring
+  pdl_trigger();
   float *mw = reinterpret_cast<float *>(stages);  // [warps][GC] (at most 64)
   float *lw = mw + 64;                            // [warps][GC]
   float *ow = mw + 128;                           // [warps][GC][128], 16-byte aligned
@@ -561,8 +563,7 @@ cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap *tk, const CUtens
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  kern<<<grid, 32 * (1 + a.nw), smem, st>>>(a, *tk, *tv);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(32 * (1 + a.nw)), smem, st, a, *tk, *tv);
 }
 
 template <class T, int GC, bool MMA>

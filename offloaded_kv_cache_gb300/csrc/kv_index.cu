@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256)
     minmax_build_kernel(const T *__restrict__ k, const int32_t *__restrict__ bt,
                         const int32_t *__restrict__ ctx, T *__restrict__ mm, int B, int Hkv,
                         int ps, int maxP, long long nphys, int *status) {
+  pdl_wait();
   constexpr int C = kHeadDim * (int)sizeof(T) / 16;  // 16-byte chunks per row
   constexpr int RG = 32 / C;                          // row groups per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(256)
       hi.x = max(hi.x, x.x); hi.y = max(hi.y, x.y); hi.z = max(hi.z, x.z); hi.w = max(hi.w, x.w);
     }
   }
+  pdl_trigger();
   if constexpr (RG == 2) {
     // merge the two row groups (lanes l and l ^ 16 hold the same chunk)
     uint4 lo2, hi2;
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(32 * kScoreWarps)
                       const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
                       float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
                       long long nphys, int nchunk, int *status) {
+  pdl_wait();
   constexpr int PPW = kScorePagesPerWarp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z;
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
                           const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
                           float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
                           long long nphys, int nchunk, int *status) {
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int b = blockIdx.z;
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
                          sign_part(w.w, neg));
     }
   }
+  pdl_trigger();
   float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -331,24 +336,21 @@ cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, con
       dim3 g((maxP + 16 * kScoreMmaWarps - 1) / (16 * kScoreMmaWarps), Hkv * nchunk, B);
       const T *qq = static_cast<const T *>(q);
       const T *m = static_cast<const T *>(mm);
-      if (gs == 8)
-        page_score_mma_kernel<T, 8><<<g, 32 * kScoreMmaWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status);
-      else
-        page_score_mma_kernel<T, 4><<<g, 32 * kScoreMmaWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status);
-      return cudaGetLastError();
+      auto kern = gs == 8 ? page_score_mma_kernel<T, 8> : page_score_mma_kernel<T, 4>;
+      return launch_pdl(kern, g, dim3(32 * kScoreMmaWarps), 0, st, qq, m, bt, ctx, scores, Hq,
+                        Hkv, ps, maxP, nphys, nchunk, status);
     }
   }
   dim3 grid((maxP + kScoreWarps * kScorePagesPerWarp - 1) / (kScoreWarps * kScorePagesPerWarp),
             Hkv * nchunk, B);
   const T *qq = static_cast<const T *>(q);
   const T *m = static_cast<const T *>(mm);
-  switch (gs) {
-    case 8: page_score_kernel<T, 8><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
-    case 4: page_score_kernel<T, 4><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
-    case 2: page_score_kernel<T, 2><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
-    default: page_score_kernel<T, 1><<<grid, 32 * kScoreWarps, 0, st>>>(qq, m, bt, ctx, scores, Hq, Hkv, ps, maxP, nphys, nchunk, status); break;
-  }
-  return cudaGetLastError();
+  auto kern = gs == 8   ? page_score_kernel<T, 8>
+              : gs == 4 ? page_score_kernel<T, 4>
+              : gs == 2 ? page_score_kernel<T, 2>
+                        : page_score_kernel<T, 1>;
+  return launch_pdl(kern, grid, dim3(32 * kScoreWarps), 0, st, qq, m, bt, ctx, scores, Hq, Hkv,
+                    ps, maxP, nphys, nchunk, status);
 }
 
 }  // namespace
@@ -360,20 +362,18 @@ cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, con
   const unsigned blocks = (unsigned)((items + 7) / 8);
   switch (dtype) {
     case KV_F32:
-      minmax_build_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float *>(k), bt, ctx,
-          static_cast<float *>(minmax), B, Hkv, ps, maxP, nphys, status);
-      break;
+      return launch_pdl(minmax_build_kernel<float>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const float *>(k), bt, ctx, static_cast<float *>(minmax), B,
+                        Hkv, ps, maxP, nphys, status);
     case KV_F16:
-      minmax_build_kernel<__half><<<blocks, 256, 0, st>>>(static_cast<const __half *>(k), bt, ctx,
-          static_cast<__half *>(minmax), B, Hkv, ps, maxP, nphys, status);
-      break;
+      return launch_pdl(minmax_build_kernel<__half>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const __half *>(k), bt, ctx, static_cast<__half *>(minmax), B,
+                        Hkv, ps, maxP, nphys, status);
     default:
-      minmax_build_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(k), bt, ctx, static_cast<__nv_bfloat16 *>(minmax), B,
-          Hkv, ps, maxP, nphys, status);
-      break;
+      return launch_pdl(minmax_build_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const __nv_bfloat16 *>(k), bt, ctx,
+                        static_cast<__nv_bfloat16 *>(minmax), B, Hkv, ps, maxP, nphys, status);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,

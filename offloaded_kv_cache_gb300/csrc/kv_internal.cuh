@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvsparse.h"
 
 namespace kvs {
@@ -75,6 +77,49 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch.  Every kernel of the path waits for its
+// predecessor in the stream to finish (and its writes to be visible) before
+// it reads any global input (pdl_wait, its first statement), and lets the
+// next kernel be scheduled once its own main loop is done (pdl_trigger), so
+// the next kernel's launch and prologue overlap this kernel's tail.  No data
+// dependence changes: a kernel that never reaches pdl_trigger releases its
+// dependent when it exits.
+//   KVS_PDL 0: plain stream order; 1: trigger at entry; 2: trigger late.
+// ---------------------------------------------------------------------------
+#ifndef KVS_PDL
+#define KVS_PDL 2
+#endif
+__device__ __forceinline__ void pdl_wait() {
+#if KVS_PDL == 1
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+#if KVS_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#if KVS_PDL == 2
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = KVS_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

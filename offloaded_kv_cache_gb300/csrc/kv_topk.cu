@@ -50,6 +50,7 @@ __device__ __forceinline__ unsigned long long warp_bases64(unsigned long long v,
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx, int Hq, int ps,
                 int maxP, int K, int keys_in_smem, int32_t *__restrict__ out, int *status) {
+  pdl_wait();
   extern __shared__ uint32_t skeys[];
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long wsum[kTopkWarps];
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       break;
     }
   }
+  pdl_trigger();
   // selected: keys whose masked value beats the prefix, plus those equal to
   // it -- all of them when all_taken, else the first krem in page order
   const int seg = ((P + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;  // pages per warp
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kUnionThreads)
     union_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ ctx, int Hq, int G,
                  int gc, int ps, int maxP, int K, int umax, int32_t *__restrict__ upages,
                  uint32_t *__restrict__ umasks, int32_t *__restrict__ ucount, int *status) {
+  pdl_wait();
   extern __shared__ uint32_t words[];  // one byte of head bits per page, 4 pages a word
   __shared__ unsigned long long wsum[kUnionWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(kUnionThreads)
     atomicOr(&words[p >> 2], (1u << g) << ((p & 3) * 8));
   }
   __syncthreads();
+  pdl_trigger();
   // one contiguous segment of pages per warp, walked 32 pages at a time
   const int seg = ((P + kUnionWarps - 1) / kUnionWarps + 31) / 32 * 32;
   const int lo = warp * seg, hi = min(P, lo + seg);
@@ -241,6 +245,7 @@ constexpr int kMaxCombineSplits = 1024;
 __global__ void __launch_bounds__(kHeadDim)
     combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                    float *__restrict__ out, int S, long long rows) {
+  pdl_wait();
   __shared__ float w[kMaxCombineSplits];
   __shared__ float red[kHeadDim / 32];
   __shared__ float s_M, s_l;
@@ -281,6 +286,7 @@ __global__ void __launch_bounds__(kHeadDim)
     s_l = l;
   }
   __syncthreads();
+  pdl_trigger();
   float o = 0.f;
   const float *po = part_o + r * kHeadDim + c;
   const long long stride = rows * kHeadDim;
@@ -298,9 +304,8 @@ cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, 
   constexpr size_t kMaxSmemKeys = 11264;
   const int in_smem = (size_t)maxP <= kMaxSmemKeys ? 1 : 0;
   const size_t smem = in_smem ? (size_t)maxP * 4 : 0;
-  topk_kernel<<<(unsigned)((long long)B * Hq), kTopkThreads, smem, st>>>(scores, ctx, Hq, ps, maxP,
-                                                                       k, in_smem, indices, status);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3((unsigned)((long long)B * Hq)), dim3(kTopkThreads), smem, st,
+                    scores, ctx, Hq, ps, maxP, k, in_smem, indices, status);
 }
 
 cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,
@@ -318,16 +323,15 @@ cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int 
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
   dim3 grid(Hkv * (G / gc), B);
-  union_kernel<<<grid, kUnionThreads, smem, st>>>(indices, ctx, Hq, G, gc, ps, maxP, k, umax,
-                                                  upages, umasks, ucount, status);
-  return cudaGetLastError();
+  return launch_pdl(union_kernel, grid, dim3(kUnionThreads), smem, st, indices, ctx, Hq, G, gc, ps,
+                    maxP, k, umax, upages, umasks, ucount, status);
 }
 
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st) {
   const long long rows = (long long)B * Hq;
-  combine_kernel<<<(unsigned)rows, kHeadDim, 0, st>>>(part_o, part_ml, out, S, rows);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)rows), dim3(kHeadDim), 0, st, part_o, part_ml,
+                    out, S, rows);
 }
 
 }  // namespace kvs
