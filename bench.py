@@ -39,7 +39,10 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "opt6.7b-b32-ctx544": {"bytes": 289.141248e6, "src": "b0cbb0e7e54c7984"},
+    "llama3.1-8b-b4-ctx32k": {"bytes": 192.472064e6, "src": "b0cbb0e7e54c7984"},
+}
 
 
 def kernel_source_hash() -> str:
