@@ -326,7 +326,7 @@ def main():
     from offloaded_kv_cache_gb300 import build as kbuild
     from offloaded_kv_cache_gb300 import kvsparse as kv
     from offloaded_kv_cache_gb300 import workloads as W
-    from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+    from offloaded_kv_cache_gb300.pipeline import DecodeLayer, storage_to_torch
 
     ws, rank, local = dist_setup()
     if ws > 1:
@@ -496,6 +496,27 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e_ms = float(t.item())
     e2e_value = ws * step_bytes / (e_ms * 1e-3) / 1e9
+    assert kv.kv_device_status() == kv.KV_OK
+
+    # decode append (one token per row, min/max updated in place).  The
+    # workloads are full, so the append targets each row's last slot
+    # (lengths - 1) and rewrites it on every call.
+    kn, vn = W.new_tokens(spec, 0)
+    kn_d = storage_to_torch(kn, spec.dtype).cuda()
+    vn_d = storage_to_torch(vn, spec.dtype).cuda()
+    ctx_last = (layer.context_lens - 1).contiguous()
+
+    def append_call():
+        kv.kv_append_token(layer.shape, kn_d, vn_d, layer.k_cache, layer.v_cache,
+                           layer.block_table, ctx_last, None, layer.minmax,
+                           torch.cuda.current_stream())
+
+    n_app = max(3, args.steps // 4)
+    a_total, _ = timed([("append", append_call)], n_app, 3)
+    a_ms = a_total / n_app
+    a_bytes = 8 * spec.batch * spec.num_kv_heads * spec.head_dim * spec.elem_bytes
+    extra["append"] = {"ms": round(a_ms, 5), "GB_s": round(a_bytes / (a_ms * 1e-3) / 1e9, 2),
+                       "bytes": a_bytes}
     assert kv.kv_device_status() == kv.KV_OK
 
     peak, peak_kind = measured_peaks()

@@ -7,6 +7,8 @@
  * cache offloading", steps (1)-(3); section 2.2 "Sparse attention" for the
  * Quest index):
  *   kv_page_minmax_build  -> per-page channel-wise key min/max (the index)
+ *   kv_append_token       -> one new decode token per sequence into the cache,
+ *                            with its page's min/max updated in place
  *   kv_page_score         -> q against the index: an upper bound on q.k
  *   kv_topk_select        -> the K highest-scoring pages per query head
  *   kv_sparse_decode_attn -> softmax attention over only those pages
@@ -100,6 +102,30 @@ typedef struct {
  * rows must be full in each. */
 int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
                          const int32_t *context_lens, void *minmax, void *stream);
+
+/* Decode append (KVDrive, section 2.1: each decode step appends the new key
+ * and value vectors to the cache; DirectKV, core method 4: with the cache in
+ * pinned host memory, decode appends the new token there).
+ *   k_new, v_new [B][Hkv][d] dtype, device memory: the new token's K and V.
+ * The token of sequence b is stored at position len_b = context_lens[b], the
+ * length BEFORE the append (0 <= len_b < maxP * ps): physical page
+ * block_table[b][len_b / ps], slot len_b % ps, every kv head; the bits are
+ * copied unchanged.  k_cache / v_cache are written where kv_loc says (for
+ * KV_LOC_HOST_PINNED, through the mapped host pointer).
+ * minmax (may be NULL: no index update): the entry of that physical page
+ * becomes the channel-wise min/max of its len_b % ps + 1 valid tokens, i.e.
+ * min(old, k) / max(old, k) in IEEE totalOrder, or k itself when the token
+ * opens the page -- bit-identical to kv_page_minmax_build on the new length.
+ * Precondition: the entry holds the page's first len_b % ps tokens (from the
+ * build or earlier appends), and the page is not shared with another row.
+ * Calling again at the same position without advancing rewrites K/V, but the
+ * min/max keeps the overwritten key too (a looser, still valid bound).
+ * context_lens_out (may be NULL, may equal context_lens): receives len_b + 1.
+ * A row whose len_b or block-table entry is out of range is skipped, keeps
+ * its length and sets KV_ERR_BOUNDS in the device status word. */
+int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new, void *k_cache,
+                    void *v_cache, const int32_t *block_table, const int32_t *context_lens,
+                    int32_t *context_lens_out, void *minmax, void *stream);
 
 /* Page criticality (KVDrive, section 2.2): scores[b][h][p] =
  * sum_c max(q_c * min_c, q_c * max_c) over the minmax entry of page

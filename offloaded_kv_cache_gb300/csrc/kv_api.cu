@@ -455,6 +455,29 @@ int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
+int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new, void *k_cache,
+                    void *v_cache, const int32_t *block_table, const int32_t *context_lens,
+                    int32_t *context_lens_out, void *minmax, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!al16(k_new) || !al16(v_new) || !al4(block_table) || !al4(context_lens) ||
+      (minmax && !al16(minmax)) || (context_lens_out && !al4(context_lens_out)))
+    return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  const void *kd = nullptr, *vd = nullptr;
+  if ((rc = resolve_kv(shape, k_cache, &kd)) != KV_OK) return rc;
+  if ((rc = resolve_kv(shape, v_cache, &vd)) != KV_OK) return rc;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_append(shape->dtype, k_new, v_new, const_cast<void *>(kd),
+                                const_cast<void *>(vd), block_table, context_lens,
+                                context_lens_out, minmax, shape->batch, shape->num_kv_heads,
+                                shape->page_size, shape->max_pages_per_seq,
+                                shape->num_phys_pages, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
                   const int32_t *block_table, const int32_t *context_lens, float *scores,
                   void *stream) {

@@ -254,6 +254,10 @@ constexpr int kMaxStages = 16;
 cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
                                 void *minmax, int B, int Hkv, int ps, int maxP, long long nphys,
                                 int *status, cudaStream_t st);
+cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void *k_cache,
+                          void *v_cache, const int32_t *bt, const int32_t *ctx,
+                          int32_t *ctx_out, void *minmax, int B, int Hkv, int ps, int maxP,
+                          long long nphys, int *status, cudaStream_t st);
 cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,
                               const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
                               int maxP, long long nphys, int *status, cudaStream_t st);

@@ -61,6 +61,7 @@ def load(path: str = LIB_PATH):
     i32, sz, f32 = ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     sig = {
         "kv_page_minmax_build": (ctypes.c_int, [S, P, P, P, P, P]),
+        "kv_append_token": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P]),
         "kv_page_score": (ctypes.c_int, [S, P, P, P, P, P, P]),
         "kv_topk_workspace_bytes": (sz, [S, i32]),
         "kv_topk_select": (ctypes.c_int, [S, P, P, i32, P, P, sz, P]),
@@ -120,6 +121,14 @@ def kv_page_minmax_build(shape, k_cache, block_table, context_lens, minmax, stre
     rc = load().kv_page_minmax_build(ctypes.byref(shape), _ptr(k_cache), _ptr(block_table),
                                      _ptr(context_lens), _ptr(minmax), _stream(stream))
     return _ret(rc, "kv_page_minmax_build", check)
+
+
+def kv_append_token(shape, k_new, v_new, k_cache, v_cache, block_table, context_lens,
+                    context_lens_out=None, minmax=None, stream=None, check=True):
+    rc = load().kv_append_token(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(block_table), _ptr(context_lens),
+                                _ptr(context_lens_out), _ptr(minmax), _stream(stream))
+    return _ret(rc, "kv_append_token", check)
 
 
 def kv_page_score(shape, q, minmax, block_table, context_lens, scores, stream=None, check=True):

@@ -5,6 +5,7 @@ outputs and workspaces the C ABI needs, and runs the path through the ctypes
 binding:
 
     build_index()  -> kv_page_minmax_build
+    append()       -> kv_append_token
     sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
     dense_step()   -> kv_dense_decode_attn
 
@@ -101,6 +102,18 @@ class DecodeLayer:
         stream = self._st(stream)
         kv.kv_page_minmax_build(self.shape, self.k_cache, self.block_table, self.context_lens,
                                 self.minmax, stream)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, advance: bool = True,
+               update_index: bool = True, stream=None):
+        """Append one token per sequence (k_new, v_new: [B][Hkv][d] on the device).
+
+        advance: context_lens grows by one in place; else the lengths stay and a
+        repeated call rewrites the same slot.
+        """
+        stream = self._st(stream)
+        kv.kv_append_token(self.shape, k_new, v_new, self.k_cache, self.v_cache, self.block_table,
+                           self.context_lens, self.context_lens if advance else None,
+                           self.minmax if update_index else None, stream)
 
     def score(self, stream=None):
         stream = self._st(stream)

@@ -272,6 +272,20 @@ def generate(spec: WorkloadSpec, context_lens=None, threads: int | None = None) 
                     context_lens=ctx)
 
 
+def new_tokens(spec: WorkloadSpec, step: int = 0):
+    """Seeded K and V rows of one appended decode token per sequence.
+
+    Returns (k_new, v_new), each [B][Hkv][d] in the storage type, drawn like the
+    cache (N(0, value_scale^2), rounded once); ``step`` selects the draw.
+    """
+    B, Hkv, d = spec.batch, spec.num_kv_heads, spec.head_dim
+    root = np.random.SeedSequence([spec.seed, 0x0A99E7D, step])
+    s_k, s_v = root.spawn(2)
+    k = _normal_storage(s_k, B * Hkv * d, spec.value_scale, spec.dtype, 1).reshape(B, Hkv, d)
+    v = _normal_storage(s_v, B * Hkv * d, spec.value_scale, spec.dtype, 1).reshape(B, Hkv, d)
+    return k, v
+
+
 def tiny_spec(dtype="bf16", batch=2, hq=4, hkv=2, d=128, context=100, ps=16, topk=3,
               scale=1.0, plant="none", index=100, **kw) -> WorkloadSpec:
     """A small workload for parity tests (several pages, ragged last page)."""

@@ -55,6 +55,9 @@ def _load():
             lib.okv_minmax_build.restype = None
             lib.okv_minmax_build.argtypes = [ctypes.c_int] + [ctypes.c_int] * 5 + [
                 _vp, _i32p, _i32p, _f64p, _f64p]
+            lib.okv_append.restype = None
+            lib.okv_append.argtypes = [ctypes.c_int] * 6 + [_vp, _vp, _vp, _vp, _i32p, _i32p,
+                                                            _f64p, _f64p]
             lib.okv_page_score.restype = ctypes.c_double
             lib.okv_page_score.argtypes = [ctypes.c_int, _f64p, _f64p, _f64p]
             lib.okv_scores.restype = None
@@ -131,6 +134,37 @@ def minmax_build(dtype: str, k_cache: np.ndarray, block_table: np.ndarray,
     lib.okv_minmax_build(DTYPE_CODE[dtype], B, hkv, d, ps, maxP, k.ctypes.data, _ptr(bt, _i32p),
                          _ptr(ctx, _i32p), _ptr(mn, _f64p), _ptr(mx, _f64p))
     return mn, mx
+
+
+def append_token(dtype: str, k_new: np.ndarray, v_new: np.ndarray, k_cache: np.ndarray,
+                 v_cache: np.ndarray, block_table: np.ndarray, context_lens: np.ndarray,
+                 mn: np.ndarray | None = None, mx: np.ndarray | None = None):
+    """Append one token per sequence at position context_lens[b].
+
+    Returns new copies (k_cache, v_cache, mn, mx); mn/mx are the fp64 tables of
+    minmax_build with the appended pages' entries recomputed (None when not
+    given).  k_new / v_new are [B][Hkv][d] in the cache's storage type.
+    """
+    lib = _load()
+    k = np.array(k_cache, copy=True, order="C")
+    v = np.array(v_cache, copy=True, order="C")
+    kn = _c(k_new)
+    vn = _c(v_new)
+    assert kn.dtype == k.dtype and vn.dtype == v.dtype
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    nphys, hkv, ps, d = k.shape
+    B, maxP = bt.shape
+    assert kn.shape == (B, hkv, d) and vn.shape == (B, hkv, d)
+    if mn is not None:
+        mn = np.array(mn, dtype=np.float64, copy=True, order="C")
+        mx = np.array(mx, dtype=np.float64, copy=True, order="C")
+        mn_p, mx_p = _ptr(mn, _f64p), _ptr(mx, _f64p)
+    else:
+        mn_p = mx_p = None
+    lib.okv_append(DTYPE_CODE[dtype], B, hkv, d, ps, maxP, kn.ctypes.data, vn.ctypes.data,
+                   k.ctypes.data, v.ctypes.data, _ptr(bt, _i32p), _ptr(ctx, _i32p), mn_p, mx_p)
+    return k, v, mn, mx
 
 
 def page_score(q: np.ndarray, mn: np.ndarray, mx: np.ndarray) -> float:

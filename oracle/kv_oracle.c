@@ -128,6 +128,43 @@ void okv_minmax_build(int dtype, int B, int Hkv, int d, int ps, int max_pages,
 }
 
 /* ------------------------------------------------------------------------- */
+/* decode append: one new token per sequence                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Each decode step appends the new key and value vectors to the cache
+ * (KVDrive, section 2.1), and with the cache in pinned host memory the
+ * manager appends the new token there (DirectKV, core method 4).  Token
+ * position of sequence b is len_b = context_lens[b], its length before the
+ * append: logical page p = len_b / ps, slot t = len_b % ps, physical page
+ * block_table[b][p].  k_new / v_new are [B][Hkv][d] stored elements, copied
+ * bit for bit to [phys][kvh][t][:].  The page's index entry is then the
+ * channel-wise min/max of its t + 1 valid tokens, by the definition above
+ * (mn/mx are [num_phys][Hkv][d]; NULL skips the index).  Rows with
+ * len_b < 0 or len_b >= max_pages * ps are left alone. */
+void okv_append(int dtype, int B, int Hkv, int d, int ps, int max_pages, const void *k_new,
+                const void *v_new, void *k_cache, void *v_cache, const int32_t *block_table,
+                const int32_t *context_lens, double *mn, double *mx) {
+  size_t es = dtype == OKV_F32 ? 4 : 2;
+  for (int b = 0; b < B; ++b) {
+    int len = context_lens[b];
+    if (len < 0 || len >= max_pages * ps) continue;
+    int p = len / ps, t = len % ps;
+    int64_t phys = block_table[(int64_t)b * max_pages + p];
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      int64_t src = ((int64_t)b * Hkv + kvh) * d;
+      int64_t page = (phys * Hkv + kvh) * ps * (int64_t)d;
+      int64_t dst = page + (int64_t)t * d;
+      memcpy((char *)k_cache + dst * es, (const char *)k_new + src * es, d * es);
+      memcpy((char *)v_cache + dst * es, (const char *)v_new + src * es, d * es);
+      if (mn && mx) {
+        int64_t o = (phys * Hkv + kvh) * (int64_t)d;
+        okv_page_minmax(dtype, d, t + 1, k_cache, page, mn + o, mx + o);
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* page score: upper bound of q . k over the page                              */
 /* ------------------------------------------------------------------------- */
 

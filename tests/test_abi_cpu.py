@@ -65,6 +65,8 @@ def test_bad_shapes_rejected_by_every_entry_point(kvlib, kw, code):
     s = _shape(**kw)
     assert kv.kv_page_minmax_build(s, FAKE, FAKE, FAKE, FAKE, check=False) == code
     assert kv.kv_page_score(s, FAKE, FAKE, FAKE, FAKE, FAKE, check=False) == code
+    assert kv.kv_append_token(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              check=False) == code
     assert kv.kv_topk_select(s, FAKE, FAKE, 4, FAKE, check=False) == code
     assert kv.kv_dense_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, 1 << 20,
                                    check=False) == code
@@ -79,6 +81,14 @@ def test_null_and_misaligned_pointers_rejected(kvlib):
     assert kv.kv_page_minmax_build(s, FAKE, FAKE, FAKE, FAKE + 8, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_page_score(s, FAKE + 4, FAKE, FAKE, FAKE, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_page_score(s, FAKE, FAKE, FAKE + 2, FAKE, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_append_token(s, None, FAKE, FAKE, FAKE, FAKE, FAKE, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_append_token(s, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_append_token(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_append_token(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 8,
+                              check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_topk_select(s, FAKE, FAKE, 0, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_topk_select(s, FAKE, FAKE, 4, None, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_dense_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, float("nan"), FAKE, FAKE, 64,

@@ -415,3 +415,96 @@ def test_planted_tokens_carry_the_largest_logits_in_the_fp32_workload():
     logits = keys.astype(np.float64) @ q
     top8 = np.sort(logits)[-8:]
     assert np.allclose(top8, 4 * np.linalg.norm(q), rtol=1e-6)
+
+
+# ---------------------------------------------------------------- decode append
+
+def _token(wl, b, t):
+    """K and V rows [Hkv][d] of token t of sequence b, read through the block table."""
+    ps = wl.spec.page_size
+    phys = wl.block_table[b, t // ps]
+    return wl.k_cache[phys, :, t % ps], wl.v_cache[phys, :, t % ps]
+
+
+@pytest.mark.parametrize("dtype,ps", [("bf16", 16), ("f16", 64), ("f32", 16)])
+def test_append_token_by_token_rebuilds_the_cache_and_its_index(dtype, ps):
+    # Appending every token of a workload one step at a time, into caches and
+    # min/max tables that start as garbage, must give back the workload's
+    # caches at every valid position and exactly the bulk index build.
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=4, hkv=2, context=3 * ps + 5, ps=ps, index=40)
+    lens = [3 * ps + 5, ps, 7]
+    wl = W.generate(spec, context_lens=lens)
+    rng = _rng(41)
+    k = W.to_storage(rng.standard_normal(wl.k_cache.shape).astype(np.float32) * 50, dtype)
+    v = W.to_storage(rng.standard_normal(wl.v_cache.shape).astype(np.float32) * 50, dtype)
+    mn = rng.standard_normal((spec.num_phys_pages, 2, spec.head_dim)) * 50
+    mx = mn + 1.0
+    done = spec.max_pages * ps            # a length the append leaves alone
+    for t in range(max(lens)):
+        ctx = np.array([t if t < L else done for L in lens], dtype=np.int32)
+        kn = np.zeros((3, 2, spec.head_dim), dtype=k.dtype)
+        vn = np.zeros_like(kn)
+        for b in range(3):
+            if t < lens[b]:
+                kn[b], vn[b] = _token(wl, b, t)
+        k, v, mn, mx = oracle.append_token(dtype, kn, vn, k, v, wl.block_table, ctx, mn, mx)
+    ref_mn, ref_mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
+    for b, L in enumerate(lens):
+        for t in range(L):
+            kt, vt = _token(wl, b, t)
+            phys = wl.block_table[b, t // ps]
+            assert np.array_equal(k[phys, :, t % ps].view(np.uint8), kt.view(np.uint8))
+            assert np.array_equal(v[phys, :, t % ps].view(np.uint8), vt.view(np.uint8))
+        for p in range(-(-L // ps)):
+            phys = wl.block_table[b, p]
+            assert np.array_equal(mn[phys], ref_mn[phys]) and np.array_equal(mx[phys], ref_mx[phys])
+
+
+def test_append_updates_min_max_in_closed_form():
+    # For a page holding t >= 1 tokens, appending key x gives
+    # min' = min(min, x) and max' = max(max, x) channel by channel; into an
+    # empty slot 0 it gives min' = max' = x (the page is that one token).
+    spec = W.tiny_spec(dtype="f32", batch=2, hq=2, hkv=1, context=40, ps=16, index=42)
+    wl = W.generate(spec, context_lens=[21, 32])
+    mn, mx = oracle.minmax_build("f32", wl.k_cache, wl.block_table, wl.context_lens)
+    rng = _rng(43)
+    kn = (rng.standard_normal((2, 1, 128)) * 2 + 0.01).astype(np.float32)
+    vn = rng.standard_normal((2, 1, 128)).astype(np.float32)
+    _, _, mn2, mx2 = oracle.append_token("f32", kn, vn, wl.k_cache, wl.v_cache, wl.block_table,
+                                         wl.context_lens, mn, mx)
+    p0 = wl.block_table[0, 1]                         # sequence 0: slot 5 of page 1
+    assert np.array_equal(mn2[p0, 0], np.minimum(mn[p0, 0], kn[0, 0]))
+    assert np.array_equal(mx2[p0, 0], np.maximum(mx[p0, 0], kn[0, 0]))
+    p1 = wl.block_table[1, 2]                         # sequence 1: slot 0 of page 2
+    assert np.array_equal(mn2[p1, 0], kn[1, 0].astype(np.float64))
+    assert np.array_equal(mx2[p1, 0], kn[1, 0].astype(np.float64))
+    # entries of other pages are untouched
+    others = [i for i in range(spec.num_phys_pages) if i not in (p0, p1)]
+    assert np.array_equal(mn2[others], mn[others], equal_nan=True)
+
+
+def test_append_writes_one_row_per_sequence_and_skips_out_of_range_lengths():
+    spec = W.tiny_spec(dtype="bf16", batch=3, hq=2, hkv=2, context=48, ps=16, index=44)
+    wl = W.generate(spec, context_lens=[48, 10, 1])
+    kn, vn = W.new_tokens(spec, 0)
+    ctx = np.array([48, 10, -1], dtype=np.int32)       # full row, a middle slot, invalid
+    k2, v2, _, _ = oracle.append_token("bf16", kn, vn, wl.k_cache, wl.v_cache, wl.block_table, ctx)
+    changed_k = np.argwhere((k2 != wl.k_cache).any(axis=-1))
+    changed_v = np.argwhere((v2 != wl.v_cache).any(axis=-1))
+    phys = wl.block_table[1, 0]
+    expect = {(int(phys), h, 10) for h in range(2)}
+    assert {tuple(map(int, r)) for r in changed_k} <= expect
+    assert {tuple(map(int, r)) for r in changed_v} <= expect
+    assert np.array_equal(k2[phys, :, 10], kn[1]) and np.array_equal(v2[phys, :, 10], vn[1])
+
+
+def test_attention_after_appending_to_an_empty_sequence_is_the_new_value():
+    spec = W.tiny_spec(dtype="f16", batch=1, hq=4, hkv=2, context=32, ps=16, index=45)
+    wl = W.generate(spec)
+    kn, vn = W.new_tokens(spec, 3)
+    k2, v2, _, _ = oracle.append_token("f16", kn, vn, wl.k_cache, wl.v_cache, wl.block_table,
+                                       np.array([0], dtype=np.int32))
+    out = oracle.attention("f16", wl.q, k2, v2, wl.block_table, np.array([1], dtype=np.int32),
+                           wl.scale)
+    for h in range(4):
+        assert np.array_equal(out[0, h], vn[0, h // 2].astype(np.float64))
