@@ -450,6 +450,12 @@ def main():
     extra = {}
     if sparse:
         extra["stages_ms"] = {n: round(v, 5) for n, v in per_stage.items()}
+        # selection with the sink (first 4 tokens) and local (last 64 tokens)
+        # pages forced in, the same budget
+        f_total, _ = timed([("topk_forced", lambda: layer.select(sink_tokens=4, local_tokens=64))],
+                           max(3, args.steps // 4), 3)
+        extra["stages_ms"]["topk_select_forced_4_64"] = round(f_total / max(3, args.steps // 4), 5)
+        layer.select()
         d_total, _ = timed([("dense_attn", layer.dense_step)], max(3, args.steps // 4), 3)
         d_ms = d_total / max(3, args.steps // 4)
         db = dense_bytes(spec, ctx)

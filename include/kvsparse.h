@@ -11,6 +11,7 @@
  *                            with its page's min/max updated in place
  *   kv_page_score         -> q against the index: an upper bound on q.k
  *   kv_topk_select        -> the K highest-scoring pages per query head
+ *                            (kv_topk_select_forced: sink and local pages first)
  *   kv_sparse_decode_attn -> softmax attention over only those pages
  *   kv_dense_decode_attn  -> the same over every page (Dual-Blade, "Background
  *                            and key observations": decode reads all prior KV)
@@ -147,6 +148,20 @@ size_t kv_topk_workspace_bytes(const kv_shape *shape, int32_t k);
 int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
                    int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
                    void *stream);
+
+/* Top-K selection with forced pages (KVDrive, section 9.1 "Experimental
+ * setup": sparse-attention systems always keep the sink tokens -- the first
+ * 4 -- and the 64 most recent local tokens).  As kv_topk_select, except that
+ * the pages holding tokens [0, sink_tokens) and [len_b - local_tokens, len_b)
+ * are selected first; the remaining slots go to the highest-scoring other
+ * pages.  Forced pages count within k: a caller that wants k dynamic pages on
+ * top passes k plus the number of forced pages.  If more pages are forced
+ * than k, the k lowest-index forced pages are kept.  sink_tokens = 0 and
+ * local_tokens = 0 give kv_topk_select exactly.  Both must be >= 0. */
+int kv_topk_select_forced(const kv_shape *shape, const float *scores,
+                          const int32_t *context_lens, int32_t k, int32_t sink_tokens,
+                          int32_t local_tokens, int32_t *indices, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /* Bytes of workspace the attention calls need for this shape on the current
  * device; k = 0 for kv_dense_decode_attn, the selection size for

@@ -503,22 +503,32 @@ size_t kv_topk_workspace_bytes(const kv_shape *shape, int32_t k) {
   return 0;
 }
 
-int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
-                   int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
-                   void *stream) {
+int kv_topk_select_forced(const kv_shape *shape, const float *scores,
+                          const int32_t *context_lens, int32_t k, int32_t sink_tokens,
+                          int32_t local_tokens, int32_t *indices, void *workspace,
+                          size_t workspace_bytes, void *stream) {
   (void)workspace;
   (void)workspace_bytes;
   int rc = check_shape(shape);
   if (rc) return rc;
-  if (k < 1 || !al16(scores) || !al4(indices) || !al4(context_lens)) return KV_ERR_INVALID_ARG;
+  if (k < 1 || sink_tokens < 0 || local_tokens < 0 || !al16(scores) || !al4(indices) ||
+      !al4(context_lens))
+    return KV_ERR_INVALID_ARG;
   const int dev = current_device();
   if (dev < 0) return KV_ERR_CUDA;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
   cudaError_t e = launch_topk(scores, context_lens, shape->batch, shape->num_q_heads,
-                              shape->page_size, shape->max_pages_per_seq, k, indices, status,
-                              static_cast<cudaStream_t>(stream));
+                              shape->page_size, shape->max_pages_per_seq, k, sink_tokens,
+                              local_tokens, indices, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
+                   int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+  return kv_topk_select_forced(shape, scores, context_lens, k, 0, 0, indices, workspace,
+                               workspace_bytes, stream);
 }
 
 size_t kv_attn_workspace_bytes(const kv_shape *shape, int32_t k) {

@@ -262,7 +262,8 @@ cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, cons
                               const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
                               int maxP, long long nphys, int *status, cudaStream_t st);
 cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
-                        int k, int32_t *indices, int *status, cudaStream_t st);
+                        int k, int sink_tokens, int local_tokens, int32_t *indices, int *status,
+                        cudaStream_t st);
 cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,
                          int gc, int ps, int maxP, int k, int umax, int32_t *upages,
                          uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st);

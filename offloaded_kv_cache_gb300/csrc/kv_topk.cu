@@ -18,6 +18,10 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return key32(__float_as_uint(s + 0.0f));
 }
 
+// Key of a forced page: above every score's key (+inf maps to 0xFF800000;
+// 0xFFFFFFFF is a NaN's key, and scores are never NaN).
+constexpr uint32_t kForcedKey = 0xFFFFFFFFu;
+
 // Exclusive prefix sum over the warps of the block of one 64-bit value per
 // warp (lane 0's argument counts); returns the warp's base, *total the sum.
 // Two block barriers; `wsum` holds one slot per warp.
@@ -47,9 +51,13 @@ __device__ __forceinline__ unsigned long long warp_bases64(unsigned long long v,
 // per warp; each warp walks its segment 32 pages at a time and places the
 // selected pages in index order with ballots, after one block scan of the
 // per-warp counts.  Equal keys at the threshold go to the lower page index.
+// Forced pages (the pages holding the first sink_tokens tokens and the last
+// local_tokens tokens of the row) take a key above every score's, so they are
+// selected first, lower index first among themselves.
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx, int Hq, int ps,
-                int maxP, int K, int keys_in_smem, int32_t *__restrict__ out, int *status) {
+                int maxP, int K, int keys_in_smem, int sink_tokens, int local_tokens,
+                int32_t *__restrict__ out, int *status) {
   pdl_wait();
   extern __shared__ uint32_t skeys[];
   __shared__ uint32_t hist[256];
@@ -73,12 +81,16 @@ __global__ void __launch_bounds__(kTopkThreads)
     for (int i = tid; i < K; i += kTopkThreads) orow[i] = i < P ? i : -1;
     return;
   }
-  if (keys_in_smem) {
-    for (int p = tid; p < P; p += kTopkThreads) skeys[p] = score_key(srow[p]);
-  }
-  auto key_at = [&](int p) -> uint32_t {
-    return keys_in_smem ? skeys[p] : score_key(srow[p]);
+  // forced pages: [0, f_sink) and [f_local, P)
+  const int f_sink = sink_tokens > 0 ? min(P, (sink_tokens + ps - 1) / ps) : 0;
+  const int f_local = local_tokens > 0 ? max(0, len - local_tokens) / ps : P;
+  auto raw_key = [&](int p) -> uint32_t {
+    return (p < f_sink || p >= f_local) ? kForcedKey : score_key(srow[p]);
   };
+  if (keys_in_smem) {
+    for (int p = tid; p < P; p += kTopkThreads) skeys[p] = raw_key(p);
+  }
+  auto key_at = [&](int p) -> uint32_t { return keys_in_smem ? skeys[p] : raw_key(p); };
 
   uint32_t prefix = 0, pmask = 0;
   int krem = keff;  // keys matching `prefix` that still have to be taken
@@ -299,13 +311,15 @@ __global__ void __launch_bounds__(kHeadDim)
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
-                        int k, int32_t *indices, int *status, cudaStream_t st) {
+                        int k, int sink_tokens, int local_tokens, int32_t *indices, int *status,
+                        cudaStream_t st) {
   // keys cached in shared memory, within the default 48 KB per block
   constexpr size_t kMaxSmemKeys = 11264;
   const int in_smem = (size_t)maxP <= kMaxSmemKeys ? 1 : 0;
   const size_t smem = in_smem ? (size_t)maxP * 4 : 0;
   return launch_pdl(topk_kernel, dim3((unsigned)((long long)B * Hq)), dim3(kTopkThreads), smem, st,
-                    scores, ctx, Hq, ps, maxP, k, in_smem, indices, status);
+                    scores, ctx, Hq, ps, maxP, k, in_smem, sink_tokens, local_tokens, indices,
+                    status);
 }
 
 cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,

@@ -65,6 +65,7 @@ def load(path: str = LIB_PATH):
         "kv_page_score": (ctypes.c_int, [S, P, P, P, P, P, P]),
         "kv_topk_workspace_bytes": (sz, [S, i32]),
         "kv_topk_select": (ctypes.c_int, [S, P, P, i32, P, P, sz, P]),
+        "kv_topk_select_forced": (ctypes.c_int, [S, P, P, i32, i32, i32, P, P, sz, P]),
         "kv_attn_workspace_bytes": (sz, [S, i32]),
         "kv_attn_num_splits": (i32, [S, i32]),
         "kv_sparse_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, P, i32, f32, P, P, sz, P]),
@@ -147,6 +148,14 @@ def kv_topk_select(shape, scores, context_lens, k, indices, workspace=None, work
                                _ptr(indices), _ptr(workspace), int(workspace_bytes),
                                _stream(stream))
     return _ret(rc, "kv_topk_select", check)
+
+
+def kv_topk_select_forced(shape, scores, context_lens, k, sink_tokens, local_tokens, indices,
+                          workspace=None, workspace_bytes=0, stream=None, check=True):
+    rc = load().kv_topk_select_forced(ctypes.byref(shape), _ptr(scores), _ptr(context_lens),
+                                      int(k), int(sink_tokens), int(local_tokens), _ptr(indices),
+                                      _ptr(workspace), int(workspace_bytes), _stream(stream))
+    return _ret(rc, "kv_topk_select_forced", check)
 
 
 def kv_attn_workspace_bytes(shape, k) -> int:

@@ -120,10 +120,17 @@ class DecodeLayer:
         kv.kv_page_score(self.shape, self.q, self.minmax, self.block_table, self.context_lens,
                          self.scores, stream)
 
-    def select(self, stream=None):
+    def select(self, stream=None, sink_tokens: int = 0, local_tokens: int = 0):
+        """Top-K pages per query head; sink_tokens / local_tokens force the pages
+        holding the first and the most recent tokens into the selection."""
         stream = self._st(stream)
-        kv.kv_topk_select(self.shape, self.scores, self.context_lens, self.topk, self.indices,
-                          self.workspace, self.workspace.numel(), stream)
+        if sink_tokens or local_tokens:
+            kv.kv_topk_select_forced(self.shape, self.scores, self.context_lens, self.topk,
+                                     sink_tokens, local_tokens, self.indices, self.workspace,
+                                     self.workspace.numel(), stream)
+        else:
+            kv.kv_topk_select(self.shape, self.scores, self.context_lens, self.topk,
+                              self.indices, self.workspace, self.workspace.numel(), stream)
 
     def sparse_attn(self, indices=None, stream=None):
         stream = self._st(stream)

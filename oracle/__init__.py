@@ -67,6 +67,9 @@ def _load():
             lib.okv_topk_row.argtypes = [ctypes.c_int, _f64p, ctypes.c_int, _i32p]
             lib.okv_topk.restype = None
             lib.okv_topk.argtypes = [ctypes.c_int] * 4 + [_i32p, _f64p, ctypes.c_int, _i32p]
+            lib.okv_topk_forced.restype = None
+            lib.okv_topk_forced.argtypes = [ctypes.c_int] * 4 + [
+                _i32p, _f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p]
             lib.okv_attention_row.restype = None
             lib.okv_attention_row.argtypes = [ctypes.c_int] * 5 + [
                 ctypes.c_double, _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int, _i32p,
@@ -210,6 +213,19 @@ def topk(scores_arr: np.ndarray, context_lens: np.ndarray, page_size: int, k: in
     B, Hq, maxP = s.shape
     out = np.empty((B, Hq, k), dtype=np.int32)
     lib.okv_topk(B, Hq, page_size, maxP, _ptr(ctx, _i32p), _ptr(s, _f64p), k, _ptr(out, _i32p))
+    return out
+
+
+def topk_forced(scores_arr: np.ndarray, context_lens: np.ndarray, page_size: int, k: int,
+                sink_tokens: int, local_tokens: int) -> np.ndarray:
+    """[B][Hq][k] ascending selection with the sink and local pages forced in."""
+    lib = _load()
+    s = _c(scores_arr, np.float64)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, maxP = s.shape
+    out = np.empty((B, Hq, k), dtype=np.int32)
+    lib.okv_topk_forced(B, Hq, page_size, maxP, _ptr(ctx, _i32p), _ptr(s, _f64p), k,
+                        int(sink_tokens), int(local_tokens), _ptr(out, _i32p))
     return out
 
 

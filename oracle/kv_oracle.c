@@ -252,6 +252,49 @@ void okv_topk(int B, int Hq, int ps, int max_pages, const int32_t *context_lens,
   }
 }
 
+/* Selection with forced pages.  Sparse-attention systems always keep the
+ * sink tokens (the first few) and the most recent local tokens (KVDrive,
+ * section 9.1, experimental setup: the first 4 and the last 64).  At page
+ * granularity a page is forced when the tokens it holds, [p*ps, min(len,
+ * (p+1)*ps)), meet [0, sink) or [len - local, len).  Forced pages come first,
+ * in index order; then the other pages by score (higher first, ties to the
+ * lower index); the first min(K, P) are returned ascending, -1 padded. */
+static int page_is_forced(int p, int len, int ps, int sink, int local) {
+  int lo = p * ps;
+  int hi = (p + 1) * ps < len ? (p + 1) * ps : len; /* tokens [lo, hi) */
+  if (sink > 0 && lo < sink) return 1;
+  if (local > 0 && hi > len - local) return 1;
+  return 0;
+}
+
+void okv_topk_forced_row(int P, int len, int ps, const double *scores, int K, int sink,
+                         int local, int32_t *out) {
+  int *order = (int *)malloc(sizeof(int) * (P > 0 ? P : 1));
+  int nf = 0;
+  for (int p = 0; p < P; ++p)
+    if (page_is_forced(p, len, ps, sink, local)) order[nf++] = p;
+  int n = nf;
+  for (int p = 0; p < P; ++p)
+    if (!page_is_forced(p, len, ps, sink, local)) order[n++] = p;
+  g_sort_scores = scores;
+  qsort(order + nf, P - nf, sizeof(int), by_score_desc);
+  int keff = K < P ? K : P;
+  qsort(order, keff, sizeof(int), by_index_asc);
+  for (int i = 0; i < K; ++i) out[i] = i < keff ? order[i] : -1;
+  free(order);
+}
+
+void okv_topk_forced(int B, int Hq, int ps, int max_pages, const int32_t *context_lens,
+                     const double *scores, int K, int sink, int local, int32_t *out) {
+  for (int b = 0; b < B; ++b) {
+    int len = context_lens[b];
+    int P = (len + ps - 1) / ps;
+    for (int h = 0; h < Hq; ++h)
+      okv_topk_forced_row(P, len, ps, scores + ((int64_t)b * Hq + h) * max_pages, K, sink, local,
+                          out + ((int64_t)b * Hq + h) * K);
+  }
+}
+
 /* ------------------------------------------------------------------------- */
 /* attention of one query head over a set of pages                             */
 /* ------------------------------------------------------------------------- */

@@ -68,6 +68,7 @@ def test_bad_shapes_rejected_by_every_entry_point(kvlib, kw, code):
     assert kv.kv_append_token(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                               check=False) == code
     assert kv.kv_topk_select(s, FAKE, FAKE, 4, FAKE, check=False) == code
+    assert kv.kv_topk_select_forced(s, FAKE, FAKE, 4, 4, 64, FAKE, check=False) == code
     assert kv.kv_dense_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, FAKE, FAKE, 1 << 20,
                                    check=False) == code
     assert kv.kv_sparse_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0.1, FAKE, FAKE,
@@ -91,6 +92,10 @@ def test_null_and_misaligned_pointers_rejected(kvlib):
                               check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_topk_select(s, FAKE, FAKE, 0, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_topk_select(s, FAKE, FAKE, 4, None, check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_topk_select_forced(s, FAKE, FAKE, 4, -1, 64, FAKE, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_topk_select_forced(s, FAKE, FAKE, 4, 4, -64, FAKE, check=False) == \
+        kv.KV_ERR_INVALID_ARG
     assert kv.kv_dense_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, float("nan"), FAKE, FAKE, 64,
                                    check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_dense_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, FAKE, 64,

@@ -229,6 +229,56 @@ def test_topk_all_equal_and_boundary_ties():
     assert list(oracle.topk_row(np.array([2.0, 1.0]), 4)) == [0, 1, -1, -1]
 
 
+def test_forced_selection_hand_worked_pages():
+    # 16-token pages.  len 100 (P = 7), sink 4, local 64: the sink is in page
+    # 0; tokens 36..99 are in pages 2..6.  With k = 7 every page is taken; with
+    # k = 6 the one page left out is page 1, the only unforced one.
+    s = np.arange(7, dtype=np.float64)[None, None, :] * -1.0      # page 0 scores highest
+    ctx = np.array([100], dtype=np.int32)
+    assert list(oracle.topk_forced(s, ctx, 16, 6, 4, 64)[0, 0]) == [0, 2, 3, 4, 5, 6]
+    # len 70 (P = 5), local 64 -> tokens 6..69: every page is forced; k = 3
+    # keeps the three lowest-index ones
+    ctx = np.array([70], dtype=np.int32)
+    assert list(oracle.topk_forced(s[:, :, :5], ctx, 16, 3, 0, 64)[0, 0]) == [0, 1, 2]
+    # len 64 (P = 4), local 16: only the last page; sink 17 -> pages 0 and 1;
+    # one free slot goes to the best of page 2 (score -2) alone
+    ctx = np.array([64], dtype=np.int32)
+    assert list(oracle.topk_forced(s[:, :, :4], ctx, 16, 4, 17, 16)[0, 0]) == [0, 1, 2, 3]
+    assert list(oracle.topk_forced(s[:, :, :4], ctx, 16, 3, 17, 16)[0, 0]) == [0, 1, 3]
+    # local 1: the page of the last token only (token 63 is in page 3)
+    assert list(oracle.topk_forced(s[:, :, :4], ctx, 16, 1, 0, 1)[0, 0]) == [3]
+    # sink 16 fills page 0 exactly and does not reach page 1
+    s2 = np.array([[[-5.0, -4.0, 0.0, 1.0]]])
+    assert list(oracle.topk_forced(s2, ctx, 16, 2, 16, 0)[0, 0]) == [0, 3]
+
+
+def test_forced_selection_matches_sort_with_forced_pages_at_plus_infinity():
+    # Library route: stable argsort of the scores with every forced page's
+    # score replaced by +inf picks the same set, for k below, at and above the
+    # number of forced pages, and reduces to plain top-K with nothing forced.
+    rng = _rng(50)
+    for trial in range(60):
+        ps = [16, 64][trial % 2]
+        P = int(rng.integers(1, 40))
+        L = int(rng.integers((P - 1) * ps + 1, P * ps + 1))
+        sink = int(rng.choice([0, 1, 4, 16, 40, 64]))
+        local = int(rng.choice([0, 1, 64, 200]))
+        k = int(rng.integers(1, P + 3))
+        sc = np.round(rng.standard_normal(P), 1)
+        got = oracle.topk_forced(sc[None, None, :], np.array([L], np.int32), ps, k, sink,
+                                 local)[0, 0]
+        tok_lo = np.arange(P) * ps
+        tok_hi = np.minimum(L, tok_lo + ps)
+        forced = ((sink > 0) & (tok_lo < sink)) | ((local > 0) & (tok_hi > L - local))
+        mod = np.where(forced, np.inf, sc)
+        pick = np.sort(np.argsort(-mod, kind="stable")[:min(k, P)])
+        ref = np.full(k, -1)
+        ref[:pick.size] = pick
+        assert np.array_equal(got, ref), (trial, P, L, sink, local, k)
+        if sink == 0 and local == 0:
+            assert np.array_equal(got, oracle.topk_row(sc, k))
+
+
 # ---------------------------------------------------------------- attention
 
 def _gather_dense(wl, b, h):
