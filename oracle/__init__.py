@@ -55,6 +55,16 @@ def _load():
             lib.okv_minmax_build.restype = None
             lib.okv_minmax_build.argtypes = [ctypes.c_int] + [ctypes.c_int] * 5 + [
                 _vp, _i32p, _i32p, _f64p, _f64p]
+            lib.okv_round_to_dtype.restype = ctypes.c_double
+            lib.okv_round_to_dtype.argtypes = [ctypes.c_int, ctypes.c_double]
+            lib.okv_page_mean.restype = None
+            lib.okv_page_mean.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                          ctypes.c_int64, _f64p]
+            lib.okv_mean_build.restype = None
+            lib.okv_mean_build.argtypes = [ctypes.c_int] + [ctypes.c_int] * 5 + [
+                _vp, _i32p, _i32p, _f64p]
+            lib.okv_mean_scores.restype = None
+            lib.okv_mean_scores.argtypes = [ctypes.c_int] * 7 + [_vp, _f64p, _i32p, _i32p, _f64p]
             lib.okv_append.restype = None
             lib.okv_append.argtypes = [ctypes.c_int] * 6 + [_vp, _vp, _vp, _vp, _i32p, _i32p,
                                                             _f64p, _f64p]
@@ -137,6 +147,61 @@ def minmax_build(dtype: str, k_cache: np.ndarray, block_table: np.ndarray,
     lib.okv_minmax_build(DTYPE_CODE[dtype], B, hkv, d, ps, maxP, k.ctypes.data, _ptr(bt, _i32p),
                          _ptr(ctx, _i32p), _ptr(mn, _f64p), _ptr(mx, _f64p))
     return mn, mx
+
+
+def round_to_dtype(dtype: str, x) -> np.ndarray:
+    """Nearest storage-type values (ties to even), as exact fp64 values."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    out = np.empty(a.shape)
+    flat, of = a.reshape(-1), out.reshape(-1)
+    code = DTYPE_CODE[dtype]
+    for i in range(flat.size):
+        of[i] = lib.okv_round_to_dtype(code, float(flat[i]))
+    return out
+
+
+def page_mean(dtype: str, page: np.ndarray, n: int | None = None) -> np.ndarray:
+    """Channel-wise mean of the first n tokens of a [ps][d] page, rounded to dtype."""
+    lib = _load()
+    a = _c(page)
+    ps, d = a.shape
+    n = ps if n is None else n
+    out = np.empty(d)
+    lib.okv_page_mean(DTYPE_CODE[dtype], d, n, a.ctypes.data, 0, _ptr(out, _f64p))
+    return out
+
+
+def mean_build(dtype: str, k_cache: np.ndarray, block_table: np.ndarray,
+               context_lens: np.ndarray) -> np.ndarray:
+    """[N_phys][Hkv][d] rounded page means (fp64 values); untouched entries NaN."""
+    lib = _load()
+    k = _c(k_cache)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    nphys, hkv, ps, d = k.shape
+    B, maxP = bt.shape
+    mean = np.full((nphys, hkv, d), np.nan)
+    lib.okv_mean_build(DTYPE_CODE[dtype], B, hkv, d, ps, maxP, k.ctypes.data, _ptr(bt, _i32p),
+                       _ptr(ctx, _i32p), _ptr(mean, _f64p))
+    return mean
+
+
+def mean_scores(dtype: str, q: np.ndarray, mean: np.ndarray, block_table: np.ndarray,
+                context_lens: np.ndarray, page_size: int) -> np.ndarray:
+    """[B][Hq][max_pages] fp64 q . mean scores (-inf past each row's last page)."""
+    lib = _load()
+    q = _c(q)
+    mean = _c(mean, np.float64)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    B, Hq, d = q.shape
+    Hkv = mean.shape[1]
+    maxP = bt.shape[1]
+    out = np.empty((B, Hq, maxP))
+    lib.okv_mean_scores(DTYPE_CODE[dtype], B, Hq, Hkv, d, page_size, maxP, q.ctypes.data,
+                        _ptr(mean, _f64p), _ptr(bt, _i32p), _ptr(ctx, _i32p), _ptr(out, _f64p))
+    return out
 
 
 def append_token(dtype: str, k_new: np.ndarray, v_new: np.ndarray, k_cache: np.ndarray,

@@ -128,6 +128,79 @@ void okv_minmax_build(int dtype, int B, int Hkv, int d, int ps, int max_pages,
 }
 
 /* ------------------------------------------------------------------------- */
+/* mean-key index: one representative key per page                            */
+/* ------------------------------------------------------------------------- */
+
+/* Nearest storage-type value to x, ties to the even significand (IEEE
+ * round-to-nearest-even), returned as its exact fp64 value.  f32: 24
+ * significant bits, f16: 11, bf16: 8; results that would fall below the
+ * type's normal range are not needed here (means of normal keys). */
+double okv_round_to_dtype(int dtype, double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  int bits = dtype == OKV_F32 ? 24 : dtype == OKV_F16 ? 11 : 8;
+  int e;
+  double m = frexp(x, &e);                     /* x = m * 2^e, 0.5 <= |m| < 1 */
+  double r = nearbyint(ldexp(m, bits));        /* default mode: ties to even */
+  return ldexp(r, e - bits);
+}
+
+/* Mean of the page's n valid keys, channel by channel, in fp64 (the sums of
+ * stored elements are exact here), then rounded once to the storage type.
+ * ShadowKV-style spatial chunking (KVDrive, sections 2.3 and 3, and the
+ * design overview: each page's mean key is its representative, half the
+ * index bytes of the min/max pair). */
+void okv_page_mean(int dtype, int d, int n, const void *k, int64_t off, double *mean) {
+  for (int c = 0; c < d; ++c) {
+    double sum = 0.0;
+    for (int t = 0; t < n; ++t) sum += okv_decode(dtype, k, off + (int64_t)t * d + c);
+    mean[c] = okv_round_to_dtype(dtype, sum / n);
+  }
+}
+
+/* Every (sequence, valid logical page, kv head): mean[phys][kvh][:] of
+ * [num_phys][Hkv][d]; entries of unreferenced pages are left untouched. */
+void okv_mean_build(int dtype, int B, int Hkv, int d, int ps, int max_pages, const void *k_cache,
+                    const int32_t *block_table, const int32_t *context_lens, double *mean) {
+  for (int b = 0; b < B; ++b) {
+    int len = context_lens[b];
+    int P = (len + ps - 1) / ps;
+    for (int p = 0; p < P; ++p) {
+      int n = len - p * ps < ps ? len - p * ps : ps;
+      int64_t phys = block_table[(int64_t)b * max_pages + p];
+      for (int kvh = 0; kvh < Hkv; ++kvh) {
+        int64_t off = ((phys * Hkv + kvh) * ps) * (int64_t)d;
+        okv_page_mean(dtype, d, n, k_cache, off, mean + (phys * Hkv + kvh) * (int64_t)d);
+      }
+    }
+  }
+}
+
+/* Mean-key page score: q . mean of the page (an estimate of q . k, not a
+ * bound), -inf for p >= P_b. */
+void okv_mean_scores(int dtype, int B, int Hq, int Hkv, int d, int ps, int max_pages,
+                     const void *q, const double *mean, const int32_t *block_table,
+                     const int32_t *context_lens, double *scores) {
+  int G = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    int P = (context_lens[b] + ps - 1) / ps;
+    for (int h = 0; h < Hq; ++h) {
+      double *row = scores + ((int64_t)b * Hq + h) * max_pages;
+      for (int p = 0; p < max_pages; ++p) {
+        if (p >= P) {
+          row[p] = -INFINITY;
+          continue;
+        }
+        int64_t phys = block_table[(int64_t)b * max_pages + p];
+        const double *m = mean + (phys * Hkv + h / G) * (int64_t)d;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += okv_decode(dtype, q, ((int64_t)b * Hq + h) * d + c) * m[c];
+        row[p] = s;
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* decode append: one new token per sequence                                   */
 /* ------------------------------------------------------------------------- */
 

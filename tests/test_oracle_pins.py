@@ -558,3 +558,107 @@ def test_attention_after_appending_to_an_empty_sequence_is_the_new_value():
                            wl.scale)
     for h in range(4):
         assert np.array_equal(out[0, h], vn[0, h // 2].astype(np.float64))
+
+
+# ---------------------------------------------------------------- mean-key index
+
+def _all_bf16_values():
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = ((bits >> 7) & 0xFF) != 0xFF
+    vals = (bits[finite] << 16).view(np.float32).astype(np.float64)
+    order = np.argsort(vals, kind="stable")
+    return vals[order], bits[finite][order]
+
+
+def _bf16_nearest_even(x):
+    """Brute force: the nearest finite bf16 value, ties to the even pattern."""
+    vals, bits = _all_bf16_values()
+    keep = np.concatenate([[True], np.diff(vals) != 0])        # one of +0/-0
+    vals, bits = vals[keep], bits[keep]
+    out = np.empty_like(x)
+    for i, v in enumerate(x.reshape(-1)):
+        j = np.searchsorted(vals, v)
+        cands = [c for c in (j - 1, j) if 0 <= c < vals.size]
+        best = min(cands, key=lambda c: (abs(vals[c] - v), int(bits[c]) & 1))
+        out.reshape(-1)[i] = vals[best]
+    return out
+
+
+def test_round_to_dtype_matches_library_and_brute_force():
+    rng = _rng(80)
+    x = np.concatenate([rng.standard_normal(400) * 10.0 ** rng.integers(-3, 4, 400),
+                        [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8),  # bf16 ties
+                         1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,                    # f16 ties
+                         1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 0.0]])             # f32 ties
+    assert np.array_equal(oracle.round_to_dtype("f16", x), x.astype(np.float16).astype(np.float64))
+    assert np.array_equal(oracle.round_to_dtype("f32", x), x.astype(np.float32).astype(np.float64))
+    assert np.array_equal(oracle.round_to_dtype("bf16", x), _bf16_nearest_even(x))
+    # the ties themselves: 1 + 2^-8 sits halfway between 1 and 1 + 2^-7 -> 1 (even)
+    assert oracle.round_to_dtype("bf16", np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert oracle.round_to_dtype("bf16", np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_page_mean_matches_numpy_mean_then_rounding(dtype):
+    rng = _rng(81)
+    for ps, n in [(16, 16), (16, 7), (64, 64), (64, 33), (16, 1)]:
+        x = rng.standard_normal((ps, 128)).astype(np.float32)
+        page = W.to_storage(x, dtype)
+        got = oracle.page_mean(dtype, page, n)
+        m = W.storage_to_f64(page, dtype)[:n].mean(axis=0)
+        if dtype == "f16":
+            ref = m.astype(np.float16).astype(np.float64)
+        elif dtype == "f32":
+            ref = m.astype(np.float32).astype(np.float64)
+        else:
+            ref = _bf16_nearest_even(m)
+        assert np.array_equal(got, ref), (ps, n)
+
+
+def test_mean_build_indirection_partial_pages_and_identical_keys():
+    spec = W.tiny_spec(dtype="f16", batch=3, hq=4, hkv=2, context=70, ps=16, index=82)
+    wl = W.generate(spec, context_lens=[70, 33, 16])
+    phys = wl.block_table[1, 2]                      # page 2 of row 1 holds 1 token
+    wl.k_cache[phys, :, 1:] = np.float16(1e4)        # garbage past the valid token
+    mean = oracle.mean_build("f16", wl.k_cache, wl.block_table, wl.context_lens)
+    k = W.storage_to_f64(wl.k_cache, "f16")
+    for b in range(3):
+        L = int(wl.context_lens[b])
+        for p in range(-(-L // 16)):
+            n = min(16, L - p * 16)
+            ph = wl.block_table[b, p]
+            ref = k[ph, :, :n].mean(axis=1).astype(np.float16).astype(np.float64)
+            assert np.array_equal(mean[ph], ref)
+    assert np.array_equal(mean[phys], k[phys, :, 0])     # one token: the mean is the key
+    used = {int(wl.block_table[b, p]) for b in range(3)
+            for p in range(-(-int(wl.context_lens[b]) // 16))}
+    unused = [i for i in range(spec.num_phys_pages) if i not in used]
+    assert np.isnan(mean[unused]).all()
+
+
+def test_mean_scores_gqa_head_and_block_table_by_brute_force():
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=6, hkv=2, context=50, ps=16, index=83)
+    wl = W.generate(spec, context_lens=[50, 17])
+    mean = oracle.mean_build("bf16", wl.k_cache, wl.block_table, wl.context_lens)
+    s = oracle.mean_scores("bf16", wl.q, mean, wl.block_table, wl.context_lens, 16)
+    q = W.storage_to_f64(wl.q, "bf16")
+    for b in range(2):
+        P = -(-int(wl.context_lens[b]) // 16)
+        for h in range(6):
+            for p in range(spec.max_pages):
+                if p >= P:
+                    assert s[b, h, p] == -np.inf
+                    continue
+                ref = float(np.dot(q[b, h], mean[wl.block_table[b, p], h // 3]))
+                assert abs(s[b, h, p] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_mean_score_of_a_single_token_page_is_q_dot_k():
+    spec = W.tiny_spec(dtype="bf16", batch=1, hq=2, hkv=1, context=17, ps=16, index=84)
+    wl = W.generate(spec)
+    mean = oracle.mean_build("bf16", wl.k_cache, wl.block_table, wl.context_lens)
+    s = oracle.mean_scores("bf16", wl.q, mean, wl.block_table, wl.context_lens, 16)
+    kk = W.storage_to_f64(wl.k_cache[wl.block_table[0, 1], 0, 0], "bf16")
+    for h in range(2):
+        qq = W.storage_to_f64(wl.q[0, h], "bf16")
+        assert abs(s[0, h, 1] - float(np.dot(qq, kk))) <= 1e-12 * (1 + abs(s[0, h, 1]))
