@@ -133,15 +133,19 @@ void okv_minmax_build(int dtype, int B, int Hkv, int d, int ps, int max_pages,
 
 /* Nearest storage-type value to x, ties to the even significand (IEEE
  * round-to-nearest-even), returned as its exact fp64 value.  f32: 24
- * significant bits, f16: 11, bf16: 8; results that would fall below the
- * type's normal range are not needed here (means of normal keys). */
+ * significant bits, f16: 11, bf16: 8.  The spacing of representable values
+ * near x is 2^(e - bits) for x = m * 2^e (0.5 <= |m| < 1); below the smallest
+ * normal 2^emin (f16: -14; f32, bf16: -126) it stays at the subnormal
+ * spacing 2^(emin - bits + 1).  Overflow is not needed here. */
 double okv_round_to_dtype(int dtype, double x) {
   if (x == 0.0 || !isfinite(x)) return x;
   int bits = dtype == OKV_F32 ? 24 : dtype == OKV_F16 ? 11 : 8;
+  int emin = dtype == OKV_F16 ? -14 : -126;
   int e;
-  double m = frexp(x, &e);                     /* x = m * 2^e, 0.5 <= |m| < 1 */
-  double r = nearbyint(ldexp(m, bits));        /* default mode: ties to even */
-  return ldexp(r, e - bits);
+  frexp(x, &e);
+  int qexp = e - bits > emin - bits + 1 ? e - bits : emin - bits + 1;
+  double r = nearbyint(ldexp(x, -qexp));       /* default mode: ties to even */
+  return ldexp(r, qexp);
 }
 
 /* Mean of the page's n valid keys, channel by channel, in fp64 (the sums of

@@ -589,7 +589,9 @@ def test_round_to_dtype_matches_library_and_brute_force():
     x = np.concatenate([rng.standard_normal(400) * 10.0 ** rng.integers(-3, 4, 400),
                         [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8),  # bf16 ties
                          1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,                    # f16 ties
-                         1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 0.0]])             # f32 ties
+                         1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 0.0,               # f32 ties
+                         3e-6, -7.7e-7, 2.0 ** -25, 3 * 2.0 ** -25, 5e-5,           # f16 subnormal
+                         1e-40, -3.3e-39, 2.0 ** -134, 3 * 2.0 ** -134]])          # f32/bf16 subnormal
     assert np.array_equal(oracle.round_to_dtype("f16", x), x.astype(np.float16).astype(np.float64))
     assert np.array_equal(oracle.round_to_dtype("f32", x), x.astype(np.float32).astype(np.float64))
     assert np.array_equal(oracle.round_to_dtype("bf16", x), _bf16_nearest_even(x))
