@@ -75,14 +75,15 @@ def dense_bytes(spec, ctx):
     return kv + q + out + 4 * pages + 4 * spec.batch
 
 
-def sparse_bytes(spec, ctx, indices):
+def sparse_bytes(spec, ctx, indices, table_rows=2):
     """(step bytes, attention bytes): score + select + attention over the union
-    of each (sequence, kv head) group's selected pages."""
+    of each (sequence, kv head) group's selected pages.  table_rows: 2 for the
+    min/max index, 1 for the mean-key index."""
     e = spec.elem_bytes
     B, Hq, Hkv, d, ps = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
     G = spec.group
     P = -(-np.asarray(ctx) // ps)
-    table = int(np.sum(P)) * Hkv * 2 * d * e                 # minmax read by page_score
+    table = int(np.sum(P)) * Hkv * table_rows * d * e        # index read by the page score
     scores = 2 * B * Hq * spec.max_pages * 4                 # written, then read by top-K
     idx_w = B * Hq * indices.shape[-1] * 4                   # written by top-K
     idx_r = B * Hq * indices.shape[-1] * 4                   # read by the union step
@@ -455,6 +456,29 @@ def main():
         f_total, _ = timed([("topk_forced", lambda: layer.select(sink_tokens=4, local_tokens=64))],
                            max(3, args.steps // 4), 3)
         extra["stages_ms"]["topk_select_forced_4_64"] = round(f_total / max(3, args.steps // 4), 5)
+        layer.select()
+        # the mean-key index: build, score, and the sparse step it drives
+        n_side = max(3, args.steps // 4)
+        layer.build_mean_index()
+        mb_total, _ = timed([("mean_build", layer.build_mean_index)], n_side, 3)
+        ms_total, _ = timed([("mean_score", layer.score_mean)], n_side, 3)
+        layer.score_mean()
+        layer.select()
+        torch.cuda.synchronize()
+        m_step, _ = sparse_bytes(spec, ctx, layer.indices.cpu().numpy(), table_rows=1)
+        mstep_total, _ = timed([("score_mean", layer.score_mean), ("topk_select", layer.select),
+                                ("sparse_attn", lambda: layer.sparse_attn())], n_side, 3)
+        kb = spec.num_kv_heads * int(np.sum(ctx)) * spec.head_dim * spec.elem_bytes
+        pages_all = int(np.sum(-(-ctx // spec.page_size)))
+        mtab = pages_all * spec.num_kv_heads * spec.head_dim * spec.elem_bytes
+        extra["mean_index"] = {
+            "build_ms": round(mb_total / n_side, 5),
+            "build_GB_s": round((kb + mtab) / (mb_total / n_side * 1e-3) / 1e9, 2),
+            "score_ms": round(ms_total / n_side, 5),
+            "score_GB_s": round(mtab / (ms_total / n_side * 1e-3) / 1e9, 2),
+            "sparse_step_ms": round(mstep_total / n_side, 5),
+            "sparse_step_GB_s": round(m_step / (mstep_total / n_side * 1e-3) / 1e9, 2)}
+        layer.score()
         layer.select()
         d_total, _ = timed([("dense_attn", layer.dense_step)], max(3, args.steps // 4), 3)
         d_ms = d_total / max(3, args.steps // 4)

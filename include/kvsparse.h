@@ -10,6 +10,7 @@
  *   kv_append_token       -> one new decode token per sequence into the cache,
  *                            with its page's min/max updated in place
  *   kv_page_score         -> q against the index: an upper bound on q.k
+ *   (kv_page_mean_build / kv_page_score_mean: the mean-key index instead)
  *   kv_topk_select        -> the K highest-scoring pages per query head
  *                            (kv_topk_select_forced: sink and local pages first)
  *   kv_sparse_decode_attn -> softmax attention over only those pages
@@ -136,6 +137,31 @@ int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new,
 int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
                   const int32_t *block_table, const int32_t *context_lens, float *scores,
                   void *stream);
+
+/* Mean-key page index (KVDrive, section 2.3: ShadowKV-style spatial chunking
+ * represents a block by its mean key; section 3, Finding 2: comparing the
+ * query with one mean key per block costs less than Quest's min and max; the
+ * design overview: half the index bytes of the min/max pair).
+ *   mean [N][Hkv][d] dtype, device memory.
+ * kv_page_mean_build: for every sequence b, valid logical page p and kv head,
+ * mean[block_table[b][p]][kvh][c] = (sum over the page's valid tokens of
+ * K[..][t][c]) / (number of valid tokens), rounded once to dtype (nearest,
+ * ties to even).  Sums run in fp32 (exact for typical 16-bit keys, whose page
+ * values span few binades), the division in fp64.  Entries of unreferenced
+ * pages are not written.
+ * kv_page_mean_refresh: the same for the page holding each row's last token
+ * only (B x Hkv entries) -- what an append changes.
+ * kv_page_score_mean: scores[b][h][p] = sum_c q_c * mean_c of page
+ * block_table[b][p], kv head h / G (an estimate of q . k, not a bound), fp32
+ * accumulation; p >= P_b -> -inf.  Same layouts and errors as kv_page_score;
+ * its output feeds kv_topk_select unchanged. */
+int kv_page_mean_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                       const int32_t *context_lens, void *mean, void *stream);
+int kv_page_mean_refresh(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                         const int32_t *context_lens, void *mean, void *stream);
+int kv_page_score_mean(const kv_shape *shape, const void *q, const void *mean,
+                       const int32_t *block_table, const int32_t *context_lens, float *scores,
+                       void *stream);
 
 /* Bytes of workspace kv_topk_select needs for this shape and k (may be 0). */
 size_t kv_topk_workspace_bytes(const kv_shape *shape, int32_t k);

@@ -489,10 +489,57 @@ int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
   if (dev < 0) return KV_ERR_CUDA;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
-  cudaError_t e = launch_page_score(shape->dtype, q, minmax, block_table, context_lens, scores,
-                                    shape->batch, shape->num_q_heads, shape->num_kv_heads,
-                                    shape->page_size, shape->max_pages_per_seq,
-                                    shape->num_phys_pages, status,
+  cudaError_t e = launch_page_score(shape->dtype, false, q, minmax, block_table, context_lens,
+                                    scores, shape->batch, shape->num_q_heads,
+                                    shape->num_kv_heads, shape->page_size,
+                                    shape->max_pages_per_seq, shape->num_phys_pages, status,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+static int mean_build_common(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                      const int32_t *context_lens, void *mean, bool last_only, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!al16(mean) || !al4(block_table) || !al4(context_lens)) return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  const void *kd = nullptr;
+  if ((rc = resolve_kv(shape, k_cache, &kd)) != KV_OK) return rc;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_mean_build(shape->dtype, kd, block_table, context_lens, mean,
+                                    shape->batch, shape->num_kv_heads, shape->page_size,
+                                    shape->max_pages_per_seq, shape->num_phys_pages, last_only,
+                                    status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+int kv_page_mean_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                       const int32_t *context_lens, void *mean, void *stream) {
+  return mean_build_common(shape, k_cache, block_table, context_lens, mean, false, stream);
+}
+
+int kv_page_mean_refresh(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
+                         const int32_t *context_lens, void *mean, void *stream) {
+  return mean_build_common(shape, k_cache, block_table, context_lens, mean, true, stream);
+}
+
+int kv_page_score_mean(const kv_shape *shape, const void *q, const void *mean,
+                       const int32_t *block_table, const int32_t *context_lens, float *scores,
+                       void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!al16(q) || !al16(mean) || !al16(scores) || !al4(block_table) || !al4(context_lens))
+    return KV_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaError_t e = launch_page_score(shape->dtype, true, q, mean, block_table, context_lens,
+                                    scores, shape->batch, shape->num_q_heads,
+                                    shape->num_kv_heads, shape->page_size,
+                                    shape->max_pages_per_seq, shape->num_phys_pages, status,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }

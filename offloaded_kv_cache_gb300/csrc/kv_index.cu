@@ -8,6 +8,8 @@
 //
 // Both kernels stream their input once with coalesced 16-byte loads; they are
 // HBM-bound (or host-link bound for a host-resident K cache in the build).
+#include <type_traits>
+
 #include "kv_internal.cuh"
 
 namespace kvs {
@@ -132,9 +134,10 @@ constexpr int kScoreWarps = 8;
 constexpr int kScorePagesPerWarp = 8;
 
 // One warp scores kScorePagesPerWarp pages of one (b, kv head, head chunk):
-// the pages' block-table entries arrive in one load, every min/max load is
+// the pages' block-table entries arrive in one load, every table load is
 // issued before any arithmetic, then each page's GS head sums are reduced.
-template <class T, int GS>
+// MEAN: the table row is the page's mean key and the score is q . mean.
+template <class T, int GS, bool MEAN>
 __global__ void __launch_bounds__(32 * kScoreWarps)
     page_score_kernel(const T *__restrict__ q, const T *__restrict__ mm,
                       const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
@@ -168,17 +171,22 @@ __global__ void __launch_bounds__(32 * kScoreWarps)
     if (ph >= 0 && ph < nphys) my_phys = ph;
     else flag_error(status, KV_ERR_BOUNDS);
   }
-  float mn[PPW][4], mx[PPW][4];
+  constexpr int kRows = MEAN ? 1 : 2;  // table rows per (page, kv head)
+  float mn[PPW][4], mx[PPW][MEAN ? 1 : 4];
 #pragma unroll
   for (int i = 0; i < PPW; ++i) {
     const long long phys = __shfl_sync(0xFFFFFFFFu, my_phys, i);
     if (phys >= 0) {
-      const T *row = mm + ((phys * Hkv + kvh) * 2) * kHeadDim + 4 * lane;
+      const T *row = mm + ((phys * Hkv + kvh) * kRows) * kHeadDim + 4 * lane;
       load4(row, mn[i]);
-      load4(row + kHeadDim, mx[i]);
+      if constexpr (!MEAN) load4(row + kHeadDim, mx[i]);
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) mn[i][e] = mx[i][e] = 0.f;
+      for (int e = 0; e < 4; ++e) mn[i][e] = 0.f;
+      if constexpr (!MEAN) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx[i][e] = 0.f;
+      }
     }
   }
   float qf[GS][4];
@@ -201,7 +209,9 @@ __global__ void __launch_bounds__(32 * kScoreWarps)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         // max(q*mn, q*mx) == q * (q >= 0 ? mx : mn) because mx >= mn
-        const float bound = qf[g][e] >= 0.f ? mx[i][e] : mn[i][e];
+        float bound;
+        if constexpr (MEAN) bound = mn[i][e];
+        else bound = qf[g][e] >= 0.f ? mx[i][e] : mn[i][e];
         s = fmaf(qf[g][e], bound, s);
       }
       part[g] = s;
@@ -250,7 +260,9 @@ __device__ __forceinline__ uint32_t sign_part(uint32_t w, bool neg) {
 
 constexpr int kScoreMmaWarps = 8;
 
-template <class T, int GS>
+// MEAN: the contraction runs over the 128-long mean row with q itself as the
+// coefficients (4 chunks per lane instead of 8).
+template <class T, int GS, bool MEAN>
 __global__ void __launch_bounds__(32 * kScoreMmaWarps)
     page_score_mma_kernel(const T *__restrict__ q, const T *__restrict__ mm,
                           const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
@@ -281,32 +293,38 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
   }
   const long long ph_a = __shfl_sync(0xFFFFFFFFu, ph_lane, gid);
   const long long ph_b = __shfl_sync(0xFFFFFFFFu, ph_lane, gid + 8);
-  uint4 ra[8], rb[8];
-  const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * 2 * kHeadDim);
-  const uint4 *rowb = reinterpret_cast<const uint4 *>(mm + ((ph_b < 0 ? 0 : ph_b) * Hkv + kvh) * 2 * kHeadDim);
+  constexpr int NCH = MEAN ? 4 : 8;       // 16-byte chunks per lane per row
+  constexpr int kRowElems = MEAN ? kHeadDim : 2 * kHeadDim;
+  uint4 ra[NCH], rb[NCH];
+  const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * kRowElems);
+  const uint4 *rowb = reinterpret_cast<const uint4 *>(mm + ((ph_b < 0 ? 0 : ph_b) * Hkv + kvh) * kRowElems);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NCH; ++i) {
     ra[i] = ph_a >= 0 ? rowa[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
     rb[i] = ph_b >= 0 ? rowb[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
   }
-  // coefficients [q- | q+] of head gid in the same k order
-  uint4 cf[8];
+  // coefficients of head gid in the same k order: [q- | q+] (min/max) or q (mean)
+  uint4 cf[NCH];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NCH; ++i) {
     cf[i] = make_uint4(0u, 0u, 0u, 0u);
     if (gid < GS) {
-      const int ch = tig + 4 * i;  // chunk of the 256-long [q- | q+] row
+      const int ch = tig + 4 * i;  // chunk of the coefficient row
       const uint4 w = reinterpret_cast<const uint4 *>(
           q + ((long long)b * Hq + head0 + gid) * kHeadDim)[ch & 15];
-      const bool neg = ch < 16;
-      cf[i] = make_uint4(sign_part(w.x, neg), sign_part(w.y, neg), sign_part(w.z, neg),
-                         sign_part(w.w, neg));
+      if constexpr (MEAN) {
+        cf[i] = w;
+      } else {
+        const bool neg = ch < 16;
+        cf[i] = make_uint4(sign_part(w.x, neg), sign_part(w.y, neg), sign_part(w.z, neg),
+                           sign_part(w.w, neg));
+      }
     }
   }
   pdl_trigger();
   float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NCH; ++i) {
     const uint32_t a0[4] = {ra[i].x, rb[i].x, ra[i].y, rb[i].y};
     mma_score(c, a0, cf[i].x, cf[i].y, T());
     const uint32_t a1[4] = {ra[i].z, rb[i].z, ra[i].w, rb[i].w};
@@ -324,7 +342,7 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
   }
 }
 
-template <class T>
+template <class T, bool MEAN>
 cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, const int32_t *ctx,
                            float *scores, int B, int Hq, int Hkv, int ps, int maxP,
                            long long nphys, int *status, cudaStream_t st) {
@@ -336,7 +354,7 @@ cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, con
       dim3 g((maxP + 16 * kScoreMmaWarps - 1) / (16 * kScoreMmaWarps), Hkv * nchunk, B);
       const T *qq = static_cast<const T *>(q);
       const T *m = static_cast<const T *>(mm);
-      auto kern = gs == 8 ? page_score_mma_kernel<T, 8> : page_score_mma_kernel<T, 4>;
+      auto kern = gs == 8 ? page_score_mma_kernel<T, 8, MEAN> : page_score_mma_kernel<T, 4, MEAN>;
       return launch_pdl(kern, g, dim3(32 * kScoreMmaWarps), 0, st, qq, m, bt, ctx, scores, Hq,
                         Hkv, ps, maxP, nphys, nchunk, status);
     }
@@ -345,10 +363,10 @@ cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, con
             Hkv * nchunk, B);
   const T *qq = static_cast<const T *>(q);
   const T *m = static_cast<const T *>(mm);
-  auto kern = gs == 8   ? page_score_kernel<T, 8>
-              : gs == 4 ? page_score_kernel<T, 4>
-              : gs == 2 ? page_score_kernel<T, 2>
-                        : page_score_kernel<T, 1>;
+  auto kern = gs == 8   ? page_score_kernel<T, 8, MEAN>
+              : gs == 4 ? page_score_kernel<T, 4, MEAN>
+              : gs == 2 ? page_score_kernel<T, 2, MEAN>
+                        : page_score_kernel<T, 1, MEAN>;
   return launch_pdl(kern, grid, dim3(32 * kScoreWarps), 0, st, qq, m, bt, ctx, scores, Hq, Hkv,
                     ps, maxP, nphys, nchunk, status);
 }
@@ -376,13 +394,152 @@ cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, con
   }
 }
 
-cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,
-                              const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
-                              int maxP, long long nphys, int *status, cudaStream_t st) {
+cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
+                              const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
+                              int Hkv, int ps, int maxP, long long nphys, int *status,
+                              cudaStream_t st) {
+#define KVS_SCORE(T, M) \
+  score_dispatch<T, M>(q, table, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st)
   switch (dtype) {
-    case KV_F32: return score_dispatch<float>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
-    case KV_F16: return score_dispatch<__half>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
-    default: return score_dispatch<__nv_bfloat16>(q, minmax, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st);
+    case KV_F32: return mean ? KVS_SCORE(float, true) : KVS_SCORE(float, false);
+    case KV_F16: return mean ? KVS_SCORE(__half, true) : KVS_SCORE(__half, false);
+    default: return mean ? KVS_SCORE(__nv_bfloat16, true) : KVS_SCORE(__nv_bfloat16, false);
+  }
+#undef KVS_SCORE
+}
+
+// ---------------------------------------------------------------------------
+// mean-key index: per (page, kv head), the mean of the valid keys
+// ---------------------------------------------------------------------------
+// Same lane layout as the min/max build (lane = 16-byte column chunk x row
+// group).  Sums accumulate in fp32 (exact for the usual 16-bit keys: the
+// values of one page span few enough binades).  The quotient by the token
+// count is rounded once to the storage type, ties to even: for a full page
+// (n a power of two) the fp32 division is exact, otherwise it runs in fp64
+// (fp64 is slow on this part, so only partial pages take that route).
+// last_only: one item per (b, kv head), the page holding the row's last
+// token -- the refresh after an append.
+namespace {
+
+template <class T>
+__device__ __forceinline__ uint16_t round16(float x) {
+  if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__float2half_rn(x));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <class T>
+__device__ __forceinline__ uint16_t round16(double x) {
+  if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__double2half(x));
+  else return __bfloat16_as_ushort(__double2bfloat16(x));
+}
+
+template <class T>
+__device__ __forceinline__ void store_mean(T *dst, const float (&s)[16 / sizeof(T)], int n) {
+  constexpr int E = 16 / sizeof(T);
+  const bool pow2 = (n & (n - 1)) == 0;
+  const float inv = 1.0f / (float)n;  // exact for a power of two
+  if constexpr (sizeof(T) == 4) {
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = pow2 ? s[j] * inv : (float)((double)s[j] / n);
+    *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+    uint32_t w[E / 2];
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) {
+      uint16_t lo, hi;
+      if (pow2) {
+        lo = round16<T>(s[2 * j] * inv);
+        hi = round16<T>(s[2 * j + 1] * inv);
+      } else {
+        lo = round16<T>((double)s[2 * j] / n);
+        hi = round16<T>((double)s[2 * j + 1] / n);
+      }
+      w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <class T>
+__global__ void __launch_bounds__(256)
+    mean_build_kernel(const T *__restrict__ k, const int32_t *__restrict__ bt,
+                      const int32_t *__restrict__ ctx, T *__restrict__ mean, int B, int Hkv,
+                      int ps, int maxP, long long nphys, int last_only, int *status) {
+  pdl_wait();
+  constexpr int C = kHeadDim * (int)sizeof(T) / 16;  // 16-byte chunks per row
+  constexpr int RG = 32 / C;                          // row groups per warp
+  constexpr int E = 16 / (int)sizeof(T);              // elements per chunk
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * 8 + warp;
+  const long long items = (long long)B * (last_only ? 1 : maxP) * Hkv;
+  if (item >= items) return;
+  const int kvh = (int)(item % Hkv);
+  const long long bp = item / Hkv;
+  const int b = (int)(last_only ? bp : bp / maxP);
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if ((last_only || bp % maxP == 0) && kvh == 0 && lane == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int p = last_only ? (len - 1) / ps : (int)(bp % maxP);
+  if (p * ps >= len) return;
+  const int n = min(ps, len - p * ps);
+  const long long phys = bt[(long long)b * maxP + p];
+  if (phys < 0 || phys >= nphys) {
+    if (lane == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int chunk = lane % C, rg = lane / C;
+  const uint4 *src = reinterpret_cast<const uint4 *>(k) + ((phys * Hkv + kvh) * ps) * C + chunk;
+  float s[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) s[e] = 0.f;
+#pragma unroll 4
+  for (int r = rg; r < n; r += RG) {
+    const uint4 x = src[(long long)r * C];
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack2(w[j], T());
+        s[2 * j] += f.x;
+        s[2 * j + 1] += f.y;
+      }
+    } else {
+      s[0] += __uint_as_float(x.x); s[1] += __uint_as_float(x.y);
+      s[2] += __uint_as_float(x.z); s[3] += __uint_as_float(x.w);
+    }
+  }
+  pdl_trigger();
+  if constexpr (RG == 2) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) s[e] += __shfl_xor_sync(0xFFFFFFFFu, s[e], 16);
+  }
+  if (rg == 0)
+    store_mean<T>(mean + (phys * Hkv + kvh) * kHeadDim + chunk * E, s, n);
+}
+
+}  // namespace
+
+cudaError_t launch_mean_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
+                              void *mean, int B, int Hkv, int ps, int maxP, long long nphys,
+                              bool last_only, int *status, cudaStream_t st) {
+  const long long items = (long long)B * (last_only ? 1 : maxP) * Hkv;
+  const unsigned blocks = (unsigned)((items + 7) / 8);
+  const int lo = last_only ? 1 : 0;
+  switch (dtype) {
+    case KV_F32:
+      return launch_pdl(mean_build_kernel<float>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const float *>(k), bt, ctx, static_cast<float *>(mean), B,
+                        Hkv, ps, maxP, nphys, lo, status);
+    case KV_F16:
+      return launch_pdl(mean_build_kernel<__half>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const __half *>(k), bt, ctx, static_cast<__half *>(mean), B,
+                        Hkv, ps, maxP, nphys, lo, status);
+    default:
+      return launch_pdl(mean_build_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, st,
+                        static_cast<const __nv_bfloat16 *>(k), bt, ctx,
+                        static_cast<__nv_bfloat16 *>(mean), B, Hkv, ps, maxP, nphys, lo, status);
   }
 }
 

@@ -258,9 +258,13 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void 
                           void *v_cache, const int32_t *bt, const int32_t *ctx,
                           int32_t *ctx_out, void *minmax, int B, int Hkv, int ps, int maxP,
                           long long nphys, int *status, cudaStream_t st);
-cudaError_t launch_page_score(int dtype, const void *q, const void *minmax, const int32_t *bt,
-                              const int32_t *ctx, float *scores, int B, int Hq, int Hkv, int ps,
-                              int maxP, long long nphys, int *status, cudaStream_t st);
+cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
+                              const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
+                              int Hkv, int ps, int maxP, long long nphys, int *status,
+                              cudaStream_t st);
+cudaError_t launch_mean_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
+                              void *mean, int B, int Hkv, int ps, int maxP, long long nphys,
+                              bool last_only, int *status, cudaStream_t st);
 cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
                         int k, int sink_tokens, int local_tokens, int32_t *indices, int *status,
                         cudaStream_t st);

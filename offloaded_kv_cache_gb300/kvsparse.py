@@ -63,6 +63,9 @@ def load(path: str = LIB_PATH):
         "kv_page_minmax_build": (ctypes.c_int, [S, P, P, P, P, P]),
         "kv_append_token": (ctypes.c_int, [S, P, P, P, P, P, P, P, P, P]),
         "kv_page_score": (ctypes.c_int, [S, P, P, P, P, P, P]),
+        "kv_page_mean_build": (ctypes.c_int, [S, P, P, P, P, P]),
+        "kv_page_mean_refresh": (ctypes.c_int, [S, P, P, P, P, P]),
+        "kv_page_score_mean": (ctypes.c_int, [S, P, P, P, P, P, P]),
         "kv_topk_workspace_bytes": (sz, [S, i32]),
         "kv_topk_select": (ctypes.c_int, [S, P, P, i32, P, P, sz, P]),
         "kv_topk_select_forced": (ctypes.c_int, [S, P, P, i32, i32, i32, P, P, sz, P]),
@@ -136,6 +139,26 @@ def kv_page_score(shape, q, minmax, block_table, context_lens, scores, stream=No
     rc = load().kv_page_score(ctypes.byref(shape), _ptr(q), _ptr(minmax), _ptr(block_table),
                               _ptr(context_lens), _ptr(scores), _stream(stream))
     return _ret(rc, "kv_page_score", check)
+
+
+def kv_page_mean_build(shape, k_cache, block_table, context_lens, mean, stream=None, check=True):
+    rc = load().kv_page_mean_build(ctypes.byref(shape), _ptr(k_cache), _ptr(block_table),
+                                   _ptr(context_lens), _ptr(mean), _stream(stream))
+    return _ret(rc, "kv_page_mean_build", check)
+
+
+def kv_page_mean_refresh(shape, k_cache, block_table, context_lens, mean, stream=None,
+                         check=True):
+    rc = load().kv_page_mean_refresh(ctypes.byref(shape), _ptr(k_cache), _ptr(block_table),
+                                     _ptr(context_lens), _ptr(mean), _stream(stream))
+    return _ret(rc, "kv_page_mean_refresh", check)
+
+
+def kv_page_score_mean(shape, q, mean, block_table, context_lens, scores, stream=None,
+                       check=True):
+    rc = load().kv_page_score_mean(ctypes.byref(shape), _ptr(q), _ptr(mean), _ptr(block_table),
+                                   _ptr(context_lens), _ptr(scores), _stream(stream))
+    return _ret(rc, "kv_page_score_mean", check)
 
 
 def kv_topk_workspace_bytes(shape, k) -> int:

@@ -5,6 +5,7 @@ outputs and workspaces the C ABI needs, and runs the path through the ctypes
 binding:
 
     build_index()  -> kv_page_minmax_build
+    build_mean_index(), score_mean() -> kv_page_mean_build, kv_page_score_mean
     append()       -> kv_append_token
     sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
     dense_step()   -> kv_dense_decode_attn
@@ -83,6 +84,7 @@ class DecodeLayer:
                                    device=dev)
         self.out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim),
                                dtype=torch.float32, device=dev)
+        self.mean = None  # the mean-key index, allocated by build_mean_index()
         self.ws_dense_bytes = kv.kv_attn_workspace_bytes(self.shape, 0)
         self.ws_sparse_bytes = kv.kv_attn_workspace_bytes(self.shape, k) if self.topk else 0
         self.ws_topk_bytes = kv.kv_topk_workspace_bytes(self.shape, k)
@@ -114,6 +116,20 @@ class DecodeLayer:
         kv.kv_append_token(self.shape, k_new, v_new, self.k_cache, self.v_cache, self.block_table,
                            self.context_lens, self.context_lens if advance else None,
                            self.minmax if update_index else None, stream)
+
+    def build_mean_index(self, stream=None, last_only=False):
+        stream = self._st(stream)
+        if self.mean is None:
+            spec = self.spec
+            self.mean = torch.zeros((spec.num_phys_pages, spec.num_kv_heads, spec.head_dim),
+                                    dtype=TORCH_DTYPE[spec.dtype], device=self.device)
+        fn = kv.kv_page_mean_refresh if last_only else kv.kv_page_mean_build
+        fn(self.shape, self.k_cache, self.block_table, self.context_lens, self.mean, stream)
+
+    def score_mean(self, stream=None):
+        stream = self._st(stream)
+        kv.kv_page_score_mean(self.shape, self.q, self.mean, self.block_table, self.context_lens,
+                              self.scores, stream)
 
     def score(self, stream=None):
         stream = self._st(stream)
@@ -154,3 +170,6 @@ class DecodeLayer:
     # --- host views --------------------------------------------------------
     def minmax_bits(self) -> np.ndarray:
         return torch_to_bits(self.minmax)
+
+    def mean_bits(self) -> np.ndarray:
+        return torch_to_bits(self.mean)

@@ -65,6 +65,9 @@ def test_bad_shapes_rejected_by_every_entry_point(kvlib, kw, code):
     s = _shape(**kw)
     assert kv.kv_page_minmax_build(s, FAKE, FAKE, FAKE, FAKE, check=False) == code
     assert kv.kv_page_score(s, FAKE, FAKE, FAKE, FAKE, FAKE, check=False) == code
+    assert kv.kv_page_mean_build(s, FAKE, FAKE, FAKE, FAKE, check=False) == code
+    assert kv.kv_page_mean_refresh(s, FAKE, FAKE, FAKE, FAKE, check=False) == code
+    assert kv.kv_page_score_mean(s, FAKE, FAKE, FAKE, FAKE, FAKE, check=False) == code
     assert kv.kv_append_token(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                               check=False) == code
     assert kv.kv_topk_select(s, FAKE, FAKE, 4, FAKE, check=False) == code
@@ -81,6 +84,12 @@ def test_null_and_misaligned_pointers_rejected(kvlib):
     assert kv.kv_page_minmax_build(s, FAKE, FAKE, FAKE, None, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_page_minmax_build(s, FAKE, FAKE, FAKE, FAKE + 8, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_page_score(s, FAKE + 4, FAKE, FAKE, FAKE, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_page_mean_build(s, FAKE, FAKE, FAKE, FAKE + 8, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_page_mean_refresh(s, FAKE, FAKE, FAKE, None, check=False) == \
+        kv.KV_ERR_INVALID_ARG
+    assert kv.kv_page_score_mean(s, FAKE, FAKE + 4, FAKE, FAKE, FAKE, check=False) == \
+        kv.KV_ERR_INVALID_ARG
     assert kv.kv_page_score(s, FAKE, FAKE, FAKE + 2, FAKE, FAKE, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_append_token(s, None, FAKE, FAKE, FAKE, FAKE, FAKE, check=False) == \
         kv.KV_ERR_INVALID_ARG
