@@ -80,6 +80,9 @@ def _load():
             lib.okv_topk_forced.restype = None
             lib.okv_topk_forced.argtypes = [ctypes.c_int] * 4 + [
                 _i32p, _f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p]
+            lib.okv_window_step.restype = ctypes.c_int
+            lib.okv_window_step.argtypes = [ctypes.c_int] * 6 + [
+                _i32p, _i32p, ctypes.c_int, _f64p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
             lib.okv_attention_row.restype = None
             lib.okv_attention_row.argtypes = [ctypes.c_int] * 5 + [
                 ctypes.c_double, _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int, _i32p,
@@ -292,6 +295,42 @@ def topk_forced(scores_arr: np.ndarray, context_lens: np.ndarray, page_size: int
     lib.okv_topk_forced(B, Hq, page_size, maxP, _ptr(ctx, _i32p), _ptr(s, _f64p), k,
                         int(sink_tokens), int(local_tokens), _ptr(out, _i32p))
     return out
+
+
+class Window:
+    """State of the GPU-resident page window, one group per (sequence, kv head)."""
+
+    def __init__(self, batch: int, num_kv_heads: int, max_pages: int, cache_pages: int):
+        self.C = cache_pages
+        self.slot_page = np.full((batch, num_kv_heads, cache_pages), -1, dtype=np.int32)
+        self.page_slot = np.full((batch, num_kv_heads, max_pages), -1, dtype=np.int32)
+
+    def step(self, indices: np.ndarray, scores_arr: np.ndarray, context_lens: np.ndarray,
+             page_size: int):
+        """One decode step; returns (fetch list [(page, slot)] per group, stats
+        [B][Hkv][4] = needed, hits, fetched, evicted)."""
+        lib = _load()
+        idx = _c(indices, np.int32)
+        s = _c(scores_arr, np.float64)
+        ctx = _c(context_lens, np.int32)
+        B, Hq, K = idx.shape
+        _, Hkv, C = self.slot_page.shape
+        maxP = self.page_slot.shape[2]
+        fpage = np.full((B, Hkv, C), -1, dtype=np.int32)
+        fslot = np.full((B, Hkv, C), -1, dtype=np.int32)
+        fcount = np.zeros((B, Hkv), dtype=np.int32)
+        stats = np.zeros((B, Hkv, 4), dtype=np.int32)
+        rc = lib.okv_window_step(B, Hq, Hkv, page_size, maxP, C, _ptr(ctx, _i32p),
+                                 _ptr(idx, _i32p), K, _ptr(s, _f64p),
+                                 _ptr(self.slot_page, _i32p), _ptr(self.page_slot, _i32p),
+                                 _ptr(fpage, _i32p), _ptr(fslot, _i32p), _ptr(fcount, _i32p),
+                                 _ptr(stats, _i32p))
+        if rc != 0:
+            raise ValueError("a group needs more pages than the window holds")
+        fetch = [[list(zip(fpage[b, h, :fcount[b, h]].tolist(),
+                           fslot[b, h, :fcount[b, h]].tolist()))
+                  for h in range(Hkv)] for b in range(B)]
+        return fetch, stats
 
 
 def attention(dtype: str, q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,

@@ -373,6 +373,139 @@ void okv_topk_forced(int B, int Hq, int ps, int max_pages, const int32_t *contex
 }
 
 /* ------------------------------------------------------------------------- */
+/* GPU-resident window of critical pages                                       */
+/* ------------------------------------------------------------------------- */
+
+/* KVDrive, section 5.1 "Sliding window with lookahead eviction": the GPU keeps
+ * a window of recently critical KV entries; each decode step fetches from host
+ * memory only the critical entries the window lacks and evicts the entries
+ * with the lowest attention score of the current step, the least likely to be
+ * reused.  Section 3, Finding 1 sizes it in multiples (x N) of the per-step
+ * budget.
+ *
+ * Unit: one (sequence b, kv head) group with C slots, each holding one page of
+ * that kv head.  State: slot_page[g][C] (logical page or -1) and
+ * page_slot[g][max_pages] (slot or -1).  One step, given the selection
+ * indices[b][h][K] of the group's G query heads and this step's page scores:
+ *   need    = the pages any of the G heads selected (p < P_b);
+ *   hits    = needed pages already in a slot; misses = the others;
+ *   a cached page at or past P_b scores -inf (stale); a cached page that is
+ *   not needed scores max over the G heads of scores[b][h][page];
+ *   evict   = the (misses - free slots) non-needed cached pages with the
+ *             lowest score, ties to the lower slot;
+ *   assign  = misses in ascending page order take the free and evicted slots
+ *             in ascending slot order;
+ *   fetch   = the misses, plus the row's last page when it is a hit (the
+ *             cached copy may lack tokens appended since), each with its
+ *             slot, in ascending page order.
+ * Requires C >= |need|.  stats[g] = {needed, hits, fetched, evicted}. */
+static const double *g_evict_score;
+static int by_evict_order(const void *pa, const void *pb) {
+  int a = *(const int *)pa, b = *(const int *)pb; /* slots */
+  double sa = g_evict_score[a], sb = g_evict_score[b];
+  if (sa < sb) return -1;
+  if (sa > sb) return 1;
+  return (a > b) - (a < b);
+}
+
+int okv_window_step(int B, int Hq, int Hkv, int ps, int max_pages, int C,
+                    const int32_t *context_lens, const int32_t *indices, int K,
+                    const double *scores, int32_t *slot_page, int32_t *page_slot,
+                    int32_t *fetch_page, int32_t *fetch_slot, int32_t *fetch_count,
+                    int32_t *stats) {
+  int G = Hq / Hkv;
+  char *need = (char *)malloc(max_pages > 0 ? max_pages : 1);
+  double *escore = (double *)malloc(sizeof(double) * C);
+  int *cand = (int *)malloc(sizeof(int) * C);
+  int *freed = (int *)malloc(sizeof(int) * C);
+  int *is_freed = (int *)malloc(sizeof(int) * C);
+  int rc = 0;
+  for (int b = 0; b < B; ++b) {
+    int len = context_lens[b];
+    int P = (len + ps - 1) / ps;
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      int64_t g = (int64_t)b * Hkv + kvh;
+      int32_t *sp = slot_page + g * C;
+      int32_t *ps_map = page_slot + g * max_pages;
+      memset(need, 0, max_pages);
+      int n_need = 0;
+      for (int h = kvh * G; h < (kvh + 1) * G; ++h)
+        for (int i = 0; i < K; ++i) {
+          int p = indices[((int64_t)b * Hq + h) * K + i];
+          if (p >= 0 && p < P && !need[p]) {
+            need[p] = 1;
+            ++n_need;
+          }
+        }
+      if (n_need > C) {
+        rc = -1;
+        continue;
+      }
+      int n_hit = 0, n_free = 0, n_cand = 0;
+      for (int s = 0; s < C; ++s) {
+        is_freed[s] = 0;
+        int p = sp[s];
+        if (p < 0) {
+          is_freed[s] = 1;
+          ++n_free;
+        } else if (p < P && need[p]) {
+          ++n_hit;
+        } else {
+          double sc = -INFINITY;
+          if (p < P)
+            for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+              double v = scores[((int64_t)b * Hq + h) * max_pages + p];
+              if (v > sc) sc = v;
+            }
+          escore[s] = sc;
+          cand[n_cand++] = s;
+        }
+      }
+      int n_miss = n_need - n_hit;
+      int n_evict = n_miss > n_free ? n_miss - n_free : 0;
+      g_evict_score = escore;
+      qsort(cand, n_cand, sizeof(int), by_evict_order);
+      for (int i = 0; i < n_evict; ++i) {
+        int s = cand[i];
+        ps_map[sp[s]] = -1;
+        sp[s] = -1;
+        is_freed[s] = 1;
+      }
+      int nf = 0;
+      for (int s = 0; s < C; ++s)
+        if (is_freed[s]) freed[nf++] = s;
+      int r = 0, nfetch = 0;
+      int32_t *fp = fetch_page + g * C;
+      int32_t *fs = fetch_slot + g * C;
+      for (int p = 0; p < P; ++p) {
+        if (!need[p]) continue;
+        if (ps_map[p] < 0) { /* a miss: next free slot */
+          int s = freed[r++];
+          sp[s] = p;
+          ps_map[p] = s;
+          fp[nfetch] = p;
+          fs[nfetch++] = s;
+        } else if (p == P - 1) { /* a hit on the growing last page: refresh */
+          fp[nfetch] = p;
+          fs[nfetch++] = ps_map[p];
+        }
+      }
+      fetch_count[g] = nfetch;
+      stats[g * 4 + 0] = n_need;
+      stats[g * 4 + 1] = n_hit;
+      stats[g * 4 + 2] = nfetch;
+      stats[g * 4 + 3] = n_evict;
+    }
+  }
+  free(need);
+  free(escore);
+  free(cand);
+  free(freed);
+  free(is_freed);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------- */
 /* attention of one query head over a set of pages                             */
 /* ------------------------------------------------------------------------- */
 

@@ -664,3 +664,112 @@ def test_mean_score_of_a_single_token_page_is_q_dot_k():
     for h in range(2):
         qq = W.storage_to_f64(wl.q[0, h], "bf16")
         assert abs(s[0, h, 1] - float(np.dot(qq, kk))) <= 1e-12 * (1 + abs(s[0, h, 1]))
+
+
+# ---------------------------------------------------------------- page window
+
+def _window_scenario(seed, steps, B=2, Hq=4, Hkv=2, maxP=40, K=5, C=14, ps=16, drift=0.3):
+    """Selections and scores of a slowly drifting query: each step keeps most
+    of the previous step's high-scoring pages."""
+    rng = _rng(seed)
+    base = rng.standard_normal((B, Hq, maxP))
+    ctx = np.array([maxP * ps - 3, (maxP - 9) * ps], dtype=np.int32)
+    out = []
+    for _ in range(steps):
+        base = base + drift * rng.standard_normal(base.shape)
+        s = np.round(base, 2)
+        for b in range(B):
+            s[b, :, -(-int(ctx[b]) // ps):] = -np.inf
+        idx = oracle.topk(s, ctx, ps, K)
+        out.append((idx, s))
+    return ctx, out
+
+
+def _needed(idx, ctx, ps, b, kvh, G):
+    P = -(-int(ctx[b]) // ps)
+    sel = idx[b, kvh * G:(kvh + 1) * G].reshape(-1)
+    return {int(p) for p in sel if 0 <= p < P}
+
+
+def test_window_repeated_selection_hits_everything():
+    ctx, steps = _window_scenario(90, 1)
+    idx, s = steps[0]
+    w = oracle.Window(2, 2, 40, 14)
+    _, st1 = w.step(idx, s, ctx, 16)
+    assert (st1[..., 1] == 0).all() and (st1[..., 2] == st1[..., 0]).all()
+    fetch, st2 = w.step(idx, s, ctx, 16)
+    assert (st2[..., 1] == st2[..., 0]).all() and (st2[..., 3] == 0).all()
+    for b in range(2):
+        P = -(-int(ctx[b]) // 16)
+        for kvh in range(2):
+            need = _needed(idx, ctx, 16, b, kvh, 2)
+            # only the growing last page is fetched again, and only if needed
+            assert [p for p, _ in fetch[b][kvh]] == ([P - 1] if P - 1 in need else [])
+
+
+def test_window_invariants_and_lookahead_eviction_by_brute_force():
+    ctx, steps = _window_scenario(91, 12)
+    C, G, ps = 14, 2, 16
+    w = oracle.Window(2, 2, 40, C)
+    for idx, s in steps:
+        before = w.slot_page.copy()
+        fetch, st = w.step(idx, s, ctx, ps)
+        for b in range(2):
+            P = -(-int(ctx[b]) // ps)
+            for kvh in range(2):
+                need = _needed(idx, ctx, ps, b, kvh, G)
+                old = before[b, kvh]
+                cached_old = {int(p) for p in old if p >= 0}
+                misses = sorted(need - cached_old)
+                free = [i for i in range(C) if old[i] < 0]
+                cands = [i for i in range(C) if old[i] >= 0 and int(old[i]) not in need]
+                score = {i: (s[b, kvh * G:(kvh + 1) * G, old[i]].max() if old[i] < P else -np.inf)
+                         for i in cands}
+                n_ev = max(0, len(misses) - len(free))
+                evicted = sorted(cands, key=lambda i: (score[i], i))[:n_ev]
+                freed = sorted(free + evicted)
+                expect = old.copy()
+                expect[evicted] = -1
+                for p, slot in zip(misses, freed):
+                    expect[slot] = p
+                assert np.array_equal(w.slot_page[b, kvh], expect)
+                # the two maps are inverse to each other and every needed page is in
+                for slot, p in enumerate(w.slot_page[b, kvh]):
+                    if p >= 0:
+                        assert w.page_slot[b, kvh, p] == slot
+                assert (w.page_slot[b, kvh] >= 0).sum() == (w.slot_page[b, kvh] >= 0).sum()
+                assert all(w.page_slot[b, kvh, p] >= 0 for p in need)
+                fetched = [p for p, _ in fetch[b][kvh]]
+                assert fetched == sorted(set(misses) | ({P - 1} & (need - set(misses))))
+                assert tuple(st[b, kvh]) == (len(need), len(need) - len(misses), len(fetched),
+                                             n_ev)
+
+
+def test_window_large_enough_never_evicts():
+    ctx, steps = _window_scenario(92, 10)
+    w = oracle.Window(2, 2, 40, 40)
+    seen = [[set(), set()], [set(), set()]]
+    for idx, s in steps:
+        _, st = w.step(idx, s, ctx, 16)
+        assert (st[..., 3] == 0).all()
+        for b in range(2):
+            for kvh in range(2):
+                seen[b][kvh] |= _needed(idx, ctx, 16, b, kvh, 2)
+                assert {int(p) for p in w.slot_page[b, kvh] if p >= 0} == seen[b][kvh]
+
+
+def test_window_evicts_stale_pages_first_and_refuses_overflow():
+    # slots hold pages 0 and 5; the row now has 4 pages, so page 5 is stale
+    # (-inf) and goes before page 0 although page 0 scores lowest of the rest
+    w = oracle.Window(1, 1, 8, 2)
+    w.slot_page[0, 0] = [0, 5]
+    w.page_slot[0, 0, 0], w.page_slot[0, 0, 5] = 0, 1
+    s = np.array([[[-5.0, 1.0, 2.0, 3.0, -np.inf, -np.inf, -np.inf, -np.inf]]])
+    _, st = w.step(np.array([[[3, -1]]], dtype=np.int32), s, np.array([4 * 16], np.int32), 16)
+    assert list(w.slot_page[0, 0]) == [0, 3] and tuple(st[0, 0]) == (1, 0, 1, 1)
+    assert w.page_slot[0, 0, 5] == -1 and w.page_slot[0, 0, 3] == 1
+    # two misses: page 0 (lowest score, not needed) is evicted next
+    _, st = w.step(np.array([[[1, 3]]], dtype=np.int32), s, np.array([4 * 16], np.int32), 16)
+    assert list(w.slot_page[0, 0]) == [1, 3] and tuple(st[0, 0]) == (2, 1, 2, 1)
+    with pytest.raises(ValueError):
+        w.step(np.array([[[0, 1, 2]]], dtype=np.int32), s, np.array([4 * 16], np.int32), 16)
