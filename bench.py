@@ -100,6 +100,80 @@ def sparse_bytes(spec, ctx, indices, table_rows=2):
     return table + q + scores + idx_w + attn, attn
 
 
+def window_measurement(spec, wl, layer, steps=128, sigma=0.5, reps=2):
+    """Decode sequence of `steps` drifting queries through the page window
+    (x1 and x2 of the per-step budget G*K per (sequence, kv head)) against the
+    same steps read zero-copy: per-step time, hit rate, host-link bytes.
+
+    Each variant's whole sequence is one CUDA graph; every step also writes a
+    256 MiB buffer (twice the L2) so no step reads the previous step's pages
+    from L2, and that flush's own time, measured alone, is subtracted.  Hit
+    rates come from an eager pass over the sequence that starts from the
+    state the timed replays start from."""
+    import torch
+    from offloaded_kv_cache_gb300 import kvsparse as kv
+    from offloaded_kv_cache_gb300 import workloads as W
+    from offloaded_kv_cache_gb300.pipeline import storage_to_torch
+    qs = [storage_to_torch(q, spec.dtype).cuda() for q in
+          W.drifting_queries(spec, wl.q, steps, sigma)]
+    q0 = layer.q
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    page_bytes = 2 * spec.page_size * spec.head_dim * spec.elem_bytes   # K + V, one kv head
+
+    def step(t, attn):
+        flush.fill_(t & 0xFF)
+        if attn is None:
+            return
+        layer.q = qs[t]
+        layer.score()
+        layer.select()
+        attn()
+
+    def graph_ms(attn):
+        for _ in range(2):                       # eager warm-up passes
+            for t in range(steps):
+                step(t, attn)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for t in range(steps):
+                step(t, attn)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * steps)
+
+    flush_ms = graph_ms(None)
+    res = {"steps": steps, "query_drift_sigma": sigma, "l2_flush_ms_subtracted": round(flush_ms, 5)}
+    res["zero_copy_ms_per_step"] = round(graph_ms(lambda: layer.sparse_attn()) - flush_ms, 5)
+    for mult in (1, 2):
+        C = mult * spec.group * layer.topk
+        layer.enable_window(C)
+        ms = graph_ms(lambda: layer.window_attn()) - flush_ms
+        hits = need = fetched = 0
+        for t in range(steps):                   # same start state as a replay
+            step(t, lambda: layer.window_attn())
+            torch.cuda.synchronize()
+            st = layer.win_stats.cpu().numpy()
+            need += int(st[..., 0].sum())
+            hits += int(st[..., 1].sum())
+            fetched += int(st[..., 2].sum())
+        assert kv.kv_device_status() == kv.KV_OK
+        res[f"x{mult}"] = {"cache_pages": C, "hit_rate": round(hits / max(1, need), 4),
+                           "needed_pages_per_step": round(need / steps, 1),
+                           "fetched_pages_per_step": round(fetched / steps, 1),
+                           "host_MB_per_step": round(fetched / steps * page_bytes / 1e6, 3),
+                           "ms_per_step": round(ms, 5)}
+    layer.q = q0
+    del flush
+    return res
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -484,6 +558,8 @@ def main():
         d_ms = d_total / max(3, args.steps // 4)
         db = dense_bytes(spec, ctx)
         extra["dense"] = {"ms_per_step": round(d_ms, 4), "GB_s": round(db / (d_ms * 1e-3) / 1e9, 2)}
+        if spec.kv_loc == "host":
+            extra["window"] = window_measurement(spec, wl, layer)
     ib_total, _ = timed([("index_build", layer.build_index)], max(3, args.steps // 4), 3)
     ib_ms = ib_total / max(3, args.steps // 4)
     kbytes = spec.num_kv_heads * int(np.sum(ctx)) * spec.head_dim * spec.elem_bytes

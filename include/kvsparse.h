@@ -14,6 +14,8 @@
  *   kv_topk_select        -> the K highest-scoring pages per query head
  *                            (kv_topk_select_forced: sink and local pages first)
  *   kv_sparse_decode_attn -> softmax attention over only those pages
+ *                            (kv_sparse_decode_attn_window: through a
+ *                            GPU-resident window of recently critical pages)
  *   kv_dense_decode_attn  -> the same over every page (Dual-Blade, "Background
  *                            and key observations": decode reads all prior KV)
  * K/V pages live in device memory (HBM) or in pinned host memory that the GPU
@@ -254,6 +256,60 @@ int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q, const voi
  * blocks per SM are used).  Time it with events on `stream`. */
 int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
                          int32_t sink_words, void *stream);
+
+/* GPU-resident window of critical pages (KVDrive, section 5.1 "Sliding
+ * window with lookahead eviction"; section 3, Finding 1: a window of several
+ * steps' critical entries cuts host-to-GPU transfer; section 6.3: with most
+ * critical entries served from GPU memory, attention stays on the GPU).
+ *
+ * The window has one group per (sequence b, kv head) with C = cache_pages
+ * slots; slot s of group (b, kvh) holds one page of that kv head at
+ *   cache_k / cache_v [B * C][Hkv][ps][d] dtype, device memory,
+ * page index b * C + s.  State (device memory, owned by the caller):
+ *   slot_page [B][Hkv][C]     logical page in the slot, -1 = free
+ *   page_slot [B][Hkv][maxP]  slot of a logical page, -1 = not cached
+ *   stats     [B][Hkv][4]     (may be NULL) of the last call: pages needed,
+ *                             hits, pages fetched, pages evicted.
+ * kv_window_reset empties the window (both maps to -1). */
+typedef struct {
+  int32_t cache_pages; /* C >= min(G * k, maxP); maxP + 8 C <= 200 KiB */
+  int32_t reserved;
+  void *cache_k;
+  void *cache_v;
+  int32_t *slot_page;
+  int32_t *page_slot;
+  int32_t *stats;
+} kv_window;
+
+/* Workspace for kv_sparse_decode_attn_window with this shape, k and C. */
+size_t kv_window_workspace_bytes(const kv_shape *shape, int32_t k, int32_t cache_pages);
+
+int kv_window_reset(const kv_shape *shape, const kv_window *win, void *stream);
+
+/* One decode step of sparse attention through the window.  Inputs as
+ * kv_sparse_decode_attn (k_cache / v_cache where kv_loc says, typically
+ * pinned host memory), plus this step's page scores [B][Hq][maxP] (the
+ * kv_page_score output the indices were selected from).  Per group:
+ *   need    = pages any of the G query heads selected;
+ *   hits    = needed pages already in the window, misses = the rest;
+ *   evict   = as many non-needed cached pages as the misses need slots,
+ *             lowest score first (score = max over the G heads this step;
+ *             pages at or past the row's end first; ties to the lower slot);
+ *   assign  = misses in ascending page order take the free slots in
+ *             ascending slot order;
+ *   fetch   = the misses, and the row's last page when it is a hit (tokens
+ *             may have been appended since it was copied): their valid
+ *             tokens are copied from k_cache / v_cache into the window;
+ * then attention runs over the window (HBM) exactly as kv_sparse_decode_attn
+ * -- same out.  C must hold every needed page: C >= min(G * k, maxP), else
+ * KV_ERR_INVALID_ARG.  cache_k / cache_v must be device memory
+ * (KV_ERR_LOCATION).  The workspace must hold kv_window_workspace_bytes. */
+int kv_sparse_decode_attn_window(const kv_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_table,
+                                 const int32_t *context_lens, const int32_t *indices, int32_t k,
+                                 const float *scores, float scale, float *out,
+                                 const kv_window *win, void *workspace, size_t workspace_bytes,
+                                 void *stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: KV_OK, KV_ERR_DEVICE_TIMEOUT or KV_ERR_BOUNDS (the

@@ -350,9 +350,31 @@ int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
   return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
 }
 
+// The page window's part of an attention call: its state, this step's page
+// scores, and the shape the attention sees (K/V = the window arrays).
+struct WindowCall {
+  const kv_window *win;
+  const float *scores;
+  kv_shape wshape;  // num_phys_pages = B * C, kv_loc = HBM
+};
+
+// Window shape and workspace: the attention plan of the window shape, then
+// the fetch lists [B][Hkv][C] (page, slot) and counts [B][Hkv].
+kv_shape window_shape(const kv_shape *s, int C) {
+  kv_shape w = *s;
+  w.num_phys_pages = (int64_t)s->batch * C;
+  w.kv_loc = KV_LOC_HBM;
+  return w;
+}
+size_t window_lists_bytes(const kv_shape *s, int C) {
+  const size_t groups = (size_t)s->batch * s->num_kv_heads;
+  return 2 * align256(groups * (size_t)C * 4) + align256(groups * 4);
+}
+
 int attn_common(const kv_shape *s, const void *q, const void *k_cache, const void *v_cache,
                 const int32_t *bt, const int32_t *ctx, const int32_t *indices, int32_t k,
-                float scale, float *out, void *ws, size_t ws_bytes, void *stream) {
+                float scale, float *out, void *ws, size_t ws_bytes, void *stream,
+                const WindowCall *wc = nullptr) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!al16(q) || !al16(out) || !al4(bt) || !al4(ctx)) return KV_ERR_INVALID_ARG;
@@ -368,12 +390,37 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   const void *kd = nullptr, *vd = nullptr;
   if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
   if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
-  const Plan pl = cached_plan(s, indices ? k : 0);
-  if (pl.total > 0 && (ws == nullptr || ws_bytes < pl.total || !al16(ws))) return KV_ERR_WORKSPACE;
+  const kv_shape *as = wc ? &wc->wshape : s;  // the shape the attention reads
+  const Plan pl = cached_plan(as, indices ? k : 0);
+  const int C = wc ? wc->win->cache_pages : 0;
+  const size_t need_ws = pl.total + (wc ? window_lists_bytes(s, C) : 0);
+  if (need_ws > 0 && (ws == nullptr || ws_bytes < need_ws || !al16(ws))) return KV_ERR_WORKSPACE;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);
+  if (wc) {
+    // the window step: update the state, then copy the fetch list into the
+    // window; the attention below reads the window only
+    const size_t groups = (size_t)s->batch * s->num_kv_heads;
+    int32_t *fpage = reinterpret_cast<int32_t *>(w + pl.total);
+    int32_t *fslot = reinterpret_cast<int32_t *>(w + pl.total + align256(groups * C * 4));
+    int32_t *fcount = reinterpret_cast<int32_t *>(w + pl.total + 2 * align256(groups * C * 4));
+    const kv_window *win = wc->win;
+    cudaError_t e = launch_window_update(indices, wc->scores, ctx, s->batch, s->num_q_heads,
+                                         s->num_kv_heads, s->page_size, s->max_pages_per_seq, k,
+                                         C, win->slot_page, win->page_slot, fpage, fslot, fcount,
+                                         win->stats, status, st);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+    const int bpg = (int)std::max<long long>(
+        1, std::min<long long>(C, (long long)sm_count(dev) * 8 / (long long)groups));
+    e = launch_window_fetch(s->dtype, kd, vd, win->cache_k, win->cache_v, bt, ctx, fpage, fslot,
+                            fcount, s->batch, s->num_kv_heads, s->page_size,
+                            s->max_pages_per_seq, C, s->num_phys_pages, bpg, status, st);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+    kd = win->cache_k;
+    vd = win->cache_v;
+  }
 
   AttnArgs a{};
   a.q = q;
@@ -383,7 +430,11 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   a.context_lens = ctx;
   a.out = out;
   a.status = status;
-  a.nphys = s->num_phys_pages;
+  a.nphys = as->num_phys_pages;
+  if (wc) {
+    a.page_slot = wc->win->page_slot;
+    a.cache_C = C;
+  }
   a.B = s->batch;
   a.Hq = s->num_q_heads;
   a.Hkv = s->num_kv_heads;
@@ -417,10 +468,10 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   CUtensorMap tk, tv;
   memset(&tk, 0, sizeof tk);
   memset(&tv, 0, sizeof tv);
-  a.use_tma = s->kv_loc == KV_LOC_HBM ? 1 : 0;
+  a.use_tma = as->kv_loc == KV_LOC_HBM ? 1 : 0;
   if (a.use_tma) {
-    if ((rc = make_kv_map(s, kd, &tk)) != KV_OK) return rc;
-    if ((rc = make_kv_map(s, vd, &tv)) != KV_OK) return rc;
+    if ((rc = make_kv_map(as, kd, &tk)) != KV_OK) return rc;
+    if ((rc = make_kv_map(as, vd, &tv)) != KV_OK) return rc;
   }
   dim3 grid(pl.S, pl.groups, s->batch);
   cudaError_t e = pl.mma ? launch_attn_mma(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st)
@@ -604,6 +655,61 @@ int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cac
                          size_t workspace_bytes, void *stream) {
   return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, nullptr, 0, scale,
                      out, workspace, workspace_bytes, stream);
+}
+
+size_t kv_window_workspace_bytes(const kv_shape *shape, int32_t k, int32_t cache_pages) {
+  if (check_shape(shape) != KV_OK || k < 1 || cache_pages < 1) return 0;
+  const kv_shape w = window_shape(shape, cache_pages);
+  return cached_plan(&w, k).total + window_lists_bytes(shape, cache_pages);
+}
+
+static int check_window(const kv_shape *s, const kv_window *win, int32_t k) {
+  if (!win || win->cache_pages < 1) return KV_ERR_INVALID_ARG;
+  const long long C = win->cache_pages;
+  const long long G = s->num_q_heads / s->num_kv_heads;
+  if (C < std::min<long long>(G * k, s->max_pages_per_seq)) return KV_ERR_INVALID_ARG;
+  if (window_update_smem(s->max_pages_per_seq, (int)C) > 200 * 1024) return KV_ERR_UNSUPPORTED;
+  if ((long long)s->batch * C * s->num_kv_heads * s->page_size > INT_MAX) return KV_ERR_UNSUPPORTED;
+  if (!al16(win->cache_k) || !al16(win->cache_v) || !al4(win->slot_page) ||
+      !al4(win->page_slot) || (win->stats && !al4(win->stats)))
+    return KV_ERR_INVALID_ARG;
+  return KV_OK;
+}
+
+int kv_window_reset(const kv_shape *shape, const kv_window *win, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!win || win->cache_pages < 1 || !al4(win->slot_page) || !al4(win->page_slot))
+    return KV_ERR_INVALID_ARG;
+  const long long groups = (long long)shape->batch * shape->num_kv_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_fill(win->slot_page, groups * win->cache_pages, -1, st) != cudaSuccess ||
+      launch_fill(win->page_slot, groups * shape->max_pages_per_seq, -1, st) != cudaSuccess)
+    return KV_ERR_CUDA;
+  return KV_OK;
+}
+
+int kv_sparse_decode_attn_window(const kv_shape *shape, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_table,
+                                 const int32_t *context_lens, const int32_t *indices, int32_t k,
+                                 const float *scores, float scale, float *out,
+                                 const kv_window *win, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!indices || k < 1 || !al16(scores)) return KV_ERR_INVALID_ARG;
+  if ((rc = check_window(shape, win, k)) != KV_OK) return rc;
+  cudaPointerAttributes at;
+  for (const void *p : {win->cache_k, win->cache_v}) {
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return KV_ERR_CUDA;
+    }
+    if (at.type != cudaMemoryTypeDevice) return KV_ERR_LOCATION;
+  }
+  WindowCall wc{win, scores, window_shape(shape, win->cache_pages)};
+  return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, indices, k, scale, out,
+                     workspace, workspace_bytes, stream, &wc);
 }
 
 int kv_device_status(void *stream) {

@@ -178,7 +178,13 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     }
     PageEnt ent{-1, 0};
     if (p >= 0 && p < P) {
-      const long long ph = a.block_table[(long long)b * a.maxP + p];
+      long long ph;
+      if (a.page_slot) {  // the page's slot in the window (page b*C + slot)
+        const int sl = a.page_slot[((long long)b * a.Hkv + kvh) * a.maxP + p];
+        ph = (sl >= 0 && sl < a.cache_C) ? (long long)b * a.cache_C + sl : -1;
+      } else {
+        ph = a.block_table[(long long)b * a.maxP + p];
+      }
       if (ph >= 0 && ph < a.nphys) {
         ent.phys = (int)ph;
         ent.info = min(ps, len - p * ps) | (int)(mask << 8);

@@ -215,6 +215,8 @@ struct AttnArgs {
   const int32_t *union_pages;   // sparse: [B][groups][umax], else null
   const uint32_t *union_masks;  // sparse: [B][groups][umax]
   const int32_t *union_count;   // sparse: [B][groups]
+  const int32_t *page_slot;     // window: [B][Hkv][maxP] slot of a page, else null
+  int cache_C;                  // window: slots per (b, kv head); K/V are the window
   float *out;                   // [B][Hq][d]      (num_splits == 1)
   float *part_o;                // [S][B][Hq][d]   (num_splits > 1)
   float *part_ml;               // [S][B][Hq][2]   (log2-domain max, sum)
@@ -258,6 +260,19 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void 
                           void *v_cache, const int32_t *bt, const int32_t *ctx,
                           int32_t *ctx_out, void *minmax, int B, int Hkv, int ps, int maxP,
                           long long nphys, int *status, cudaStream_t st);
+size_t window_update_smem(int maxP, int C);
+cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
+                                 int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
+                                 int32_t *slot_page, int32_t *page_slot, int32_t *fetch_page,
+                                 int32_t *fetch_slot, int32_t *fetch_count, int32_t *stats,
+                                 int *status, cudaStream_t st);
+cudaError_t launch_window_fetch(int dtype, const void *k_src, const void *v_src, void *k_win,
+                                void *v_win, const int32_t *bt, const int32_t *ctx,
+                                const int32_t *fetch_page, const int32_t *fetch_slot,
+                                const int32_t *fetch_count, int B, int Hkv, int ps, int maxP,
+                                int C, long long nphys, int blocks_per_group, int *status,
+                                cudaStream_t st);
+cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
 cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
                               const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
                               int Hkv, int ps, int maxP, long long nphys, int *status,

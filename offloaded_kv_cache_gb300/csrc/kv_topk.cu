@@ -5,13 +5,12 @@
 // LLM Inference, section 2.2: for each query only the Top-K most important
 // blocks are retrieved.  Ties go to the lower page index; pages come out
 // ascending.
-#include "kv_internal.cuh"
+#include "kv_select.cuh"
 
 namespace kvs {
 namespace {
 
 constexpr int kTopkThreads = 256;
-constexpr int kTopkWarps = kTopkThreads / 32;
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   // +0.0f folds -0.0 into +0.0 so that equal scores compare equal
@@ -22,35 +21,9 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 // 0xFFFFFFFF is a NaN's key, and scores are never NaN).
 constexpr uint32_t kForcedKey = 0xFFFFFFFFu;
 
-// Exclusive prefix sum over the warps of the block of one 64-bit value per
-// warp (lane 0's argument counts); returns the warp's base, *total the sum.
-// Two block barriers; `wsum` holds one slot per warp.
-template <int WARPS>
-__device__ __forceinline__ unsigned long long warp_bases64(unsigned long long v,
-                                                           unsigned long long *wsum,
-                                                           unsigned long long *total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) wsum[warp] = v;
-  __syncthreads();
-  unsigned long long base = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < WARPS; ++w) {
-    const unsigned long long t = wsum[w];
-    base += w < warp ? t : 0ull;
-    tot += t;
-  }
-  __syncthreads();
-  *total = tot;
-  return base;
-}
-
-// One CTA per (b, h) row.  Radix select of the K-th largest key, 8 bits per
-// pass from the top (a shared-memory histogram whose threshold digit one warp
-// finds with a shuffle scan), stopping early once every key of the threshold
-// bin is taken.  The output pass splits the pages into one contiguous segment
-// per warp; each warp walks its segment 32 pages at a time and places the
-// selected pages in index order with ballots, after one block scan of the
-// per-warp counts.  Equal keys at the threshold go to the lower page index.
+// One CTA per (b, h) row: a radix select of the K largest keys (8 bits per
+// pass, early exit) and an in-order ballot compaction of the selected pages
+// (kv_select.cuh).  Equal keys at the threshold go to the lower page index.
 // Forced pages (the pages holding the first sink_tokens tokens and the last
 // local_tokens tokens of the row) take a key above every score's, so they are
 // selected first, lower index first among themselves.
@@ -60,11 +33,8 @@ __global__ void __launch_bounds__(kTopkThreads)
                 int32_t *__restrict__ out, int *status) {
   pdl_wait();
   extern __shared__ uint32_t skeys[];
-  __shared__ uint32_t hist[256];
-  __shared__ unsigned long long wsum[kTopkWarps];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_krem, s_all;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ RadixScratch sc;
+  const int tid = threadIdx.x;
   const long long row = blockIdx.x;
   const int b = (int)(row / Hq);
   int32_t *orow = out + row * K;
@@ -92,89 +62,11 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   auto key_at = [&](int p) -> uint32_t { return keys_in_smem ? skeys[p] : raw_key(p); };
 
-  uint32_t prefix = 0, pmask = 0;
-  int krem = keff;  // keys matching `prefix` that still have to be taken
-  bool all_taken = false;
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;  // kTopkThreads == 256 bins
-    __syncthreads();
-    for (int p = tid; p < P; p += kTopkThreads) {
-      const uint32_t k = key_at(p);
-      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid < 32) {
-      // lane l owns digits 255-8l .. 248-8l, scanned from the top
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = (int)hist[255 - 8 * tid - j];
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (tid >= off) incl += t;
-      }
-      int above = incl - sum;
-      if (above < krem && krem <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above + c[j] >= krem) {
-            s_digit = (uint32_t)(255 - 8 * tid - j);
-            s_krem = krem - above;
-            s_all = (above + c[j] == krem) ? 1 : 0;
-            break;
-          }
-          above += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    pmask |= 255u << shift;
-    krem = s_krem;
-    if (s_all) {
-      all_taken = true;  // every key with this prefix is selected
-      break;
-    }
-  }
+  const RadixSel sel = radix_select_top<kTopkThreads>(key_at, P, keff, sc);
   pdl_trigger();
-  // selected: keys whose masked value beats the prefix, plus those equal to
-  // it -- all of them when all_taken, else the first krem in page order
-  const int seg = ((P + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;  // pages per warp
-  const int lo = warp * seg, hi = min(P, lo + seg);
-  uint32_t gt_n = 0, eq_n = 0;
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
-    gt_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k > prefix));
-    eq_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k == prefix));
-  }
-  unsigned long long tot;
-  const unsigned long long base =
-      warp_bases64<kTopkWarps>(((unsigned long long)eq_n << 32) | gt_n, wsum, &tot);
-  long long gt_b = (long long)(base & 0xFFFFFFFFull);
-  long long eq_b = (long long)(base >> 32);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
-    const unsigned gtb = __ballot_sync(0xFFFFFFFFu, p < hi && k > prefix);
-    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, p < hi && k == prefix);
-    const long long my_gt = gt_b + __popc(gtb & lt_mask);
-    const long long my_eq = eq_b + __popc(eqb & lt_mask);
-    const bool is_gt = (gtb >> lane) & 1u, is_eq = (eqb >> lane) & 1u;
-    const bool sel = is_gt || (is_eq && (all_taken || my_eq < krem));
-    if (sel) {
-      const long long pos = my_gt + (all_taken ? my_eq : min(my_eq, (long long)krem));
-      if (pos < K) orow[pos] = p;
-    }
-    gt_b += __popc(gtb);
-    eq_b += __popc(eqb);
-  }
+  radix_emit<kTopkThreads>(key_at, P, sel, sc, [&](long long pos, int p) {
+    if (pos < K) orow[pos] = p;
+  });
   for (int i = keff + tid; i < K; i += kTopkThreads) orow[i] = -1;
 }
 

@@ -38,6 +38,13 @@ class kv_shape(ctypes.Structure):
                 ("kv_loc", ctypes.c_int32)]
 
 
+class kv_window(ctypes.Structure):
+    _fields_ = [("cache_pages", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cache_k", ctypes.c_void_p), ("cache_v", ctypes.c_void_p),
+                ("slot_page", ctypes.c_void_p), ("page_slot", ctypes.c_void_p),
+                ("stats", ctypes.c_void_p)]
+
+
 class KvError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {status_string(code)} ({code})")
@@ -73,6 +80,10 @@ def load(path: str = LIB_PATH):
         "kv_attn_num_splits": (i32, [S, i32]),
         "kv_sparse_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, P, i32, f32, P, P, sz, P]),
         "kv_dense_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, f32, P, P, sz, P]),
+        "kv_window_workspace_bytes": (sz, [S, i32, i32]),
+        "kv_window_reset": (ctypes.c_int, [S, ctypes.POINTER(kv_window), P]),
+        "kv_sparse_decode_attn_window": (ctypes.c_int, [S, P, P, P, P, P, P, i32, P, f32, P,
+                                                        ctypes.POINTER(kv_window), P, sz, P]),
         "kv_device_status": (ctypes.c_int, [P]),
         "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv_debug_config": (ctypes.c_int, [i32, ctypes.c_uint64]),
@@ -100,6 +111,31 @@ def _stream(s):
     if isinstance(s, int):
         return s
     return s.cuda_stream
+
+
+def make_window(cache_pages, cache_k, cache_v, slot_page, page_slot, stats=None) -> kv_window:
+    return kv_window(int(cache_pages), 0, _ptr(cache_k), _ptr(cache_v), _ptr(slot_page),
+                     _ptr(page_slot), _ptr(stats))
+
+
+def kv_window_workspace_bytes(shape, k, cache_pages) -> int:
+    return int(load().kv_window_workspace_bytes(ctypes.byref(shape), int(k), int(cache_pages)))
+
+
+def kv_window_reset(shape, win, stream=None, check=True):
+    rc = load().kv_window_reset(ctypes.byref(shape), ctypes.byref(win), _stream(stream))
+    return _ret(rc, "kv_window_reset", check)
+
+
+def kv_sparse_decode_attn_window(shape, q, k_cache, v_cache, block_table, context_lens, indices,
+                                 k, scores, scale, out, win, workspace, workspace_bytes,
+                                 stream=None, check=True):
+    rc = load().kv_sparse_decode_attn_window(
+        ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(context_lens), _ptr(indices), int(k), _ptr(scores), float(scale), _ptr(out),
+        None if win is None else ctypes.byref(win), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+    return _ret(rc, "kv_sparse_decode_attn_window", check)
 
 
 def make_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,

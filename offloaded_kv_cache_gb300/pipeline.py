@@ -8,6 +8,7 @@ binding:
     build_mean_index(), score_mean() -> kv_page_mean_build, kv_page_score_mean
     append()       -> kv_append_token
     sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
+    enable_window(C), window_attn() -> kv_window_reset, kv_sparse_decode_attn_window
     dense_step()   -> kv_dense_decode_attn
 
 PyTorch is used for allocation, host<->device copies and streams only; every
@@ -90,6 +91,43 @@ class DecodeLayer:
         self.ws_topk_bytes = kv.kv_topk_workspace_bytes(self.shape, k)
         nbytes = max(self.ws_dense_bytes, self.ws_sparse_bytes, self.ws_topk_bytes, 16)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    # --- the GPU-resident page window -----------------------------------------
+    def enable_window(self, cache_pages: int, stream=None):
+        """Allocate and empty a window of cache_pages slots per (sequence, kv head)."""
+        spec = self.spec
+        C = int(cache_pages)
+        tdt = TORCH_DTYPE[spec.dtype]
+        shp = (spec.batch * C, spec.num_kv_heads, spec.page_size, spec.head_dim)
+        self.win_k = torch.zeros(shp, dtype=tdt, device=self.device)
+        self.win_v = torch.zeros(shp, dtype=tdt, device=self.device)
+        self.win_slot_page = torch.empty((spec.batch, spec.num_kv_heads, C), dtype=torch.int32,
+                                         device=self.device)
+        self.win_page_slot = torch.empty((spec.batch, spec.num_kv_heads, spec.max_pages),
+                                         dtype=torch.int32, device=self.device)
+        self.win_stats = torch.zeros((spec.batch, spec.num_kv_heads, 4), dtype=torch.int32,
+                                     device=self.device)
+        self.window = kv.make_window(C, self.win_k, self.win_v, self.win_slot_page,
+                                     self.win_page_slot, self.win_stats)
+        nbytes = kv.kv_window_workspace_bytes(self.shape, max(1, self.topk), C)
+        if nbytes > self.workspace.numel():
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        kv.kv_window_reset(self.shape, self.window, self._st(stream))
+
+    def window_attn(self, indices=None, scores=None, stream=None):
+        stream = self._st(stream)
+        idx = self.indices if indices is None else indices
+        sc = self.scores if scores is None else scores
+        kv.kv_sparse_decode_attn_window(self.shape, self.q, self.k_cache, self.v_cache,
+                                        self.block_table, self.context_lens, idx, idx.shape[-1],
+                                        sc, self.scale, self.out, self.window, self.workspace,
+                                        self.workspace.numel(), stream)
+
+    def window_step(self, stream=None):
+        stream = self._st(stream)
+        self.score(stream)
+        self.select(stream)
+        self.window_attn(stream=stream)
 
     def use_copy(self, i: int):
         self.k_cache = self.k_copies[i % len(self.k_copies)]

@@ -286,6 +286,21 @@ def new_tokens(spec: WorkloadSpec, step: int = 0):
     return k, v
 
 
+def drifting_queries(spec: WorkloadSpec, q0: np.ndarray, steps: int, sigma: float):
+    """Queries of `steps` consecutive decode steps starting at q0 ([B][Hq][d]
+    storage values): each step adds N(0, (sigma * value_scale)^2) noise to the
+    previous step's fp32 values and rounds once, so consecutive steps select
+    overlapping pages (the temporal locality a page window exploits)."""
+    root = np.random.SeedSequence([spec.seed, 0xD41F7, steps])
+    g = np.random.Generator(np.random.PCG64(root))
+    x = storage_to_f64(q0, spec.dtype).astype(np.float32)
+    out = []
+    for _ in range(steps):
+        x = x + np.float32(sigma * spec.value_scale) * g.standard_normal(x.shape, dtype=np.float32)
+        out.append(to_storage(x, spec.dtype))
+    return out
+
+
 def tiny_spec(dtype="bf16", batch=2, hq=4, hkv=2, d=128, context=100, ps=16, topk=3,
               scale=1.0, plant="none", index=100, **kw) -> WorkloadSpec:
     """A small workload for parity tests (several pages, ragged last page)."""
