@@ -49,16 +49,16 @@ struct RadixScratch {
 // The k (1 <= k <= n) largest of key_at(0 .. n-1), 8 bits per pass from the
 // top: a shared-memory histogram whose threshold digit one warp finds with a
 // shuffle scan; stops early once every key of the threshold bin is taken.
-// THREADS must be 256 (one histogram bin per thread).
+// THREADS: 256, 512 or 1024 (the block size).
 template <int THREADS, class KeyAt>
 __device__ __forceinline__ RadixSel radix_select_top(KeyAt key_at, int n, int k,
                                                      RadixScratch &sc) {
-  static_assert(THREADS == 256, "one histogram bin per thread");
+  static_assert(THREADS % 256 == 0 && THREADS <= 1024, "256, 512 or 1024 threads");
   const int tid = threadIdx.x;
   RadixSel r{0u, 0u, k, false};
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
-    sc.hist[tid] = 0;
+    if (tid < 256) sc.hist[tid] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += THREADS) {
       const uint32_t key = key_at(i);

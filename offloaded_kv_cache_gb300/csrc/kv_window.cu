@@ -23,7 +23,8 @@
 namespace kvs {
 namespace {
 
-constexpr int kWinThreads = 256;
+// one CTA per group and few groups: a wide CTA shortens every pass
+constexpr int kWinThreads = 1024;
 constexpr int kWinWarps = kWinThreads / 32;
 
 __device__ __forceinline__ uint32_t win_score_key(float s) {
