@@ -575,25 +575,22 @@ def main():
     h2d = q_host.numel() * q_host.element_size() + ctx_host.numel() * 4
     d2h = out_host.numel() * 4
 
-    step = layer.sparse_step if sparse else layer.dense_step
-
-    def e2e_step():
-        layer.q.copy_(q_host, non_blocking=True)
-        layer.context_lens.copy_(ctx_host, non_blocking=True)
-        step()
-        out_host.copy_(layer.out, non_blocking=True)
+    # one kv_decode_step call per step: q and the lengths copied in from the
+    # pinned host buffers, the path, the output copied back
+    ios = []
+    for c in range(copies):
+        layer.use_copy(c)
+        ios.append(layer.host_io(q_host, ctx_host, out_host, sparse))
 
     for i in range(args.warmup):
-        layer.use_copy(i)
-        e2e_step()
+        layer.host_step(ios[i % copies])
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        layer.use_copy(i)
-        e2e_step()
+        layer.host_step(ios[i % copies])
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1) / args.steps

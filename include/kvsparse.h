@@ -257,6 +257,37 @@ int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q, const voi
 int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
                          int32_t sink_words, void *stream);
 
+/* One decode step of one layer on host buffers: q and context_lens come from
+ * host memory, the path runs (k > 0: kv_page_score, kv_topk_select,
+ * kv_sparse_decode_attn; k == 0: kv_dense_decode_attn) and out lands in host
+ * memory, all asynchronous on `stream`.  A host buffer the device has mapped
+ * (cudaHostAlloc, or pinned and registered) is used in place: the kernels
+ * read q and the lengths and write out across the host link, the zero-copy
+ * access DirectKV applies to K/V (core method 1).  Any other host buffer is
+ * copied through the matching device buffer with cudaMemcpyAsync (q,
+ * context_lens, out may then be NULL only for mapped buffers).  The same
+ * outputs as the separate calls.  The index (minmax) must be built. */
+typedef struct {
+  const void *q_host;               /* [B][Hq][d] dtype, host                  */
+  const int32_t *context_lens_host; /* [B], host                               */
+  float *out_host;                  /* [B][Hq][d], host                        */
+  void *q;                          /* device copies of the three              */
+  int32_t *context_lens;
+  float *out;
+  const void *k_cache;              /* where kv_loc says                       */
+  const void *v_cache;
+  const int32_t *block_table;       /* device                                  */
+  const void *minmax;               /* device; sparse steps only               */
+  float *scores;                    /* device [B][Hq][maxP]; sparse only       */
+  int32_t *indices;                 /* device [B][Hq][k]; sparse only          */
+  int32_t k;                        /* 0: dense step; else pages per head      */
+  float scale;
+  void *workspace;                  /* >= kv_attn_workspace_bytes(shape, k)   */
+  size_t workspace_bytes;
+} kv_step_io;
+
+int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream);
+
 /* GPU-resident window of critical pages (KVDrive, section 5.1 "Sliding
  * window with lookahead eviction"; section 3, Finding 1: a window of several
  * steps' critical entries cuts host-to-GPU transfer; section 6.3: with most

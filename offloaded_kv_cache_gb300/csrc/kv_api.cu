@@ -371,6 +371,45 @@ size_t window_lists_bytes(const kv_shape *s, int C) {
   return 2 * align256(groups * (size_t)C * 4) + align256(groups * 4);
 }
 
+// Encoded tensor maps depend only on (device, base address, rows, dtype);
+// encoding two per call cost measurable host time, so keep the last few.
+struct MapEntry {
+  int dev, dtype;
+  const void *base;
+  long long rows;
+  CUtensorMap map;
+};
+std::mutex g_map_mutex;
+MapEntry g_maps[16];
+int g_map_n = 0;
+
+int kv_map_cached(const kv_shape *s, const void *base, CUtensorMap *map) {
+  const int dev = current_device();
+  const long long rows = s->num_phys_pages * (long long)s->num_kv_heads * s->page_size;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < std::min(g_map_n, 16); ++i) {
+      const MapEntry &e = g_maps[i];
+      if (e.dev == dev && e.base == base && e.rows == rows && e.dtype == s->dtype) {
+        *map = e.map;
+        return KV_OK;
+      }
+    }
+  }
+  const int rc = make_kv_map(s, base, map);
+  if (rc == KV_OK && dev >= 0) {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    MapEntry &e = g_maps[g_map_n % 16];
+    e.dev = dev;
+    e.dtype = s->dtype;
+    e.base = base;
+    e.rows = rows;
+    e.map = *map;
+    ++g_map_n;
+  }
+  return rc;
+}
+
 int attn_common(const kv_shape *s, const void *q, const void *k_cache, const void *v_cache,
                 const int32_t *bt, const int32_t *ctx, const int32_t *indices, int32_t k,
                 float scale, float *out, void *ws, size_t ws_bytes, void *stream,
@@ -470,8 +509,8 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   memset(&tv, 0, sizeof tv);
   a.use_tma = as->kv_loc == KV_LOC_HBM ? 1 : 0;
   if (a.use_tma) {
-    if ((rc = make_kv_map(as, kd, &tk)) != KV_OK) return rc;
-    if ((rc = make_kv_map(as, vd, &tv)) != KV_OK) return rc;
+    if ((rc = kv_map_cached(as, kd, &tk)) != KV_OK) return rc;
+    if ((rc = kv_map_cached(as, vd, &tv)) != KV_OK) return rc;
   }
   dim3 grid(pl.S, pl.groups, s->batch);
   cudaError_t e = pl.mma ? launch_attn_mma(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st)
@@ -655,6 +694,77 @@ int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cac
                          size_t workspace_bytes, void *stream) {
   return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, nullptr, 0, scale,
                      out, workspace, workspace_bytes, stream);
+}
+
+// Device-visible address of host memory the device has mapped (pinned), or
+// nullptr when it is not mapped.
+static void *mapped_host(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!io || !io->q_host || !io->context_lens_host || !io->out_host || io->k < 0)
+    return KV_ERR_INVALID_ARG;
+  if (io->k > 0 && (!io->minmax || !io->scores || !io->indices)) return KV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)shape->batch * shape->num_q_heads;
+  // Host buffers the device has mapped are used in place (zero-copy: the
+  // kernels read q and the lengths and write out across the host link, as
+  // the pages read K/V); others are copied through the device buffers.
+  const void *q = mapped_host(io->q_host);
+  const int32_t *ctx = static_cast<const int32_t *>(mapped_host(io->context_lens_host));
+  float *out = static_cast<float *>(mapped_host(io->out_host));
+  if (!q) {
+    if (!al16(io->q)) return KV_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(io->q, io->q_host, rows * kHeadDim * elem_bytes(shape->dtype),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KV_ERR_CUDA;
+    }
+    q = io->q;
+  }
+  if (!ctx) {
+    if (!al4(io->context_lens)) return KV_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(io->context_lens, io->context_lens_host, (size_t)shape->batch * 4,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KV_ERR_CUDA;
+    }
+    ctx = io->context_lens;
+  }
+  const bool copy_out = out == nullptr;
+  if (copy_out) {
+    if (!al16(io->out)) return KV_ERR_INVALID_ARG;
+    out = io->out;
+  }
+  if (io->k > 0) {
+    if ((rc = kv_page_score(shape, q, io->minmax, io->block_table, ctx, io->scores, stream)) !=
+        KV_OK)
+      return rc;
+    if ((rc = kv_topk_select(shape, io->scores, ctx, io->k, io->indices, nullptr, 0, stream)) !=
+        KV_OK)
+      return rc;
+    rc = kv_sparse_decode_attn(shape, q, io->k_cache, io->v_cache, io->block_table, ctx,
+                               io->indices, io->k, io->scale, out, io->workspace,
+                               io->workspace_bytes, stream);
+  } else {
+    rc = kv_dense_decode_attn(shape, q, io->k_cache, io->v_cache, io->block_table, ctx,
+                              io->scale, out, io->workspace, io->workspace_bytes, stream);
+  }
+  if (rc != KV_OK) return rc;
+  if (copy_out && cudaMemcpyAsync(io->out_host, io->out, rows * kHeadDim * 4,
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
 }
 
 size_t kv_window_workspace_bytes(const kv_shape *shape, int32_t k, int32_t cache_pages) {

@@ -45,6 +45,17 @@ class kv_window(ctypes.Structure):
                 ("stats", ctypes.c_void_p)]
 
 
+class kv_step_io(ctypes.Structure):
+    _fields_ = [("q_host", ctypes.c_void_p), ("context_lens_host", ctypes.c_void_p),
+                ("out_host", ctypes.c_void_p), ("q", ctypes.c_void_p),
+                ("context_lens", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("minmax", ctypes.c_void_p),
+                ("scores", ctypes.c_void_p), ("indices", ctypes.c_void_p),
+                ("k", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
 class KvError(RuntimeError):
     def __init__(self, code: int, where: str):
         super().__init__(f"{where}: {status_string(code)} ({code})")
@@ -84,6 +95,7 @@ def load(path: str = LIB_PATH):
         "kv_window_reset": (ctypes.c_int, [S, ctypes.POINTER(kv_window), P]),
         "kv_sparse_decode_attn_window": (ctypes.c_int, [S, P, P, P, P, P, P, i32, P, f32, P,
                                                         ctypes.POINTER(kv_window), P, sz, P]),
+        "kv_decode_step": (ctypes.c_int, [S, ctypes.POINTER(kv_step_io), P]),
         "kv_device_status": (ctypes.c_int, [P]),
         "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv_debug_config": (ctypes.c_int, [i32, ctypes.c_uint64]),
@@ -136,6 +148,11 @@ def kv_sparse_decode_attn_window(shape, q, k_cache, v_cache, block_table, contex
         None if win is None else ctypes.byref(win), _ptr(workspace), int(workspace_bytes),
         _stream(stream))
     return _ret(rc, "kv_sparse_decode_attn_window", check)
+
+
+def kv_decode_step(shape, io, stream=None, check=True):
+    rc = load().kv_decode_step(ctypes.byref(shape), ctypes.byref(io), _stream(stream))
+    return _ret(rc, "kv_decode_step", check)
 
 
 def make_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,

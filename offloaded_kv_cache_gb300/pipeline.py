@@ -10,6 +10,7 @@ binding:
     sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
     enable_window(C), window_attn() -> kv_window_reset, kv_sparse_decode_attn_window
     dense_step()   -> kv_dense_decode_attn
+    host_step()    -> kv_decode_step (host q / lengths in, out back)
 
 PyTorch is used for allocation, host<->device copies and streams only; every
 step of the computation runs in libkvsparse's kernels.
@@ -204,6 +205,21 @@ class DecodeLayer:
         kv.kv_dense_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
                                 self.context_lens, self.scale, self.out, self.workspace,
                                 self.workspace.numel(), stream)
+
+    def host_io(self, q_host: torch.Tensor, ctx_host: torch.Tensor, out_host: torch.Tensor,
+                sparse: bool):
+        """The kv_step_io of one decode step on these host buffers."""
+        k = self.topk if sparse else 0
+        return kv.kv_step_io(
+            q_host.data_ptr(), ctx_host.data_ptr(), out_host.data_ptr(), self.q.data_ptr(),
+            self.context_lens.data_ptr(), self.out.data_ptr(), self.k_cache.data_ptr(),
+            self.v_cache.data_ptr(), self.block_table.data_ptr(),
+            self.minmax.data_ptr() if sparse else None, self.scores.data_ptr() if sparse else None,
+            self.indices.data_ptr() if sparse else None, k, self.scale,
+            self.workspace.data_ptr(), self.workspace.numel())
+
+    def host_step(self, io, stream=None):
+        kv.kv_decode_step(self.shape, io, self._st(stream))
 
     # --- host views --------------------------------------------------------
     def minmax_bits(self) -> np.ndarray:

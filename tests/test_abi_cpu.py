@@ -114,6 +114,8 @@ def test_null_and_misaligned_pointers_rejected(kvlib):
     assert kv.kv_sparse_decode_attn(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0.1, FAKE, FAKE,
                                     64, check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_debug_config(-1, 0, check=False) == kv.KV_ERR_INVALID_ARG
+    io = kv.kv_step_io()
+    assert kv.kv_decode_step(s, io, check=False) == kv.KV_ERR_INVALID_ARG
 
 
 def test_workspace_sizes_follow_the_plan(kvlib):

@@ -1,0 +1,82 @@
+"""kv_decode_step (one decode step on host buffers) against the separate calls
+and the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from offloaded_kv_cache_gb300 import kvsparse as kv
+from offloaded_kv_cache_gb300 import workloads as W
+from offloaded_kv_cache_gb300.pipeline import DecodeLayer, storage_to_torch
+from parity_util import ATOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(kvlib):
+    kv.kv_debug_config(-1, 2_000_000_000)
+    kv.kv_device_status()
+    yield
+
+
+@pytest.mark.parametrize("dtype,sparse,kv_loc,pinned", [
+    ("bf16", True, "hbm", True), ("f16", False, "hbm", True), ("bf16", True, "host", True),
+    ("f32", False, "host", True),
+    ("bf16", True, "hbm", False), ("f16", False, "hbm", False),   # pageable: copied
+])
+def test_host_step_equals_separate_calls_and_oracle(dtype, sparse, kv_loc, pinned):
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=8, hkv=2, context=16 * 20 + 5, ps=16, topk=4,
+                       index=130)
+    wl = W.generate(spec, context_lens=[16 * 20 + 5, 16 * 7, 9])
+    layer = DecodeLayer(wl, kv_loc=kv_loc, topk=4)
+    layer.build_index()
+    # a new step's query and lengths arrive in host memory
+    q2 = W.drifting_queries(spec, wl.q, 1, 0.5)[0]
+    ctx2 = np.array([16 * 20 + 5, 16 * 7 - 1, 9], dtype=np.int32)
+    q_host = storage_to_torch(q2, dtype).clone()
+    ctx_host = torch.from_numpy(ctx2).clone()
+    out_host = torch.full(layer.out.shape, np.nan, dtype=torch.float32)
+    if pinned:      # mapped: the kernels use the host buffers in place
+        q_host, ctx_host, out_host = q_host.pin_memory(), ctx_host.pin_memory(), out_host.pin_memory()
+    q_before = layer.q.cpu().clone()
+    layer.host_step(layer.host_io(q_host, ctx_host, out_host, sparse))
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    got = out_host.numpy().copy()
+    # in place: the device buffers were not used; copied: they hold the inputs
+    assert torch.equal(layer.q.cpu(), q_before if pinned else q_host)
+    # the separate calls on the same inputs give the same bits
+    layer.q.copy_(q_host)
+    layer.context_lens.copy_(ctx_host)
+    if sparse:
+        layer.sparse_step()
+    else:
+        layer.dense_step()
+    torch.cuda.synchronize()
+    assert np.array_equal(layer.out.cpu().numpy(), got)
+    # and the oracle agrees (sparse: on the oracle's own selection)
+    if sparse:
+        mn, mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
+        s = oracle.scores(dtype, q2, mn, mx, wl.block_table, ctx2, 16)
+        idx = oracle.topk(s, ctx2, 16, 4)
+        layer.sparse_attn(indices=torch.from_numpy(idx).cuda())
+        torch.cuda.synchronize()
+        ref = oracle.attention(dtype, q2, wl.k_cache, wl.v_cache, wl.block_table, ctx2, wl.scale,
+                               indices=idx)
+        assert np.abs(layer.out.cpu().numpy() - ref).max() <= ATOL[dtype]
+    else:
+        ref = oracle.attention(dtype, q2, wl.k_cache, wl.v_cache, wl.block_table, ctx2, wl.scale)
+        assert np.abs(got - ref).max() <= ATOL[dtype]
+
+
+def test_host_step_rejects_missing_sparse_buffers():
+    spec = W.tiny_spec(dtype="bf16", batch=1, hq=4, hkv=1, context=64, ps=16, index=131)
+    wl = W.generate(spec)
+    layer = DecodeLayer(wl, topk=2)
+    q_host = layer.q.cpu().pin_memory()
+    ctx_host = layer.context_lens.cpu().pin_memory()
+    out_host = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    io = layer.host_io(q_host, ctx_host, out_host, True)
+    io.scores = None
+    assert kv.kv_decode_step(layer.shape, io, check=False) == kv.KV_ERR_INVALID_ARG
