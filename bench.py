@@ -40,8 +40,8 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
 NCU_TRAFFIC = {
-    "opt6.7b-b32-ctx544": {"bytes": 289.141248e6, "src": "b0cbb0e7e54c7984"},
-    "llama3.1-8b-b4-ctx32k": {"bytes": 192.472064e6, "src": "b0cbb0e7e54c7984"},
+    "opt6.7b-b32-ctx544": {"bytes": 289.548032e6, "src": "b64eee89734597a4"},
+    "llama3.1-8b-b4-ctx32k": {"bytes": 192.65408e6, "src": "b64eee89734597a4"},
 }
 
 
@@ -390,6 +390,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window-steps", type=int, default=0,
+                    help="profiling aid: run this many eager page-window decode steps "
+                         "(x1 window, drifting queries) on the workload and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -423,6 +426,20 @@ def main():
     layer = DecodeLayer(wl, kv_copies=copies)
     stream = torch.cuda.current_stream()
     sparse = spec.topk > 0
+
+    if args.window_steps > 0:  # profiling aid, no timing
+        layer.build_index()
+        layer.enable_window(spec.group * max(1, spec.topk))
+        for q in W.drifting_queries(spec, wl.q, args.window_steps, 0.5):
+            layer.q = storage_to_torch(q, spec.dtype).cuda()
+            layer.score()
+            layer.select()
+            layer.window_attn()
+        torch.cuda.synchronize()
+        assert kv.kv_device_status() == kv.KV_OK
+        print(json.dumps({"window_steps": args.window_steps,
+                          "last_step_stats": layer.win_stats.sum(dim=(0, 1)).tolist()}))
+        return 0
 
     # index (built once per page; timed separately below)
     layer.build_index()
