@@ -338,17 +338,11 @@ def host_link_gbs(kv, torch, nbytes=512 << 20, reps=10):
 
 # ---------------------------------------------------------------------------
 
-def dist_setup():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
-
-
 def run_reference(args, spec_name):
     from offloaded_kv_cache_gb300 import workloads as W
     import oracle
-    ws, rank, _ = dist_setup()
+    from offloaded_kv_cache_gb300 import replicas as R
+    ws, rank, _ = R.rank_info()
     if rank != 0:
         return 0
     spec = W.WORKLOADS[spec_name]
@@ -400,20 +394,18 @@ def main():
         return run_reference(args, args.workload)
 
     import torch
-    import torch.distributed as dist
     from offloaded_kv_cache_gb300 import build as kbuild
+    from offloaded_kv_cache_gb300 import replicas as R
     from offloaded_kv_cache_gb300 import kvsparse as kv
     from offloaded_kv_cache_gb300 import workloads as W
     from offloaded_kv_cache_gb300.pipeline import DecodeLayer, storage_to_torch
 
-    ws, rank, local = dist_setup()
-    if ws > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ws, rank, local = R.rank_info()
+    R.init(ws, "nccl", torch.device("cuda", local))
     torch.cuda.set_device(local)
     if rank == 0:
         kbuild.build()
-    if ws > 1:
-        dist.barrier()
+    R.barrier(ws)
     kv.load()
 
     spec = W.WORKLOADS[args.workload]
@@ -489,8 +481,7 @@ def main():
         for _ in range(max(1, warm // R)):
             g_r.replay()
         torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
+        R.barrier(ws)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -500,8 +491,7 @@ def main():
             g_1.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        if ws > 1:
-            dist.barrier()
+        R.barrier(ws)
         return e0.elapsed_time(e1)
 
     def timed(fns, k, warm):
@@ -522,14 +512,10 @@ def main():
     total_ms, per_stage = timed(stages, args.steps, args.warmup)
     clocks.mark_off()
     kern_ms = per_stage[dominant]
-    t_local = total_ms
-    if ws > 1:
-        t = torch.tensor([t_local], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_local = float(t.item())
+    t_local = R.max_over_ranks(total_ms, ws, "cuda")
     ms_per_step = t_local / args.steps
-    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
-    qps = ws * spec.batch * spec.num_q_heads / (ms_per_step * 1e-3)
+    value = R.whole_job_rate(step_bytes, ms_per_step * 1e-3, ws) / 1e9
+    qps = R.whole_job_rate(spec.batch * spec.num_q_heads, ms_per_step * 1e-3, ws)
 
     # sustained window for the clock record when the timed region is short
     if rank == 0 and total_ms < 500:
@@ -602,20 +588,15 @@ def main():
     for i in range(args.warmup):
         layer.host_step(ios[i % copies])
     torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
+    R.barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         layer.host_step(ios[i % copies])
     e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        t = torch.tensor([e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e_value = ws * step_bytes / (e_ms * 1e-3) / 1e9
+    e_ms = R.max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, "cuda")
+    e2e_value = R.whole_job_rate(step_bytes, e_ms * 1e-3, ws) / 1e9
     assert kv.kv_device_status() == kv.KV_OK
 
     # decode append (one token per row, min/max updated in place).  The
@@ -695,9 +676,7 @@ def main():
             **extra,
         }
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    R.finish(ws)
     return 0
 
 
