@@ -42,6 +42,10 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 NCU_TRAFFIC = {
     "opt6.7b-b32-ctx544": {"bytes": 289.548032e6, "src": "b64eee89734597a4"},
     "llama3.1-8b-b4-ctx32k": {"bytes": 192.65408e6, "src": "b64eee89734597a4"},
+    # host-resident K/V: DRAM carries only q and the lists; the K/V bytes
+    # arrive over the host link (ctc__rx_bytes_data_user.sum)
+    "llama3.1-8b-b1-ctx128k-host": {"bytes": 183040.0, "link_bytes": 105.875456e6,
+                                    "src": "b64eee89734597a4"},
 }
 
 
@@ -341,8 +345,8 @@ def host_link_gbs(kv, torch, nbytes=512 << 20, reps=10):
 def run_reference(args, spec_name):
     from offloaded_kv_cache_gb300 import workloads as W
     import oracle
-    from offloaded_kv_cache_gb300 import replicas as R
-    ws, rank, _ = R.rank_info()
+    from offloaded_kv_cache_gb300 import replicas
+    ws, rank, _ = replicas.rank_info()
     if rank != 0:
         return 0
     spec = W.WORKLOADS[spec_name]
@@ -395,17 +399,17 @@ def main():
 
     import torch
     from offloaded_kv_cache_gb300 import build as kbuild
-    from offloaded_kv_cache_gb300 import replicas as R
+    from offloaded_kv_cache_gb300 import replicas
     from offloaded_kv_cache_gb300 import kvsparse as kv
     from offloaded_kv_cache_gb300 import workloads as W
     from offloaded_kv_cache_gb300.pipeline import DecodeLayer, storage_to_torch
 
-    ws, rank, local = R.rank_info()
-    R.init(ws, "nccl", torch.device("cuda", local))
+    ws, rank, local = replicas.rank_info()
+    replicas.init(ws, "nccl", torch.device("cuda", local))
     torch.cuda.set_device(local)
     if rank == 0:
         kbuild.build()
-    R.barrier(ws)
+    replicas.barrier(ws)
     kv.load()
 
     spec = W.WORKLOADS[args.workload]
@@ -481,7 +485,7 @@ def main():
         for _ in range(max(1, warm // R)):
             g_r.replay()
         torch.cuda.synchronize()
-        R.barrier(ws)
+        replicas.barrier(ws)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -491,7 +495,7 @@ def main():
             g_1.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        R.barrier(ws)
+        replicas.barrier(ws)
         return e0.elapsed_time(e1)
 
     def timed(fns, k, warm):
@@ -512,10 +516,10 @@ def main():
     total_ms, per_stage = timed(stages, args.steps, args.warmup)
     clocks.mark_off()
     kern_ms = per_stage[dominant]
-    t_local = R.max_over_ranks(total_ms, ws, "cuda")
+    t_local = replicas.max_over_ranks(total_ms, ws, "cuda")
     ms_per_step = t_local / args.steps
-    value = R.whole_job_rate(step_bytes, ms_per_step * 1e-3, ws) / 1e9
-    qps = R.whole_job_rate(spec.batch * spec.num_q_heads, ms_per_step * 1e-3, ws)
+    value = replicas.whole_job_rate(step_bytes, ms_per_step * 1e-3, ws) / 1e9
+    qps = replicas.whole_job_rate(spec.batch * spec.num_q_heads, ms_per_step * 1e-3, ws)
 
     # sustained window for the clock record when the timed region is short
     if rank == 0 and total_ms < 500:
@@ -588,15 +592,15 @@ def main():
     for i in range(args.warmup):
         layer.host_step(ios[i % copies])
     torch.cuda.synchronize()
-    R.barrier(ws)
+    replicas.barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         layer.host_step(ios[i % copies])
     e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = R.max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, "cuda")
-    e2e_value = R.whole_job_rate(step_bytes, e_ms * 1e-3, ws) / 1e9
+    e_ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, "cuda")
+    e2e_value = replicas.whole_job_rate(step_bytes, e_ms * 1e-3, ws) / 1e9
     assert kv.kv_device_status() == kv.KV_OK
 
     # decode append (one token per row, min/max updated in place).  The
@@ -632,8 +636,10 @@ def main():
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
     traffic = None
     rec = NCU_TRAFFIC.get(spec.name)
+    link_traffic = None
     if rec and rec.get("src") == kernel_source_hash():
         traffic = rec["bytes"]
+        link_traffic = rec.get("link_bytes")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -664,6 +670,7 @@ def main():
             "queries_per_s": round(qps, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         **({"link_traffic": link_traffic} if spec.kv_loc == "host" else {}),
                          "kernel": ("kv_sparse_decode_attn (union + attention + combine)" if sparse
                                     else "kv_dense_decode_attn (attention"
                                     + (" + combine)" if splits > 1 else ")")),
@@ -676,7 +683,7 @@ def main():
             **extra,
         }
         print(json.dumps(line), flush=True)
-    R.finish(ws)
+    replicas.finish(ws)
     return 0
 
 
