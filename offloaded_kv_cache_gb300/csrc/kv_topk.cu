@@ -297,6 +297,7 @@ cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, 
   const size_t smem = in_smem ? (size_t)maxP * 4 : 0;
   // long rows with few of them get wider CTAs: the histogram and output
   // passes are latency-bound loops over the row
+  // (1024 threads on 2048-page rows measured slower: 6.68 against 6.48 us)
   constexpr long long kSms = 152;  // GB300
   const long long rows = (long long)B * Hq;
   const int threads = (maxP >= 4096 && rows < 2 * kSms) ? 1024 : 256;

@@ -233,3 +233,34 @@ def test_out_of_range_device_data_is_flagged_not_read():
     layer.select()
     assert kv.kv_device_status() == kv.KV_ERR_BOUNDS
     assert kv.kv_device_status() == kv.KV_OK
+
+
+# ---------------------------------------------------------------- wide block table
+
+@pytest.mark.parametrize("dtype,hq,hkv", [("bf16", 8, 2), ("f16", 4, 4)])
+def test_sparse_attention_with_a_70000_page_block_table(dtype, hq, hkv):
+    # Short contexts in a block table 70000 pages wide: the union's page map
+    # and the top-K rows span the whole width, only the first pages are used.
+    spec = W.tiny_spec(dtype=dtype, batch=2, hq=hq, hkv=hkv, context=16 * 40 + 3, ps=16,
+                       index=140 + hq)
+    wl = W.generate(spec, context_lens=[16 * 40 + 3, 16 * 13])
+    wide = 70000
+    bt = np.full((spec.batch, wide), -1, dtype=np.int32)
+    bt[:, :spec.max_pages] = wl.block_table
+    K = 5
+    mn, mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
+    s = oracle.scores(dtype, wl.q, mn, mx, wl.block_table, wl.context_lens, 16)
+    idx = oracle.topk(s, wl.context_lens, 16, K)
+    shape = kv.make_shape(spec.batch, hq, hkv, 128, 16, wide, spec.num_phys_pages, dtype)
+    layer = DecodeLayer(wl, topk=K)
+    out = torch.empty_like(layer.out)
+    nbytes = kv.kv_attn_workspace_bytes(shape, K)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    kv.kv_sparse_decode_attn(shape, layer.q, layer.k_cache, layer.v_cache,
+                             torch.from_numpy(bt).cuda(), layer.context_lens,
+                             torch.from_numpy(idx).cuda(), K, wl.scale, out, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    ref = oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, bt, wl.context_lens, wl.scale,
+                           indices=idx)
+    assert np.abs(out.cpu().numpy() - ref).max() <= ATOL[dtype]
