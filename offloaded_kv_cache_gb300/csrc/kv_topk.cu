@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(kTopkThreads)
 // ---------------------------------------------------------------------------
 // union of the selected pages of the gc heads of one (b, kv head, head chunk)
 // ---------------------------------------------------------------------------
-constexpr int kUnionThreads = 256;
+// one CTA per group; 512 threads measured faster than 256 and 1024
+// (Llama-3.1-8B 32k attention call 44.5 -> 43.1 us)
+constexpr int kUnionThreads = 512;
 constexpr int kUnionWarps = kUnionThreads / 32;
 
 __global__ void __launch_bounds__(kUnionThreads)
