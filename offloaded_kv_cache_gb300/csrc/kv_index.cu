@@ -268,42 +268,16 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
                           const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
                           float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
                           long long nphys, int nchunk, int *status) {
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int b = blockIdx.z;
   const int kvh = blockIdx.y / nchunk, chunk = blockIdx.y % nchunk;
   const int G = Hq / Hkv;
   const int head0 = kvh * G + chunk * GS;
-  const int len = ctx[b];
-  if (len < 1 || len > maxP * ps) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
-    return;
-  }
-  const int P = (len + ps - 1) / ps;
-  const int p0 = (blockIdx.x * kScoreMmaWarps + warp) * 16;  // this warp's 16 pages
-  if (p0 >= maxP) return;
-
-  // physical pages of rows gid and gid + 8 (lanes 0..15 load the 16 entries)
-  long long ph_lane = -1;
-  if (lane < 16 && p0 + lane < P) {
-    const long long ph = bt[(long long)b * maxP + p0 + lane];
-    if (ph >= 0 && ph < nphys) ph_lane = ph;
-    else flag_error(status, KV_ERR_BOUNDS);
-  }
-  const long long ph_a = __shfl_sync(0xFFFFFFFFu, ph_lane, gid);
-  const long long ph_b = __shfl_sync(0xFFFFFFFFu, ph_lane, gid + 8);
-  constexpr int NCH = MEAN ? 4 : 8;       // 16-byte chunks per lane per row
-  constexpr int kRowElems = MEAN ? kHeadDim : 2 * kHeadDim;
-  uint4 ra[NCH], rb[NCH];
-  const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * kRowElems);
-  const uint4 *rowb = reinterpret_cast<const uint4 *>(mm + ((ph_b < 0 ? 0 : ph_b) * Hkv + kvh) * kRowElems);
-#pragma unroll
-  for (int i = 0; i < NCH; ++i) {
-    ra[i] = ph_a >= 0 ? rowa[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
-    rb[i] = ph_b >= 0 ? rowb[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
-  }
+  // q's coefficients first: no kernel of the path writes q, so they load
+  // before the wait for the previous kernel, overlapping its tail
   // coefficients of head gid in the same k order: [q- | q+] (min/max) or q (mean)
+  constexpr int NCH = MEAN ? 4 : 8;       // 16-byte chunks per lane per row
   uint4 cf[NCH];
 #pragma unroll
   for (int i = 0; i < NCH; ++i) {
@@ -320,6 +294,36 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
                            sign_part(w.w, neg));
       }
     }
+  }
+  const int p0 = (blockIdx.x * kScoreMmaWarps + warp) * 16;  // this warp's 16 pages
+  // the block-table entries too (no kernel of the path writes them)
+  long long bt_lane = -1;
+  if (lane < 16 && p0 + lane < maxP) bt_lane = bt[(long long)b * maxP + p0 + lane];
+  pdl_wait();
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int P = (len + ps - 1) / ps;
+  if (p0 >= maxP) return;
+
+  // physical pages of rows gid and gid + 8 (lanes 0..15 hold the 16 entries)
+  long long ph_lane = -1;
+  if (lane < 16 && p0 + lane < P) {
+    if (bt_lane >= 0 && bt_lane < nphys) ph_lane = bt_lane;
+    else flag_error(status, KV_ERR_BOUNDS);
+  }
+  const long long ph_a = __shfl_sync(0xFFFFFFFFu, ph_lane, gid);
+  const long long ph_b = __shfl_sync(0xFFFFFFFFu, ph_lane, gid + 8);
+  constexpr int kRowElems = MEAN ? kHeadDim : 2 * kHeadDim;
+  uint4 ra[NCH], rb[NCH];
+  const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * kRowElems);
+  const uint4 *rowb = reinterpret_cast<const uint4 *>(mm + ((ph_b < 0 ? 0 : ph_b) * Hkv + kvh) * kRowElems);
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    ra[i] = ph_a >= 0 ? rowa[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
+    rb[i] = ph_b >= 0 ? rowb[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
   }
   pdl_trigger();
   float c[4] = {0.f, 0.f, 0.f, 0.f};
