@@ -40,8 +40,8 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
 NCU_TRAFFIC = {
-    "opt6.7b-b32-ctx544": {"bytes": 289.548032e6, "src": "b64eee89734597a4"},
-    "llama3.1-8b-b4-ctx32k": {"bytes": 192.65408e6, "src": "b64eee89734597a4"},
+    "opt6.7b-b32-ctx544": {"bytes": 289.126144e6, "src": "e0f3fb86a4110dd7"},
+    "llama3.1-8b-b4-ctx32k": {"bytes": 192.608768e6, "src": "e0f3fb86a4110dd7"},
     # host-resident K/V: DRAM carries only q and the lists; the K/V bytes
     # arrive over the host link (ctc__rx_bytes_data_user.sum)
     "llama3.1-8b-b1-ctx128k-host": {"bytes": 183040.0, "link_bytes": 105.875456e6,
@@ -270,7 +270,10 @@ class ClockSampler:
 
 def oracle_sample(spec, wl, target_s: float, nthreads: int):
     """Times the oracle over whole (b, kv-head group) row sets, enough rows
-    for about target_s seconds; returns (GB/s, queries/s, seconds, sample)."""
+    for about target_s seconds; returns (GB/s, queries/s, seconds, sample).
+    The bytes are those the GPU metric counts for the same rows: dense, the
+    groups' K/V; sparse, the groups' index rows, the K/V of each group's union
+    of selected pages, q and out."""
     import oracle
     dtype = spec.dtype
     G = spec.group
@@ -278,6 +281,8 @@ def oracle_sample(spec, wl, target_s: float, nthreads: int):
 
     def rows_of(gs):
         return [b * spec.num_q_heads + kvh * G + g for b, kvh in gs for g in range(G)]
+
+    sel = {}
 
     def run(gs):
         rows = rows_of(gs)
@@ -290,6 +295,7 @@ def oracle_sample(spec, wl, target_s: float, nthreads: int):
                 s = oracle.scores(dtype, wl.q[b:b + 1], mn, mx, wl.block_table[b:b + 1],
                                   wl.context_lens[b:b + 1], spec.page_size)
                 idx = oracle.topk(s, wl.context_lens[b:b + 1], spec.page_size, spec.topk)
+                sel[b] = idx[0]
                 rb = [r - b * spec.num_q_heads for r in rows if r // spec.num_q_heads == b]
                 oracle.attention(dtype, wl.q[b:b + 1], wl.k_cache, wl.v_cache,
                                  wl.block_table[b:b + 1], wl.context_lens[b:b + 1], wl.scale,
@@ -306,8 +312,19 @@ def oracle_sample(spec, wl, target_s: float, nthreads: int):
         dt = run(groups[:n])
     gs = groups[:n]
     ctx = wl.context_lens
-    kv = sum(2 * int(ctx[b]) * spec.head_dim * spec.elem_bytes for b, _ in gs)
-    gbs = kv / dt / 1e9
+    e, d, ps = spec.elem_bytes, spec.head_dim, spec.page_size
+    if spec.topk:
+        nbytes = 0
+        for b, kvh in gs:
+            P = -(-int(ctx[b]) // ps)
+            nbytes += P * 2 * d * e                                   # index rows
+            pages = np.unique(sel[b][kvh * G:(kvh + 1) * G].reshape(-1))
+            for p in pages[pages >= 0]:
+                nbytes += 2 * min(ps, int(ctx[b]) - int(p) * ps) * d * e
+            nbytes += G * d * (e + 4)                                 # q and out
+    else:
+        nbytes = sum(2 * int(ctx[b]) * d * e + G * d * (e + 4) for b, _ in gs)
+    gbs = nbytes / dt / 1e9
     qps = len(rows_of(gs)) / dt
     what = (f"{n} of {len(groups)} (sequence, kv head) groups = {len(rows_of(gs))} query heads, "
             f"{'score+top-K+sparse attention' if spec.topk else 'dense attention'}, "
@@ -645,8 +662,11 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         gbs, cq, dt, what = oracle_sample(spec, wl, 2.0, cores)
+        gbs1, cq1, dt1, what1 = oracle_sample(spec, wl, 2.0, 1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": what, "seconds": round(dt, 3), "queries_per_s": round(cq, 2)}
+               "sample": what, "seconds": round(dt, 3), "queries_per_s": round(cq, 2),
+               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "sample": what1,
+                                 "seconds": round(dt1, 3), "queries_per_s": round(cq1, 2)}}
 
     if rank == 0:
         line = {
