@@ -44,8 +44,8 @@ NCU_TRAFFIC = {
     "llama3.1-8b-b4-ctx32k": {"bytes": 192.608768e6, "src": "e0f3fb86a4110dd7"},
     # host-resident K/V: DRAM carries only q and the lists; the K/V bytes
     # arrive over the host link (ctc__rx_bytes_data_user.sum)
-    "llama3.1-8b-b1-ctx128k-host": {"bytes": 183040.0, "link_bytes": 105.875456e6,
-                                    "src": "b64eee89734597a4"},
+    "llama3.1-8b-b1-ctx128k-host": {"bytes": 183552.0, "link_bytes": 105.728e6,
+                                    "src": "e0f3fb86a4110dd7"},
 }
 
 
