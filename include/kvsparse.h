@@ -43,7 +43,7 @@
  *    int32 arrays 4 bytes.
  *
  * Shapes: B = batch, Hq = query heads, Hkv = kv heads (Hq % Hkv == 0,
- * G = Hq / Hkv), d = head_dim (128), ps = page_size (16 or 64), maxP =
+ * G = Hq / Hkv), d = head_dim (128), ps = page_size (16, 32, 64 or 128), maxP =
  * max_pages_per_seq, N = num_phys_pages.  Sequence b holds context_lens[b]
  * tokens in pages 0 .. P_b - 1, P_b = ceil(context_lens[b] / ps); the last page
  * may be partial and only its first valid tokens take part anywhere.
@@ -75,7 +75,7 @@ typedef enum { KV_LOC_HBM = 0, KV_LOC_HOST_PINNED = 1 } kv_location;
 typedef enum {
   KV_OK = 0,
   KV_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad shape, k < 1      */
-  KV_ERR_UNSUPPORTED = -2,    /* d != 128, ps not in {16, 64}, unknown dtype,
+  KV_ERR_UNSUPPORTED = -2,    /* d != 128, ps not in {16,32,64,128}, dtype,
                                  max_pages_per_seq > 524288 (attention)      */
   KV_ERR_LOCATION = -3,       /* K/V memory does not match kv_loc               */
   KV_ERR_WORKSPACE = -4,      /* workspace null or smaller than required        */
@@ -89,7 +89,7 @@ typedef struct {
   int32_t num_q_heads;       /* Hq  >= 1                                      */
   int32_t num_kv_heads;      /* Hkv >= 1, divides Hq                          */
   int32_t head_dim;          /* d, must be 128                                */
-  int32_t page_size;         /* ps, 16 or 64 tokens                           */
+  int32_t page_size;         /* ps, 16, 32, 64 or 128 tokens                 */
   int32_t max_pages_per_seq; /* maxP >= 1                                     */
   int64_t num_phys_pages;    /* N >= 1: pages in k_cache / v_cache / minmax   */
   int32_t dtype;             /* kv_dtype of q, K, V and minmax                */

@@ -71,7 +71,10 @@ int check_shape(const kv_shape *s) {
   if (s->kv_loc != KV_LOC_HBM && s->kv_loc != KV_LOC_HOST_PINNED) return KV_ERR_INVALID_ARG;
   if (s->dtype != KV_F32 && s->dtype != KV_F16 && s->dtype != KV_BF16) return KV_ERR_UNSUPPORTED;
   if (s->head_dim != kHeadDim) return KV_ERR_UNSUPPORTED;
-  if (s->page_size != 16 && s->page_size != 64) return KV_ERR_UNSUPPORTED;
+  // pages are whole 16-token tiles; the attention keeps a page's valid-token
+  // count in 8 bits
+  if (s->page_size != 16 && s->page_size != 32 && s->page_size != 64 && s->page_size != 128)
+    return KV_ERR_UNSUPPORTED;
   // index arithmetic limits: tokens per row and K/V rows fit in int32
   if ((long long)s->max_pages_per_seq * s->page_size > INT_MAX) return KV_ERR_UNSUPPORTED;
   if (s->num_phys_pages * (long long)s->num_kv_heads * s->page_size > INT_MAX)

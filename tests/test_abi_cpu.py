@@ -53,7 +53,8 @@ FAKE = 0x10000  # 16-byte aligned address that is never dereferenced
 
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=64), kv.KV_ERR_UNSUPPORTED),
-    (dict(page_size=32), kv.KV_ERR_UNSUPPORTED),
+    (dict(page_size=48), kv.KV_ERR_UNSUPPORTED),
+    (dict(page_size=256), kv.KV_ERR_UNSUPPORTED),
     (dict(dtype=7), kv.KV_ERR_UNSUPPORTED),
     (dict(num_q_heads=6, num_kv_heads=4), kv.KV_ERR_INVALID_ARG),
     (dict(batch=0), kv.KV_ERR_INVALID_ARG),

@@ -57,6 +57,7 @@ def _check_caches(layer, wl):
 @pytest.mark.parametrize("dtype,ps,kv_loc", [
     ("bf16", 16, "hbm"), ("f16", 16, "hbm"), ("f32", 16, "hbm"),
     ("bf16", 64, "hbm"), ("f16", 64, "host"), ("bf16", 16, "host"),
+    ("bf16", 32, "hbm"), ("f16", 128, "host"),
 ])
 def test_one_append_matches_oracle(dtype, ps, kv_loc):
     # rows that open a new page (len % ps == 0), fill a page's last slot, and

@@ -264,3 +264,18 @@ def test_sparse_attention_with_a_70000_page_block_table(dtype, hq, hkv):
     ref = oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, bt, wl.context_lens, wl.scale,
                            indices=idx)
     assert np.abs(out.cpu().numpy() - ref).max() <= ATOL[dtype]
+
+
+# ---------------------------------------------------------------- page sizes 32 and 128
+
+@pytest.mark.parametrize("dtype,ps,kv_loc,hq,hkv", [
+    ("bf16", 32, "hbm", 8, 2), ("f16", 128, "hbm", 16, 2), ("f32", 32, "hbm", 2, 1),
+    ("bf16", 128, "host", 8, 2), ("f16", 32, "host", 4, 4),
+])
+def test_pages_of_32_and_128_tokens(dtype, ps, kv_loc, hq, hkv):
+    # page sizes the tiered-offload guidance recommends for 70B-class models;
+    # pages are whole 16-token tiles, ragged last pages included
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=hq, hkv=hkv, context=ps * 9 + 5, ps=ps,
+                       topk=3, index=150 + ps)
+    wl = W.generate(spec, context_lens=[ps * 9 + 5, ps * 4, 17])
+    run_pipeline_and_check(wl, 3, kv_loc=kv_loc)

@@ -70,6 +70,7 @@ def _check_slots(layer, wl):
     ("f16", 4, 2, 64, "host", 12),    # G = 2, CUDA-core attention, 64-token pages
     ("f32", 2, 2, 16, "host", 8),     # fp32, C = 2 G K
     ("bf16", 16, 2, 16, "hbm", 48),   # G = 8, window in front of HBM K/V
+    ("bf16", 8, 2, 128, "host", 20),  # 128-token pages
 ])
 def test_window_policy_and_output_match_oracle(dtype, hq, hkv, ps, kv_loc, C):
     K = 4
