@@ -329,10 +329,13 @@ int kv_window_reset(const kv_shape *shape, const kv_window *win, void *stream);
  *   assign  = misses in ascending page order take the free slots in
  *             ascending slot order;
  *   fetch   = the misses, and the row's last page when it is a hit (tokens
- *             may have been appended since it was copied): their valid
- *             tokens are copied from k_cache / v_cache into the window;
- * then attention runs over the window (HBM) exactly as kv_sparse_decode_attn
- * -- same out.  C must hold every needed page: C >= min(G * k, maxP), else
+ *             may have been appended since it was copied);
+ * then attention runs exactly as kv_sparse_decode_attn -- same out -- reading
+ * the hits from the window (HBM) and the fetched pages from k_cache /
+ * v_cache, whose valid tokens it also stores into their window slots.  When
+ * G exceeds the heads one attention CTA covers (G > 8; G > 4 for fp32), a
+ * page several head chunks need is read from k_cache once per chunk.
+ * C must hold every needed page: C >= min(G * k, maxP), else
  * KV_ERR_INVALID_ARG.  cache_k / cache_v must be device memory
  * (KV_ERR_LOCATION).  The workspace must hold kv_window_workspace_bytes. */
 int kv_sparse_decode_attn_window(const kv_shape *shape, const void *q, const void *k_cache,

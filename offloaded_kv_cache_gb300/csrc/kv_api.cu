@@ -108,6 +108,7 @@ int resolve_kv(const kv_shape *s, const void *p, const void **dev_ptr) {
 struct Plan {
   int gc = 1, nchunk = 1, groups = 1;
   bool mma = false;
+  bool win = false;  // the page-window instantiation (16-byte page-list entries)
   int S = 1, umax = 0, nstages = 4, nw = 4, header = 8192;
   size_t smem = 0;
   size_t off_part_o = 0, off_part_ml = 0, off_upages = 0, off_umasks = 0, off_ucount = 0;
@@ -139,14 +140,15 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int header_bytes(const Plan &pl, int elem, long long list_pages) {
   const long long b = attn_fixed_header(elem, pl.gc, pl.mma) +
-                      8 * std::min<long long>(list_pages, kMaxListPages);
+                      (long long)attn_entry_bytes(pl.win) *
+                          std::min<long long>(list_pages, kMaxListPages);
   return (int)((b + 1023) / 1024 * 1024);
 }
 
 // occupancy answers, cached per (device, kernel, threads, shared memory):
 // the calculator costs microseconds of host time per query
 struct OccEntry {
-  int dev, dtype, gc, mma, threads;
+  int dev, dtype, gc, mma, win, threads;
   size_t smem;
   int n;
 };
@@ -154,22 +156,23 @@ std::mutex g_occ_mutex;
 OccEntry g_occ[64];
 int g_occ_n = 0;
 
-int cached_occupancy(int dtype, int gc, bool mma, int threads, size_t smem) {
+int cached_occupancy(int dtype, int gc, bool mma, bool win, int threads, size_t smem) {
   const int dev = current_device();
   {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     for (int i = 0; i < g_occ_n; ++i) {
       const OccEntry &e = g_occ[i];
       if (e.dev == dev && e.dtype == dtype && e.gc == gc && e.mma == (int)mma &&
-          e.threads == threads && e.smem == smem)
+          e.win == (int)win && e.threads == threads && e.smem == smem)
         return e.n;
     }
   }
-  const int n = mma ? attn_occupancy_mma(dtype, gc, threads, smem)
-                    : attn_occupancy_core(dtype, gc, threads, smem);
+  const int n = win   ? attn_occupancy_win(dtype, gc, mma, threads, smem)
+                : mma ? attn_occupancy_mma(dtype, gc, threads, smem)
+                      : attn_occupancy_core(dtype, gc, threads, smem);
   if (n > 0) {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
-    g_occ[g_occ_n % 64] = OccEntry{dev, dtype, gc, (int)mma, threads, smem, n};
+    g_occ[g_occ_n % 64] = OccEntry{dev, dtype, gc, (int)mma, (int)win, threads, smem, n};
     if (g_occ_n < 64) ++g_occ_n;
   }
   return n;
@@ -180,7 +183,7 @@ int cached_occupancy(int dtype, int gc, bool mma, int threads, size_t smem) {
 int resident_ctas(const Plan &pl, int dtype, bool have_device) {
   const int threads = 32 * (1 + pl.nw);
   int n = 0;
-  if (have_device) n = cached_occupancy(dtype, pl.gc, pl.mma, threads, pl.smem);
+  if (have_device) n = cached_occupancy(dtype, pl.gc, pl.mma, pl.win, threads, pl.smem);
   if (n <= 0) {
     n = (int)((228 * 1024) / (pl.smem + 1024));
     n = std::min(n, 2048 / threads);
@@ -188,8 +191,9 @@ int resident_ctas(const Plan &pl, int dtype, bool have_device) {
   return std::max(n, 1);
 }
 
-Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
+Plan make_plan(const kv_shape *s, int k, int sms, bool have_device, bool win) {
   Plan pl;
+  pl.win = win;
   const int G = s->num_q_heads / s->num_kv_heads;
   if (s->dtype == KV_F32) {
     pl.gc = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
@@ -284,7 +288,7 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device) {
 // Plans depend only on (device, shape, k): cache them, since the split search
 // and the occupancy query cost host time on every call.
 struct PlanEntry {
-  int dev, k;
+  int dev, k, win;
   kv_shape shape;
   Plan plan;
 };
@@ -299,18 +303,19 @@ bool same_shape(const kv_shape &x, const kv_shape &y) {
          x.num_phys_pages == y.num_phys_pages && x.dtype == y.dtype && x.kv_loc == y.kv_loc;
 }
 
-Plan cached_plan(const kv_shape *s, int k) {
+Plan cached_plan(const kv_shape *s, int k, bool win = false) {
   const int dev = current_device();
   {
     std::lock_guard<std::mutex> lock(g_plan_mutex);
     for (int i = 0; i < std::min(g_plan_n, 32); ++i)
-      if (g_plans[i].dev == dev && g_plans[i].k == k && same_shape(g_plans[i].shape, *s))
+      if (g_plans[i].dev == dev && g_plans[i].k == k && g_plans[i].win == (int)win &&
+          same_shape(g_plans[i].shape, *s))
         return g_plans[i].plan;
   }
-  const Plan pl = make_plan(s, k, dev >= 0 ? sm_count(dev) : 152, dev >= 0);
+  const Plan pl = make_plan(s, k, dev >= 0 ? sm_count(dev) : 152, dev >= 0, win);
   if (dev >= 0) {
     std::lock_guard<std::mutex> lock(g_plan_mutex);
-    g_plans[g_plan_n % 32] = PlanEntry{dev, k, *s, pl};
+    g_plans[g_plan_n % 32] = PlanEntry{dev, k, (int)win, *s, pl};
     ++g_plan_n;
   }
   return pl;
@@ -362,16 +367,17 @@ struct WindowCall {
 };
 
 // Window shape and workspace: the attention plan of the window shape, then
-// the fetch lists [B][Hkv][C] (page, slot) and counts [B][Hkv].
+// the fetch bits [B][Hkv][ceil(maxP / 32)] (pages this step reads from the
+// source cache).
 kv_shape window_shape(const kv_shape *s, int C) {
   kv_shape w = *s;
   w.num_phys_pages = (int64_t)s->batch * C;
   w.kv_loc = KV_LOC_HBM;
   return w;
 }
-size_t window_lists_bytes(const kv_shape *s, int C) {
-  const size_t groups = (size_t)s->batch * s->num_kv_heads;
-  return 2 * align256(groups * (size_t)C * 4) + align256(groups * 4);
+int fetch_words(const kv_shape *s) { return (int)((s->max_pages_per_seq + 31) / 32); }
+size_t window_bits_bytes(const kv_shape *s) {
+  return align256((size_t)s->batch * s->num_kv_heads * fetch_words(s) * 4);
 }
 
 // Encoded tensor maps depend only on (device, base address, rows, dtype);
@@ -433,32 +439,25 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
   if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
   const kv_shape *as = wc ? &wc->wshape : s;  // the shape the attention reads
-  const Plan pl = cached_plan(as, indices ? k : 0);
+  const Plan pl = cached_plan(as, indices ? k : 0, wc != nullptr);
   const int C = wc ? wc->win->cache_pages : 0;
-  const size_t need_ws = pl.total + (wc ? window_lists_bytes(s, C) : 0);
+  const size_t need_ws = pl.total + (wc ? window_bits_bytes(s) : 0);
   if (need_ws > 0 && (ws == nullptr || ws_bytes < need_ws || !al16(ws))) return KV_ERR_WORKSPACE;
   int *status = status_ptr(dev);
   if (!status) return KV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *w = static_cast<char *>(ws);
+  uint32_t *fbits = nullptr;
+  const void *src_k = kd, *src_v = vd;
   if (wc) {
-    // the window step: update the state, then copy the fetch list into the
-    // window; the attention below reads the window only
-    const size_t groups = (size_t)s->batch * s->num_kv_heads;
-    int32_t *fpage = reinterpret_cast<int32_t *>(w + pl.total);
-    int32_t *fslot = reinterpret_cast<int32_t *>(w + pl.total + align256(groups * C * 4));
-    int32_t *fcount = reinterpret_cast<int32_t *>(w + pl.total + 2 * align256(groups * C * 4));
+    // the window step: update the state and mark this step's fetches; the
+    // attention below reads the window, and the fetched pages from the cache
+    fbits = reinterpret_cast<uint32_t *>(w + pl.total);
     const kv_window *win = wc->win;
     cudaError_t e = launch_window_update(indices, wc->scores, ctx, s->batch, s->num_q_heads,
                                          s->num_kv_heads, s->page_size, s->max_pages_per_seq, k,
-                                         C, win->slot_page, win->page_slot, fpage, fslot, fcount,
-                                         win->stats, status, st);
-    if (e != cudaSuccess) return KV_ERR_CUDA;
-    const int bpg = (int)std::max<long long>(
-        1, std::min<long long>(C, (long long)sm_count(dev) * 8 / (long long)groups));
-    e = launch_window_fetch(s->dtype, kd, vd, win->cache_k, win->cache_v, bt, ctx, fpage, fslot,
-                            fcount, s->batch, s->num_kv_heads, s->page_size,
-                            s->max_pages_per_seq, C, s->num_phys_pages, bpg, status, st);
+                                         C, win->slot_page, win->page_slot, fbits, win->stats,
+                                         status, st);
     if (e != cudaSuccess) return KV_ERR_CUDA;
     kd = win->cache_k;
     vd = win->cache_v;
@@ -476,6 +475,11 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   if (wc) {
     a.page_slot = wc->win->page_slot;
     a.cache_C = C;
+    a.fetch_bits = fbits;
+    a.fetch_words = fetch_words(s);
+    a.src_k = src_k;
+    a.src_v = src_v;
+    a.src_nphys = s->num_phys_pages;
   }
   a.B = s->batch;
   a.Hq = s->num_q_heads;
@@ -516,8 +520,9 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
     if ((rc = kv_map_cached(as, vd, &tv)) != KV_OK) return rc;
   }
   dim3 grid(pl.S, pl.groups, s->batch);
-  cudaError_t e = pl.mma ? launch_attn_mma(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st)
-                         : launch_attn_core(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st);
+  cudaError_t e = wc       ? launch_attn_win(s->dtype, pl.gc, pl.mma, a, &tk, &tv, grid, pl.smem, st)
+                  : pl.mma ? launch_attn_mma(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st)
+                           : launch_attn_core(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st);
   if (e != cudaSuccess) return KV_ERR_CUDA;
   if (pl.S > 1) {
     e = launch_combine(a.part_o, a.part_ml, out, pl.S, s->batch, s->num_q_heads, st);
@@ -773,7 +778,7 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
 size_t kv_window_workspace_bytes(const kv_shape *shape, int32_t k, int32_t cache_pages) {
   if (check_shape(shape) != KV_OK || k < 1 || cache_pages < 1) return 0;
   const kv_shape w = window_shape(shape, cache_pages);
-  return cached_plan(&w, k).total + window_lists_bytes(shape, cache_pages);
+  return cached_plan(&w, k, true).total + window_bits_bytes(shape);
 }
 
 static int check_window(const kv_shape *s, const kv_window *win, int32_t k) {

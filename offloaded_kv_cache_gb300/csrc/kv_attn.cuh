@@ -33,6 +33,13 @@
 //    high and a low 16-bit part so the weights keep ~16 bits); otherwise
 //    CUDA-core FMAs with lanes over (token, slab) for q.k and over channels
 //    for p.v.  Max/sum reductions are warp shuffles.
+//  * Window instantiations (WIN): K/V are the GPU-resident page window and
+//    the pages the window update marked in fetch_bits come from the source
+//    cache instead.  The producer fills a window page's stage by TMA and a
+//    fetched page's stage by cp.async from the (host-mapped) source; the
+//    consumer that used a fetched tile stores its valid rows into the page's
+//    window slot.  The host-link reads of the misses so overlap the HBM reads
+//    of the hits, and no separate copy pass runs before the attention.
 //  * Every mbarrier wait is bounded in wall time; a wait that gives up
 //    records KV_ERR_DEVICE_TIMEOUT and the CTA winds down.
 #pragma once
@@ -100,16 +107,27 @@ struct PageRange {
   int lo, n;  // first index into the (dense or union) list, count
 };
 // one page of the list, resolved once in the prologue: physical page (-1 when
-// the entry is out of range) and (valid tokens | head mask << 8)
+// the entry is out of range) and (valid tokens | head mask << 8); the window
+// instantiations add the source page to fetch (-1: the window slot holds it)
+template <bool WIN>
 struct PageEnt {
   int phys;
   int info;
 };
+template <>
+struct PageEnt<true> {
+  int phys;
+  int info;
+  int src;
+  int pad;
+};
 
-template <class T, int GC, bool MMA>
+template <class T, int GC, bool MMA, bool WIN>
 __global__ void __launch_bounds__(kAttnMaxThreads)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv) {
+  using Ent = PageEnt<WIN>;
+  static_assert(sizeof(Ent) == attn_entry_bytes(WIN), "page-list entry size");
   if constexpr (MMA) pdl_wait();
   constexpr int SL = (int)sizeof(T);        // 128-byte slabs per 128-element row
   constexpr int EPS = 128 / (int)sizeof(T); // elements per slab
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   uint64_t *empty = full + kMaxStages;
   float *q_s = reinterpret_cast<float *>(smem + 256);  // CUDA core: [GC][SL][QSTR]
   float *pbuf = q_s + GC * SL * QSTR;                  // CUDA core: [warps][GC][TP]
-  PageEnt *plist = reinterpret_cast<PageEnt *>(smem + attn_fixed_header(SL, GC, MMA));
+  Ent *plist = reinterpret_cast<Ent *>(smem + attn_fixed_header(SL, GC, MMA));
   uint8_t *stages = smem + a.header_bytes;
 
   constexpr int TT = kTileTokens;            // tokens per tile (stage)
@@ -146,7 +164,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     // that this overlaps that kernel's tail (OPT-6.7B dense 46.7 -> 46.0 us).
     if (threadIdx.x == 0) {
       for (int s = 0; s < a.nstages; ++s) {
-        mbar_init(smem_u32(&full[s]), a.use_tma ? 1u : 32u);
+        mbar_init(smem_u32(&full[s]), a.use_tma && !WIN ? 1u : 32u);
         mbar_init(smem_u32(&empty[s]), 1u);
       }
       fence_mbar_init();
@@ -176,7 +194,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
 
   if (MMA && threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(&full[s]), a.use_tma ? 1u : 32u);
+      mbar_init(smem_u32(&full[s]), a.use_tma && !WIN ? 1u : 32u);
       mbar_init(smem_u32(&empty[s]), 1u);
     }
     fence_mbar_init();
@@ -195,12 +213,20 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       p = e;
       mask = (1u << GC) - 1u;
     }
-    PageEnt ent{-1, 0};
+    Ent ent{};
+    ent.phys = -1;
+    if constexpr (WIN) ent.src = -1;
     if (p >= 0 && p < P) {
       long long ph;
-      if (a.page_slot) {  // the page's slot in the window (page b*C + slot)
-        const int sl = a.page_slot[((long long)b * a.Hkv + kvh) * a.maxP + p];
+      if constexpr (WIN) {  // the page's slot in the window (page b*C + slot)
+        const long long gk = (long long)b * a.Hkv + kvh;
+        const int sl = a.page_slot[gk * a.maxP + p];
         ph = (sl >= 0 && sl < a.cache_C) ? (long long)b * a.cache_C + sl : -1;
+        if (ph >= 0 && ((a.fetch_bits[gk * a.fetch_words + (p >> 5)] >> (p & 31)) & 1u)) {
+          const long long sp = a.block_table[(long long)b * a.maxP + p];
+          if (sp >= 0 && sp < a.src_nphys) ent.src = (int)sp;
+          else ph = -1;
+        }
       } else {
         ph = a.block_table[(long long)b * a.maxP + p];
       }
@@ -218,7 +244,51 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     // ======================= producer =====================================
     int issued = 0;
     bool ok = true;
-    if (a.use_tma) {
+    if constexpr (WIN) {
+      // all 32 lanes: a fetched page by cp.async from the source (each lane
+      // arrives when its copies land), a window page by TMA (lane 0 arms the
+      // transaction count, the other lanes arrive at once)
+      const char *kbase = static_cast<const char *>(a.src_k);
+      const char *vbase = static_cast<const char *>(a.src_v);
+      constexpr int chunks = TT * SL * 8;  // 16-byte chunks per K (or V) tile
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(smem_u32(&empty[s]), ((j / NS) - 1) & 1, a.wait_limit_ns)) {
+          if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
+          ok = false;
+          break;
+        }
+        const Ent ent = plist[j / UPP];
+        issued = j + 1;
+        if (j == a.debug_skip_page) continue;
+        const uint32_t fb = smem_u32(&full[s]);
+        const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
+        if (ent.src >= 0) {
+          const size_t src0 =
+              ((size_t)(((long long)ent.src * a.Hkv + kvh) * ps) + (size_t)(j % UPP) * TT) *
+              (SL * 128);
+          for (int i = lane; i < chunks; i += 32) {
+            const int row = i / (SL * 8), rem = i % (SL * 8);
+            const uint32_t d = dst + (rem >> 3) * slab_bytes + swz(row, rem & 7);
+            const size_t off = src0 + (size_t)row * (SL * 128) + rem * 16;
+            cp_async16(d, kbase + off);
+            cp_async16(d + kv_off, vbase + off);
+          }
+          cp_async_arrive_noinc(fb);
+        } else if (lane == 0) {
+          const long long phys = max(ent.phys, 0);
+          const int row0 = (int)((phys * a.Hkv + kvh) * ps) + (j % UPP) * TT;
+          mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+#pragma unroll
+          for (int h = 0; h < SL; ++h) tma_load_2d(dst + h * slab_bytes, &tk, h * EPS, row0, fb);
+#pragma unroll
+          for (int h = 0; h < SL; ++h)
+            tma_load_2d(dst + kv_off + h * slab_bytes, &tv, h * EPS, row0, fb);
+        } else {
+          mbar_arrive(fb);
+        }
+      }
+    } else if (a.use_tma) {
       if (lane == 0) {
         for (int j = 0; j < ntiles; ++j) {
           const int s = j % NS;
@@ -273,7 +343,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     (void)ok;
     // Drain: wait (bounded) until the last fill of every stage has landed, so
     // no asynchronous copy targets this CTA's shared memory after it moves on.
-    if (lane == 0 || !a.use_tma) {
+    if (lane == 0 || !a.use_tma || WIN) {
       for (int s = 0; s < NS && s < issued; ++s) {
         int jl = s + ((issued - 1 - s) / NS) * NS;  // last page issued into stage s
         if (jl == a.debug_skip_page) jl -= NS;
@@ -281,6 +351,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
         if (!mbar_wait(smem_u32(&full[s]), (jl / NS) & 1, a.wait_limit_ns))
           flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
       }
+      // and, whatever the waits saw, none of this lane's cp.async is in flight
+      if (WIN || !a.use_tma) cp_async_wait_all();
     }
     __syncwarp();
   }
@@ -322,7 +394,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
         if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
         break;
       }
-      const PageEnt ent = plist[j / UPP];
+      const Ent ent = plist[j / UPP];
       const uint32_t msk = (uint32_t)ent.info >> 8;
       // valid tokens of this tile (0 for a bad entry)
       const int nv = ent.phys >= 0 ? max(0, min(TT, (ent.info & 0xFF) - (j % UPP) * TT)) : 0;
@@ -491,6 +563,26 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           __syncwarp();
         }
       }
+      if constexpr (WIN) {
+        if (ent.src >= 0 && nv > 0) {
+          // a fetched tile: its valid rows go to the page's window slot
+          char *kw = static_cast<char *>(const_cast<void *>(a.k));
+          char *vw = static_cast<char *>(const_cast<void *>(a.v));
+          const size_t dst0 =
+              ((size_t)(((long long)ent.phys * a.Hkv + kvh) * ps) + (size_t)(j % UPP) * TT) *
+              (SL * 128);
+          for (int i = lane; i < nv * SL * 8; i += 32) {
+            const int row = i / (SL * 8), rem = i % (SL * 8);
+            const uint8_t *src = st + (rem >> 3) * slab_bytes + swz(row, rem & 7);
+            const size_t off = dst0 + (size_t)row * (SL * 128) + rem * 16;
+            *reinterpret_cast<uint4 *>(kw + off) = *reinterpret_cast<const uint4 *>(src);
+            *reinterpret_cast<uint4 *>(vw + off) = *reinterpret_cast<const uint4 *>(src + kv_off);
+          }
+          // the stage may next be filled by TMA: order this warp's view of
+          // the cp.async data before those async-proxy writes
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     }
@@ -568,10 +660,10 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   }
 }
 
-template <class T, int GC, bool MMA>
+template <class T, int GC, bool MMA, bool WIN = false>
 cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                           dim3 grid, size_t smem, cudaStream_t st) {
-  auto kern = attn_kernel<T, GC, MMA>;
+  auto kern = attn_kernel<T, GC, MMA, WIN>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -584,9 +676,9 @@ cudaError_t launch_attn_t(const AttnArgs &a, const CUtensorMap *tk, const CUtens
   return launch_pdl(kern, grid, dim3(32 * (1 + a.nw)), smem, st, a, *tk, *tv);
 }
 
-template <class T, int GC, bool MMA>
+template <class T, int GC, bool MMA, bool WIN = false>
 int attn_occupancy_t(int threads, size_t smem) {
-  auto kern = attn_kernel<T, GC, MMA>;
+  auto kern = attn_kernel<T, GC, MMA, WIN>;
   int dev = 0;
   cudaGetDevice(&dev);
   static int attr_done[64] = {0};

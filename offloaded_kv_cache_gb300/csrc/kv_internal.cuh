@@ -192,6 +192,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
+// Wait until every cp.async of this thread has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // ---------------------------------------------------------------------------
 // 128-byte swizzle: inside each 1024-byte block of eight 128-byte rows, the
@@ -217,6 +221,11 @@ struct AttnArgs {
   const int32_t *union_count;   // sparse: [B][groups]
   const int32_t *page_slot;     // window: [B][Hkv][maxP] slot of a page, else null
   int cache_C;                  // window: slots per (b, kv head); K/V are the window
+  const uint32_t *fetch_bits;   // window: [B][Hkv][fetch_words] pages read from the source
+  int fetch_words;              // window: ceil(maxP / 32)
+  const void *src_k;            // window: device-visible source K cache (host or HBM)
+  const void *src_v;            // window: device-visible source V cache
+  long long src_nphys;          // window: physical pages of the source cache
   float *out;                   // [B][Hq][d]      (num_splits == 1)
   float *part_o;                // [S][B][Hq][d]   (num_splits > 1)
   float *part_ml;               // [S][B][Hq][2]   (log2-domain max, sum)
@@ -251,6 +260,9 @@ __host__ __device__ inline int attn_fixed_header(int elem_bytes, int gc, bool mm
   return (off + 255) & ~255;
 }
 constexpr int kMaxStages = 16;
+// Bytes of one page-list entry: (page, tokens | head mask), plus the source
+// page to fetch in the window instantiations.
+__host__ __device__ constexpr int attn_entry_bytes(bool win) { return win ? 16 : 8; }
 
 // launchers (return a cudaError_t)
 cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
@@ -263,15 +275,8 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void 
 size_t window_update_smem(int maxP, int C);
 cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
                                  int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
-                                 int32_t *slot_page, int32_t *page_slot, int32_t *fetch_page,
-                                 int32_t *fetch_slot, int32_t *fetch_count, int32_t *stats,
-                                 int *status, cudaStream_t st);
-cudaError_t launch_window_fetch(int dtype, const void *k_src, const void *v_src, void *k_win,
-                                void *v_win, const int32_t *bt, const int32_t *ctx,
-                                const int32_t *fetch_page, const int32_t *fetch_slot,
-                                const int32_t *fetch_count, int B, int Hkv, int ps, int maxP,
-                                int C, long long nphys, int blocks_per_group, int *status,
-                                cudaStream_t st);
+                                 int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
+                                 int32_t *stats, int *status, cudaStream_t st);
 cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
 cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
                               const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
@@ -290,9 +295,13 @@ cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtenso
                              const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
 cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
                             const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
+// the window instantiations: attention that also fetches the step's misses
+cudaError_t launch_attn_win(int dtype, int gc, bool mma, const AttnArgs &a, const CUtensorMap *tk,
+                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
 // resident attention CTAs per SM for a launch shape (0 when unknown)
 int attn_occupancy_core(int dtype, int gc, int threads, size_t smem);
 int attn_occupancy_mma(int dtype, int gc, int threads, size_t smem);
+int attn_occupancy_win(int dtype, int gc, bool mma, int threads, size_t smem);
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st);
 

@@ -5,7 +5,7 @@
 // LLM Inference, section 2.2: for each query only the Top-K most important
 // blocks are retrieved.  Ties go to the lower page index; pages come out
 // ascending.
-#include "kv_select.cuh"
+#include "kv_internal.cuh"
 
 namespace kvs {
 namespace {
@@ -21,14 +21,15 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 constexpr uint32_t kForcedKey = 0xFFFFFFFFu;
 
 // One CTA per (b, h) row.  Radix select of the K-th largest key, 8 bits per
-// pass from the top (a shared-memory histogram whose threshold digit one warp
-// finds with a shuffle scan), stopping early once every key of the threshold
-// bin is taken.  The output pass splits the pages into one contiguous segment
-// per warp; each warp walks its segment 32 pages at a time and places the
-// selected pages in index order with ballots, after one block scan of the
-// per-warp counts.  Equal keys at the threshold go to the lower page index.
-// (kv_select.cuh holds the same select as reusable helpers; this hot kernel
-// keeps its own copy, which measured 0.7 us faster per launch.)
+// pass from the highest bit where the row's keys differ (the bits above it
+// are common to every key, so a pass spent on them would select nothing):
+// a shared-memory histogram, double-buffered so that a pass needs two block
+// barriers, whose threshold digit one warp finds with a shuffle scan;
+// stopping early once every key of the threshold bin is taken.  The output
+// pass gives each thread a run of consecutive pages, counts its keys above
+// and at the threshold, and after one block scan of those counts places the
+// selected pages in page order.  Equal keys at the threshold go to the lower
+// page index.  (kv_select.cuh holds a generic select for other kernels.)
 // Forced pages (the pages holding the first sink_tokens tokens and the last
 // local_tokens tokens of the row) take a key above every score's, so they are
 // selected first, lower index first among themselves.
@@ -38,9 +39,14 @@ __global__ void __launch_bounds__(kTopkThreads)
                 int maxP, int K, int keys_in_smem, int sink_tokens, int local_tokens,
                 int32_t *__restrict__ out, int *status) {
   pdl_wait();
+  constexpr int kTopkWarps = kTopkThreads / 32;
   extern __shared__ uint32_t skeys[];
-  __shared__ RadixScratch sc;
-  const int tid = threadIdx.x;
+  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t wmin[kTopkWarps], wmax[kTopkWarps];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_krem, s_all;
+  __shared__ unsigned long long wsum[kTopkWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long row = blockIdx.x;
   const int b = (int)(row / Hq);
   int32_t *orow = out + row * K;
@@ -53,41 +59,57 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   const int P = (len + ps - 1) / ps;
   const int keff = min(K, P);
-  if (keff == P) {  // every page is selected
+  if (keff == P) {
     for (int i = tid; i < K; i += kTopkThreads) orow[i] = i < P ? i : -1;
     return;
   }
-  // forced pages: [0, f_sink) and [f_local, P)
   const int f_sink = sink_tokens > 0 ? min(P, (sink_tokens + ps - 1) / ps) : 0;
   const int f_local = local_tokens > 0 ? max(0, len - local_tokens) / ps : P;
   auto raw_key = [&](int p) -> uint32_t {
     return (p < f_sink || p >= f_local) ? kForcedKey : score_key(srow[p]);
   };
-  if (keys_in_smem) {
-    for (int p = tid; p < P; p += kTopkThreads) skeys[p] = raw_key(p);
-  }
   auto key_at = [&](int p) -> uint32_t { return keys_in_smem ? skeys[p] : raw_key(p); };
 
-  constexpr int kTopkWarps = kTopkThreads / 32;
-  const int warp = tid >> 5, lane = tid & 31;
-  uint32_t prefix = 0, pmask = 0;
-  int krem = keff;  // keys matching `prefix` that still have to be taken
-  bool all_taken = false;
+  // keys (into shared memory when they fit), their minimum and maximum
+  if (tid < 256) hist[0][tid] = 0;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int p = tid; p < P; p += kTopkThreads) {
+    const uint32_t k = raw_key(p);
+    if (keys_in_smem) skeys[p] = k;
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  if (lane == 0) { wmin[warp] = kmin; wmax[warp] = kmax; }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xFFFFFFFFu, lane < kTopkWarps ? wmin[lane] : 0xFFFFFFFFu);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, lane < kTopkWarps ? wmax[lane] : 0u);
+
+  // radix select from the highest bit where the keys differ (the bits above
+  // it are common to every key), 8 bits per pass
+  const uint32_t diff = kmin ^ kmax;
+  const int top = diff ? 31 - __clz(diff) : -1;
+  uint32_t pmask = top >= 31 ? 0u : (0xFFFFFFFFu << (top + 1));
+  uint32_t prefix = kmin & pmask;
+  int krem = keff;
+  int pass = 0;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) sc.hist[tid] = 0;
-    __syncthreads();
+  for (int hb = top; hb >= 0; hb -= 8, ++pass) {
+    const int lb = max(hb - 7, 0);
+    const uint32_t dmask = (1u << (hb - lb + 1)) - 1u;
+    uint32_t *h = hist[pass & 1];
+    if (tid < 256) hist[(pass + 1) & 1][tid] = 0;  // the next pass's histogram
     for (int p = tid; p < P; p += kTopkThreads) {
       const uint32_t k = key_at(p);
-      if ((k & pmask) == prefix) atomicAdd(&sc.hist[(k >> shift) & 255u], 1u);
+      if ((k & pmask) == prefix) atomicAdd(&h[(k >> lb) & dmask], 1u);
     }
     __syncthreads();
     if (tid < 32) {
-      // lane l owns digits 255-8l .. 248-8l, scanned from the top
       int c[8], sum = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = (int)sc.hist[255 - 8 * tid - j];
+        c[j] = (int)h[255 - 8 * tid - j];
         sum += c[j];
       }
       int incl = sum;
@@ -101,9 +123,9 @@ __global__ void __launch_bounds__(kTopkThreads)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (above + c[j] >= krem) {
-            sc.digit = (uint32_t)(255 - 8 * tid - j);
-            sc.krem = krem - above;
-            sc.all = (above + c[j] == krem) ? 1 : 0;
+            s_digit = (uint32_t)(255 - 8 * tid - j);
+            s_krem = krem - above;
+            s_all = (above + c[j] == krem) ? 1 : 0;
             break;
           }
           above += c[j];
@@ -111,47 +133,66 @@ __global__ void __launch_bounds__(kTopkThreads)
       }
     }
     __syncthreads();
-    prefix |= sc.digit << shift;
-    pmask |= 255u << shift;
-    krem = sc.krem;
-    if (sc.all) {
-      all_taken = true;  // every key with this prefix is selected
-      break;
-    }
+    prefix |= s_digit << lb;
+    pmask |= dmask << lb;
+    krem = s_krem;
+    if (s_all) break;
   }
   pdl_trigger();
-  // selected: keys whose masked value beats the prefix, plus those equal to
-  // it -- all of them when all_taken, else the first krem in page order
-  const int seg = ((P + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;  // pages per warp
-  const int lo = warp * seg, hi = min(P, lo + seg);
-  uint32_t gt_n = 0, eq_n = 0;
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
-    gt_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k > prefix));
-    eq_n += __popc(__ballot_sync(0xFFFFFFFFu, p < hi && k == prefix));
-  }
-  unsigned long long tot;
-  const unsigned long long base =
-      warp_bases64<kTopkWarps>(((unsigned long long)eq_n << 32) | gt_n, sc.wsum, &tot);
-  long long gt_b = (long long)(base & 0xFFFFFFFFull);
-  long long eq_b = (long long)(base >> 32);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t k = p < hi ? key_at(p) & pmask : 0u;
-    const unsigned gtb = __ballot_sync(0xFFFFFFFFu, p < hi && k > prefix);
-    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, p < hi && k == prefix);
-    const long long my_gt = gt_b + __popc(gtb & lt_mask);
-    const long long my_eq = eq_b + __popc(eqb & lt_mask);
-    const bool is_gt = (gtb >> lane) & 1u, is_eq = (eqb >> lane) & 1u;
-    const bool sel = is_gt || (is_eq && (all_taken || my_eq < krem));
-    if (sel) {
-      const long long pos = my_gt + (all_taken ? my_eq : min(my_eq, (long long)krem));
-      if (pos < K) orow[pos] = p;
+  // selected: keys above the threshold, then the first krem equal to it in
+  // page order (all of them when the last pass took its whole bin, where
+  // krem is their count).  Each thread owns `per` consecutive pages.
+  const int per = ((P + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
+  const int lo = min(P, tid * per), hi = min(P, lo + per);
+  auto load4 = [&](int p, uint32_t (&kk)[4]) {
+    if (keys_in_smem && p + 4 <= hi) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(skeys + p);
+      kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) kk[e] = p + e < hi ? key_at(p + e) : 0u;
     }
-    gt_b += __popc(gtb);
-    eq_b += __popc(eqb);
+  };
+  uint32_t gt_n = 0, eq_n = 0;
+  for (int p = lo; p < hi; p += 4) {
+    uint32_t kk[4];
+    load4(p, kk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t k = kk[e] & pmask;
+      const bool in = p + e < hi;
+      gt_n += in && k > prefix;
+      eq_n += in && k == prefix;
+    }
+  }
+  uint32_t gi = gt_n, ei = eq_n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t tg = __shfl_up_sync(0xFFFFFFFFu, gi, off);
+    const uint32_t te = __shfl_up_sync(0xFFFFFFFFu, ei, off);
+    if (lane >= off) { gi += tg; ei += te; }
+  }
+  if (lane == 31) wsum[warp] = ((unsigned long long)ei << 32) | gi;
+  __syncthreads();
+  const unsigned long long t = lane < kTopkWarps ? wsum[lane] : 0ull;
+  const bool before = lane < warp;
+  int gt_b = (int)(__reduce_add_sync(0xFFFFFFFFu, before ? (uint32_t)t : 0u) + gi - gt_n);
+  int eq_b = (int)(__reduce_add_sync(0xFFFFFFFFu, before ? (uint32_t)(t >> 32) : 0u) + ei - eq_n);
+  for (int p = lo; p < hi; p += 4) {
+    uint32_t kk[4];
+    load4(p, kk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t k = kk[e] & pmask;
+      const bool in = p + e < hi;
+      const bool is_gt = in && k > prefix, is_eq = in && k == prefix;
+      if (is_gt || (is_eq && eq_b < krem)) {
+        const int pos = gt_b + min(eq_b, krem);
+        if (pos < K) orow[pos] = p + e;
+      }
+      gt_b += is_gt;
+      eq_b += is_eq;
+    }
   }
   for (int i = keff + tid; i < K; i += kTopkThreads) orow[i] = -1;
 }
@@ -159,18 +200,20 @@ __global__ void __launch_bounds__(kTopkThreads)
 // ---------------------------------------------------------------------------
 // union of the selected pages of the gc heads of one (b, kv head, head chunk)
 // ---------------------------------------------------------------------------
-// one CTA per group; 512 threads measured faster than 256 and 1024
-// (Llama-3.1-8B 32k attention call 44.5 -> 43.1 us)
+// One CTA per group: head bits per page by shared atomics, then each thread
+// owns a run of consecutive 4-page words, counts its union pages and, after
+// one block scan, writes them in page order.  512 threads (1024 measured the
+// same, 256 slower on 8192-page rows).
 constexpr int kUnionThreads = 512;
-constexpr int kUnionWarps = kUnionThreads / 32;
 
 __global__ void __launch_bounds__(kUnionThreads)
     union_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ ctx, int Hq, int G,
                  int gc, int ps, int maxP, int K, int umax, int32_t *__restrict__ upages,
                  uint32_t *__restrict__ umasks, int32_t *__restrict__ ucount, int *status) {
   pdl_wait();
+  constexpr int kUnionWarps = kUnionThreads / 32;
   extern __shared__ uint32_t words[];  // one byte of head bits per page, 4 pages a word
-  __shared__ unsigned long long wsum[kUnionWarps];
+  __shared__ uint32_t wsum[kUnionWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = blockIdx.x, b = blockIdx.y;
   const int nchunk = G / gc;
@@ -201,29 +244,42 @@ __global__ void __launch_bounds__(kUnionThreads)
   }
   __syncthreads();
   pdl_trigger();
-  // one contiguous segment of pages per warp, walked 32 pages at a time
-  const int seg = ((P + kUnionWarps - 1) / kUnionWarps + 31) / 32 * 32;
-  const int lo = warp * seg, hi = min(P, lo + seg);
-  unsigned long long n = 0;
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t m = p < hi ? (words[p >> 2] >> ((p & 3) * 8)) & 0xFFu : 0u;
-    n += __popc(__ballot_sync(0xFFFFFFFFu, m != 0u));
+  const int per = (nw + kUnionThreads - 1) / kUnionThreads;  // words per thread
+  const int lo = min(nw, tid * per), hi = min(nw, lo + per);
+  uint32_t n = 0;
+  for (int i = lo; i < hi; ++i) {
+    uint32_t t = words[i];
+    t |= t >> 4;
+    t |= t >> 2;
+    t |= t >> 1;
+    n += __popc(t & 0x01010101u);  // pages of the word some head selected
   }
-  unsigned long long tot;
-  unsigned long long pos = warp_bases64<kUnionWarps>(n, wsum, &tot);
-  for (int p0 = lo; p0 < hi; p0 += 32) {
-    const int p = p0 + lane;
-    const uint32_t m = p < hi ? (words[p >> 2] >> ((p & 3) * 8)) & 0xFFu : 0u;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, m != 0u);
-    const unsigned long long my = pos + __popc(bal & ((1u << lane) - 1u));
-    if (m != 0u && my < (unsigned long long)umax) {
-      upages[gbase * umax + my] = p;
-      umasks[gbase * umax + my] = m;
+  uint32_t ni = n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, ni, off);
+    if (lane >= off) ni += t;
+  }
+  if (lane == 31) wsum[warp] = ni;
+  __syncthreads();
+  const uint32_t ws = lane < kUnionWarps ? wsum[lane] : 0u;
+  uint32_t pos = __reduce_add_sync(0xFFFFFFFFu, lane < warp ? ws : 0u) + ni - n;
+  const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, ws);
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t w = words[i];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = (w >> (8 * e)) & 0xFFu;
+      if (m != 0u) {
+        if (pos < (uint32_t)umax) {
+          upages[gbase * umax + pos] = 4 * i + e;
+          umasks[gbase * umax + pos] = m;
+        }
+        ++pos;
+      }
     }
-    pos += __popc(bal);
   }
-  if (tid == 0) ucount[gbase] = (int)min(tot, (unsigned long long)umax);
+  if (tid == 0) ucount[gbase] = (int)min(tot, (uint32_t)umax);
 }
 
 // ---------------------------------------------------------------------------

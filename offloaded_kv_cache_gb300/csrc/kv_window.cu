@@ -12,10 +12,10 @@
 // [B*C][Hkv][ps][d]: slot s of group (b, kvh) is page b*C + s, kv head kvh,
 // so the attention kernel addresses the window exactly like a K/V cache.
 //   window_update_kernel  one CTA per group: need set, hits, lookahead
-//                         eviction, slot assignment, fetch list, stats;
-//   window_fetch_kernel   copies the fetch list's pages (K and V, the valid
-//                         tokens) from the (host) cache into their slots;
-// then the sparse attention runs over the window (page_slot override).
+//                         eviction, slot assignment, fetch bits, stats;
+// then the window instantiation of the sparse attention reads the hits from
+// the window and the fetched pages from the (host) cache, and stores each
+// fetched page's valid tokens into its slot as it goes.
 #include <algorithm>
 
 #include "kv_select.cuh"
@@ -24,6 +24,7 @@ namespace kvs {
 namespace {
 
 // one CTA per group and few groups: a wide CTA shortens every pass
+// (1024 threads measured faster than 512 and 256)
 constexpr int kWinThreads = 1024;
 constexpr int kWinWarps = kWinThreads / 32;
 
@@ -31,40 +32,54 @@ __device__ __forceinline__ uint32_t win_score_key(float s) {
   return key32(__float_as_uint(s + 0.0f));  // -0.0 ranks with +0.0
 }
 
+// Slot keys: a needed page's slot (a hit) 0, a free slot 1, else the eviction
+// candidate's key ~key(score), at least ~key(+inf) = 0x007FFFFF, so that the
+// largest keys are the lowest scores and hits and free slots never rank
+// among the candidates.
+constexpr uint32_t kSlotHit = 0u, kSlotFree = 1u;
+
+// Consecutive pages a thread owns in the page passes: 4, 8, 16 or 32 (so
+// that a fetch-bit word is shared by whole lanes), else a multiple of 32.
+__device__ __forceinline__ int page_run(int P) {
+  const int per = (P + kWinThreads - 1) / kWinThreads;
+  if (per <= 4) return 4;
+  if (per <= 32) return 1 << (32 - __clz(per - 1));
+  return (per + 31) & ~31;
+}
+
 // Dynamic shared memory: need[maxP] bytes (0 none, 1 miss, 2 hit), then
-// ekey[C] (eviction keys), then freed[C] (slots in ascending order).
+// skey[C] (slot keys), then aux[C] (each slot's page until the eviction,
+// then the freed slots in ascending order).
 __global__ void __launch_bounds__(kWinThreads)
     window_update_kernel(const int32_t *__restrict__ indices, const float *__restrict__ scores,
                          const int32_t *__restrict__ ctx, int Hq, int Hkv, int ps, int maxP,
                          int K, int C, int32_t *slot_page, int32_t *page_slot,
-                         int32_t *fetch_page, int32_t *fetch_slot, int32_t *fetch_count,
-                         int32_t *stats, int *status) {
+                         uint32_t *fetch_bits, int32_t *stats, int *status) {
   pdl_wait();
   extern __shared__ uint8_t wsm[];
   uint8_t *need = wsm;
-  uint32_t *ekey = reinterpret_cast<uint32_t *>(wsm + ((maxP + 15) & ~15));
-  int32_t *freed = reinterpret_cast<int32_t *>(ekey + C);
+  uint32_t *skey = reinterpret_cast<uint32_t *>(wsm + ((maxP + 15) & ~15));
+  int32_t *aux = reinterpret_cast<int32_t *>(skey + C);
   __shared__ RadixScratch sc;
-  __shared__ int s_hit, s_free, s_cand, s_need;
+  __shared__ uint32_t wred[9][kWinWarps];  // per-warp partials; row 8: the freed scan
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long g = blockIdx.x;
   const int b = (int)(g / Hkv), kvh = (int)(g % Hkv);
   const int G = Hq / Hkv;
   int32_t *sp = slot_page + g * C;
   int32_t *pslot = page_slot + g * maxP;
+  const int W = (maxP + 31) / 32;  // fetch-bit words per group
+  uint32_t *fbits = fetch_bits + g * W;
   const int len = ctx[b];
   if (len < 1 || len > maxP * ps) {
-    if (tid == 0) {
-      flag_error(status, KV_ERR_BOUNDS);
-      fetch_count[g] = 0;
-    }
+    if (tid == 0) flag_error(status, KV_ERR_BOUNDS);
+    for (int w = tid; w < W; w += kWinThreads) fbits[w] = 0u;
     return;
   }
   const int P = (len + ps - 1) / ps;
 
   // need set of the group's G query heads
   for (int i = tid; i < (maxP + 3) / 4; i += kWinThreads) reinterpret_cast<uint32_t *>(need)[i] = 0u;
-  if (tid == 0) s_hit = s_free = s_cand = s_need = 0;
   __syncthreads();
   for (int i = tid; i < G * K; i += kWinThreads) {
     const int p = indices[((long long)b * Hq + (long long)kvh * G) * K + i];
@@ -73,15 +88,16 @@ __global__ void __launch_bounds__(kWinThreads)
   __syncthreads();
 
   // classify the slots: free, hit (need -> 2), or an eviction candidate
-  // keyed by ~score so that the radix select's "largest" is the lowest score
-  int hit = 0, fre = 0, cand = 0;
+  uint32_t hit = 0, fre = 0, cand = 0, cmin = 0xFFFFFFFFu, cmax = 0u;
   for (int s = tid; s < C; s += kWinThreads) {
     const int p = sp[s];
-    uint32_t key = 0u;  // not a candidate: below every candidate's key
+    uint32_t key;
     if (p < 0 || p >= maxP) {
+      key = kSlotFree;
       ++fre;
     } else if (p < P && need[p]) {
       need[p] = 2;
+      key = kSlotHit;
       ++hit;
     } else {
       float m = -INFINITY;  // stale pages (at or past P) go first
@@ -91,162 +107,142 @@ __global__ void __launch_bounds__(kWinThreads)
       }
       key = ~win_score_key(m);
       ++cand;
+      cmin = min(cmin, key);
+      cmax = max(cmax, key);
     }
-    ekey[s] = key;
+    skey[s] = key;
+    aux[s] = p;
   }
-  if (hit) atomicAdd(&s_hit, hit);
-  if (fre) atomicAdd(&s_free, fre);
-  if (cand) atomicAdd(&s_cand, cand);
+  __syncthreads();  // need[] is final
+
+  // one pass over this thread's pages: needed, misses (scanned), fetches
+  const int per = page_run(P);
+  const int lo = min(P, tid * per), hi = min(P, lo + per);
+  uint32_t nn = 0, nm = 0, nf = 0;
+  for (int p = lo; p < hi; p += 4) {  // need[] is zero past P
+    const uint32_t w4 = *reinterpret_cast<const uint32_t *>(need + p);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t v = (w4 >> (8 * e)) & 255u;
+      nn += v != 0u;
+      nm += v == 1u;
+      nf += v == 1u || (v == 2u && p + e == P - 1);
+    }
+  }
+  uint32_t mi = nm;  // inclusive scan of the misses over the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, mi, off);
+    if (lane >= off) mi += t;
+  }
+  {
+    const uint32_t v0 = __reduce_add_sync(0xFFFFFFFFu, nn);
+    const uint32_t v1 = __reduce_add_sync(0xFFFFFFFFu, nf);
+    const uint32_t v2 = __reduce_add_sync(0xFFFFFFFFu, hit);
+    const uint32_t v3 = __reduce_add_sync(0xFFFFFFFFu, fre);
+    const uint32_t v4 = __reduce_add_sync(0xFFFFFFFFu, cand);
+    const uint32_t v5 = __reduce_min_sync(0xFFFFFFFFu, cmin);
+    const uint32_t v6 = __reduce_max_sync(0xFFFFFFFFu, cmax);
+    if (lane == 31) {
+      wred[0][warp] = mi;
+      wred[1][warp] = v0; wred[2][warp] = v1; wred[3][warp] = v2;
+      wred[4][warp] = v3; wred[5][warp] = v4; wred[6][warp] = v5; wred[7][warp] = v6;
+    }
+  }
   __syncthreads();
-  int nn = 0;
-  for (int p = tid; p < P; p += kWinThreads) nn += need[p] != 0;
-  if (nn) atomicAdd(&s_need, nn);
-  __syncthreads();
-  const int n_need = s_need, n_hit = s_hit, n_free = s_free, n_cand = s_cand;
+  const bool wl = lane < kWinWarps;
+  const uint32_t wmiss = wl ? wred[0][lane] : 0u;
+  int miss_b = (int)(__reduce_add_sync(0xFFFFFFFFu, lane < warp ? wmiss : 0u) + mi - nm);
+  const int n_need = (int)__reduce_add_sync(0xFFFFFFFFu, wl ? wred[1][lane] : 0u);
+  const int n_fetch = (int)__reduce_add_sync(0xFFFFFFFFu, wl ? wred[2][lane] : 0u);
+  const int n_hit = (int)__reduce_add_sync(0xFFFFFFFFu, wl ? wred[3][lane] : 0u);
+  const int n_free = (int)__reduce_add_sync(0xFFFFFFFFu, wl ? wred[4][lane] : 0u);
+  const int n_cand = (int)__reduce_add_sync(0xFFFFFFFFu, wl ? wred[5][lane] : 0u);
+  cmin = __reduce_min_sync(0xFFFFFFFFu, wl ? wred[6][lane] : 0xFFFFFFFFu);
+  cmax = __reduce_max_sync(0xFFFFFFFFu, wl ? wred[7][lane] : 0u);
   const int n_miss = n_need - n_hit;
   const int n_evict = max(0, n_miss - n_free);
   if (n_need > C || n_evict > n_cand) {  // the host checks C; never reached
-    if (tid == 0) {
-      flag_error(status, KV_ERR_BOUNDS);
-      fetch_count[g] = 0;
-    }
+    if (tid == 0) flag_error(status, KV_ERR_BOUNDS);
+    for (int w = tid; w < W; w += kWinThreads) fbits[w] = 0u;
     return;
   }
 
-  // lookahead eviction: the n_evict lowest-scored candidates, ties to the
-  // lower slot; their pages leave the map and their slots become free
-  auto key_at = [&](int s) -> uint32_t { return ekey[s]; };
+  // lookahead eviction: the n_evict lowest-scored candidates (the largest
+  // keys, all in [cmin, cmax]), ties to the lower slot; their pages leave
+  // the map and their slots become free
   if (n_evict > 0) {
-    const RadixSel sel = radix_select_top<kWinThreads>(key_at, C, n_evict, sc);
-    radix_emit<kWinThreads>(key_at, C, sel, sc, [&](long long, int s) {
-      pslot[sp[s]] = -1;
+    auto key_at = [&](int s) -> uint32_t { return skey[s]; };
+    const RadixSel sel = radix_select_top<kWinThreads>(key_at, C, n_evict, cmin, cmax, sc);
+    radix_emit<kWinThreads>(key_at, C, sel, sc, [&](int, int s) {
+      pslot[aux[s]] = -1;
       sp[s] = -1;
+      skey[s] = kSlotFree;
     });
     __syncthreads();
   }
   pdl_trigger();
 
-  // freed slots (free or evicted) in ascending order
+  // freed slots (free or evicted) in ascending order into aux[]
   {
-    const int seg = ((C + kWinWarps - 1) / kWinWarps + 31) / 32 * 32;
-    const int lo = warp * seg, hi = min(C, lo + seg);
-    unsigned long long cnt = 0;
-    for (int s0 = lo; s0 < hi; s0 += 32) {
-      const int s = s0 + lane;
-      cnt += __popc(__ballot_sync(0xFFFFFFFFu, s < hi && sp[s] < 0));
+    const int cper = (C + kWinThreads - 1) / kWinThreads;
+    const int clo = min(C, tid * cper), chi = min(C, clo + cper);
+    uint32_t nfr = 0;
+    for (int s = clo; s < chi; ++s) nfr += skey[s] == kSlotFree;
+    uint32_t fi = nfr;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, fi, off);
+      if (lane >= off) fi += t;
     }
-    unsigned long long tot;
-    unsigned long long pos = warp_bases64<kWinWarps>(cnt, sc.wsum, &tot);
-    for (int s0 = lo; s0 < hi; s0 += 32) {
-      const int s = s0 + lane;
-      const bool f = s < hi && sp[s] < 0;
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
-      if (f) freed[pos + __popc(bal & ((1u << lane) - 1u))] = s;
-      pos += __popc(bal);
-    }
+    if (lane == 31) wred[8][warp] = fi;
+    __syncthreads();
+    int pos = (int)(__reduce_add_sync(0xFFFFFFFFu, lane < warp && wl ? wred[8][lane] : 0u) + fi -
+                    nfr);
+    for (int s = clo; s < chi; ++s)
+      if (skey[s] == kSlotFree) aux[pos++] = s;
   }
   __syncthreads();
 
   // misses in ascending page order take the freed slots in ascending order;
-  // the fetch list holds the misses and a hit on the growing last page
+  // the fetch bits mark the misses and a hit on the growing last page (the
+  // attention reads those from the cache and refreshes their slots)
+  for (int w = (P + 31) / 32 + tid; w < W; w += kWinThreads) fbits[w] = 0u;
   {
-    const int seg = ((P + kWinWarps - 1) / kWinWarps + 31) / 32 * 32;
-    const int lo = warp * seg, hi = min(P, lo + seg);
-    unsigned long long cnt = 0;  // misses (low half), fetches (high half)
-    for (int p0 = lo; p0 < hi; p0 += 32) {
-      const int p = p0 + lane;
-      const int nd = p < hi ? need[p] : 0;
-      cnt += __popc(__ballot_sync(0xFFFFFFFFu, nd == 1));
-      cnt += (unsigned long long)__popc(
-                 __ballot_sync(0xFFFFFFFFu, nd == 1 || (nd == 2 && p == P - 1)))
-             << 32;
-    }
-    unsigned long long tot;
-    unsigned long long base = warp_bases64<kWinWarps>(cnt, sc.wsum, &tot);
-    long long mb = (long long)(base & 0xFFFFFFFFull), fb = (long long)(base >> 32);
-    const unsigned lt = (1u << lane) - 1u;
-    for (int p0 = lo; p0 < hi; p0 += 32) {
-      const int p = p0 + lane;
-      const int nd = p < hi ? need[p] : 0;
-      const bool miss = nd == 1, fetch = miss || (nd == 2 && p == P - 1);
-      const unsigned mbal = __ballot_sync(0xFFFFFFFFu, miss);
-      const unsigned fbal = __ballot_sync(0xFFFFFFFFu, fetch);
-      if (fetch) {
-        int slot;
-        if (miss) {
-          slot = freed[mb + __popc(mbal & lt)];
-          sp[slot] = p;
-          pslot[p] = slot;
-        } else {
-          slot = pslot[p];
+    const int plo = tid * per;  // unclipped: the fetch-bit word of this run
+    uint32_t bits = 0u;         // this run's fetch bits (per <= 32), or one word's
+    for (int p = lo; p < hi; p += 4) {
+      const uint32_t w4 = *reinterpret_cast<const uint32_t *>(need + p);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t v = (w4 >> (8 * e)) & 255u;
+        const int q = p + e;
+        if (v == 1u) {
+          const int slot = aux[miss_b++];
+          sp[slot] = q;
+          pslot[q] = slot;
         }
-        const long long f = fb + __popc(fbal & lt);
-        fetch_page[g * C + f] = p;
-        fetch_slot[g * C + f] = slot;
+        if (v == 1u || (v == 2u && q == P - 1)) bits |= 1u << (q & 31);
       }
-      mb += __popc(mbal);
-      fb += __popc(fbal);
-    }
-    if (tid == 0) {
-      fetch_count[g] = (int)(tot >> 32);
-      if (stats) {
-        stats[g * 4 + 0] = n_need;
-        stats[g * 4 + 1] = n_hit;
-        stats[g * 4 + 2] = (int)(tot >> 32);
-        stats[g * 4 + 3] = n_evict;
+      if (per > 32 && ((p + 4) & 31) == 0) {  // a run of whole words
+        fbits[(p >> 5)] = bits;
+        bits = 0u;
       }
     }
-  }
-}
-
-// Copies each fetch-list page of each group: the page's valid tokens of one
-// kv head, K then V, from the (host-mapped) cache into the window slot.  CTAs
-// stride over the entries of their group; each thread moves 16-byte chunks,
-// several loads in flight.
-template <int CH>  // 16-byte chunks per row
-__global__ void __launch_bounds__(256)
-    window_fetch_kernel(const uint4 *__restrict__ k_src, const uint4 *__restrict__ v_src,
-                        uint4 *__restrict__ k_win, uint4 *__restrict__ v_win,
-                        const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
-                        const int32_t *__restrict__ fetch_page,
-                        const int32_t *__restrict__ fetch_slot,
-                        const int32_t *__restrict__ fetch_count, int Hkv, int ps, int maxP,
-                        int C, long long nphys, int *status) {
-  pdl_wait();
-  const long long g = blockIdx.y;
-  const int b = (int)(g / Hkv), kvh = (int)(g % Hkv);
-  const int count = fetch_count[g];
-  const int len = ctx[b];
-  for (int e = blockIdx.x; e < count; e += gridDim.x) {
-    const int p = fetch_page[g * C + e];
-    const int slot = fetch_slot[g * C + e];
-    if (p < 0 || p * ps >= len || slot < 0 || slot >= C) {
-      if (threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
-      continue;
-    }
-    const long long phys = bt[(long long)b * maxP + p];
-    if (phys < 0 || phys >= nphys) {
-      if (threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
-      continue;
-    }
-    const int n = min(ps, len - p * ps) * CH;  // chunks of the valid rows
-    const long long src = (phys * Hkv + kvh) * ps * CH;
-    const long long dst = (((long long)b * C + slot) * Hkv + kvh) * ps * CH;
-    int i = threadIdx.x;
-    for (; i + 256 < n; i += 512) {
-      const uint4 k0 = k_src[src + i], k1 = k_src[src + i + 256];
-      const uint4 v0 = v_src[src + i], v1 = v_src[src + i + 256];
-      k_win[dst + i] = k0;
-      k_win[dst + i + 256] = k1;
-      v_win[dst + i] = v0;
-      v_win[dst + i + 256] = v1;
-    }
-    for (; i < n; i += 256) {
-      k_win[dst + i] = k_src[src + i];
-      v_win[dst + i] = v_src[src + i];
+    if (per <= 32) {
+      // the lanes of one word OR their bits; its first lane writes it
+      for (int off = 1; off < 32 / per; off <<= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, off);
+      if (plo < P && (plo & 31) == 0) fbits[plo >> 5] = bits;
+    } else if (hi > lo && (((hi + 3) & ~3) & 31) != 0) {
+      fbits[(hi - 1) >> 5] = bits;  // the run's last word, not yet written
     }
   }
-  pdl_trigger();
+  if (tid == 0 && stats) {
+    stats[g * 4 + 0] = n_need;
+    stats[g * 4 + 1] = n_hit;
+    stats[g * 4 + 2] = n_fetch;
+    stats[g * 4 + 3] = n_evict;
+  }
 }
 
 __global__ void fill_kernel(int32_t *p, long long n, int32_t v) {
@@ -264,9 +260,8 @@ size_t window_update_smem(int maxP, int C) {
 
 cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
                                  int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
-                                 int32_t *slot_page, int32_t *page_slot, int32_t *fetch_page,
-                                 int32_t *fetch_slot, int32_t *fetch_count, int32_t *stats,
-                                 int *status, cudaStream_t st) {
+                                 int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
+                                 int32_t *stats, int *status, cudaStream_t st) {
   const size_t smem = window_update_smem(maxP, C);
   static int attr_done[64] = {0};
   int dev = 0;
@@ -279,21 +274,7 @@ cudaError_t launch_window_update(const int32_t *indices, const float *scores, co
   }
   return launch_pdl(window_update_kernel, dim3((unsigned)((long long)B * Hkv)), dim3(kWinThreads),
                     smem, st, indices, scores, ctx, Hq, Hkv, ps, maxP, K, C, slot_page, page_slot,
-                    fetch_page, fetch_slot, fetch_count, stats, status);
-}
-
-cudaError_t launch_window_fetch(int dtype, const void *k_src, const void *v_src, void *k_win,
-                                void *v_win, const int32_t *bt, const int32_t *ctx,
-                                const int32_t *fetch_page, const int32_t *fetch_slot,
-                                const int32_t *fetch_count, int B, int Hkv, int ps, int maxP,
-                                int C, long long nphys, int blocks_per_group, int *status,
-                                cudaStream_t st) {
-  const dim3 grid((unsigned)blocks_per_group, (unsigned)((long long)B * Hkv));
-  auto kern = dtype == KV_F32 ? window_fetch_kernel<32> : window_fetch_kernel<16>;
-  return launch_pdl(kern, grid, dim3(256), 0, st, static_cast<const uint4 *>(k_src),
-                    static_cast<const uint4 *>(v_src), static_cast<uint4 *>(k_win),
-                    static_cast<uint4 *>(v_win), bt, ctx, fetch_page, fetch_slot, fetch_count,
-                    Hkv, ps, maxP, C, nphys, status);
+                    fetch_bits, stats, status);
 }
 
 cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st) {
