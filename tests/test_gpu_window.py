@@ -71,6 +71,8 @@ def _check_slots(layer, wl):
     ("f32", 2, 2, 16, "host", 8),     # fp32, C = 2 G K
     ("bf16", 16, 2, 16, "hbm", 48),   # G = 8, window in front of HBM K/V
     ("bf16", 8, 2, 128, "host", 20),  # 128-token pages
+    ("bf16", 32, 2, 16, "host", 80),  # G = 16: two head chunks fetch shared pages
+    ("f32", 8, 1, 32, "host", 40),    # fp32, G = 8: two chunks of 4 heads, 32-token pages
 ])
 def test_window_policy_and_output_match_oracle(dtype, hq, hkv, ps, kv_loc, C):
     K = 4
