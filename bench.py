@@ -408,6 +408,9 @@ def main():
     ap.add_argument("--window-steps", type=int, default=0,
                     help="profiling aid: run this many eager page-window decode steps "
                          "(x1 window, drifting queries) on the workload and exit")
+    ap.add_argument("--kernel-pass", type=int, default=0,
+                    help="profiling aid: run this many eager passes over every kernel of "
+                         "the path on the workload (no timing) and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -452,6 +455,41 @@ def main():
         assert kv.kv_device_status() == kv.KV_OK
         print(json.dumps({"window_steps": args.window_steps,
                           "last_step_stats": layer.win_stats.sum(dim=(0, 1)).tolist()}))
+        return 0
+
+    if args.kernel_pass > 0:  # profiling aid, no timing
+        # one pass, in this order: index build, page score, top-K, sparse
+        # attention (union, attention, combine), forced top-K, mean index build
+        # and score, page-window update and attention, dense attention, append
+        kn, vn = W.new_tokens(spec, 0)
+        kn = storage_to_torch(kn, spec.dtype).cuda()
+        vn = storage_to_torch(vn, spec.dtype).cuda()
+        ctx_last = (layer.context_lens - 1).contiguous()  # full rows: rewrite the last slot
+        if sparse:
+            layer.enable_window(spec.group * spec.topk)
+        for _ in range(args.kernel_pass):
+            layer.build_index()
+            if sparse:
+                layer.score()
+                layer.select()
+                layer.sparse_attn()
+                layer.select(sink_tokens=4, local_tokens=64)
+                layer.build_mean_index()
+                layer.score_mean()
+                layer.score()
+                layer.select()
+                layer.window_attn()
+            layer.dense_step()
+            kv.kv_append_token(layer.shape, kn, vn, layer.k_cache, layer.v_cache,
+                               layer.block_table, ctx_last, None, layer.minmax, stream)
+        torch.cuda.synchronize()
+        assert kv.kv_device_status() == kv.KV_OK
+        info = {"kernel_pass": args.kernel_pass, "workload": spec.name}
+        if sparse:
+            idx = layer.indices.cpu().numpy()
+            _, attn_b = sparse_bytes(spec, ctx, idx)
+            info["sparse_attention_bytes"] = int(attn_b)
+        print(json.dumps(info))
         return 0
 
     # index (built once per page; timed separately below)
