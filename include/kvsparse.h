@@ -261,12 +261,15 @@ int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink
  * host memory, the path runs (k > 0: kv_page_score, kv_topk_select,
  * kv_sparse_decode_attn; k == 0: kv_dense_decode_attn) and out lands in host
  * memory, all asynchronous on `stream`.  A host buffer the device has mapped
- * (cudaHostAlloc, or pinned and registered) is used in place: the kernels
- * read q and the lengths and write out across the host link, the zero-copy
- * access DirectKV applies to K/V (core method 1).  Any other host buffer is
- * copied through the matching device buffer with cudaMemcpyAsync (q,
- * context_lens, out may then be NULL only for mapped buffers).  The same
- * outputs as the separate calls.  The index (minmax) must be built. */
+ * (cudaHostAlloc, or pinned and registered) is accessed across the host
+ * link, the zero-copy access DirectKV applies to K/V (core method 1): out is
+ * written in place; for a sparse step (k > 0), mapped q and lengths are read
+ * once by a staging kernel into the device buffers q and context_lens when
+ * those are given, else (and for a dense step) the kernels read them in
+ * place.  Any other host buffer is copied through the matching device buffer
+ * with cudaMemcpyAsync (q, context_lens, out may be NULL only for mapped
+ * buffers).  The same outputs as the separate calls.  The index (minmax) must
+ * be built. */
 typedef struct {
   const void *q_host;               /* [B][Hq][d] dtype, host                  */
   const int32_t *context_lens_host; /* [B], host                               */

@@ -723,16 +723,31 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
   if (io->k > 0 && (!io->minmax || !io->scores || !io->indices)) return KV_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)shape->batch * shape->num_q_heads;
-  // Host buffers the device has mapped are used in place (zero-copy: the
-  // kernels read q and the lengths and write out across the host link, as
-  // the pages read K/V); others are copied through the device buffers.
+  // Host buffers the device has mapped are read (q, lengths) and written
+  // (out) across the host link, as the pages read K/V; others are copied
+  // through the device buffers.  For a sparse step, mapped q and lengths are
+  // first staged into the device buffers by one kernel whose host reads
+  // overlap the previous kernel, so the score, top-K, union and attention
+  // kernels each read device memory instead of paying a host round trip
+  // (Llama-3.1-8B 32k step 61.3 -> 59.5 us).  A dense step is one attention
+  // kernel that already reads q before its PDL wait: it reads them in place.
   const void *q = mapped_host(io->q_host);
   const int32_t *ctx = static_cast<const int32_t *>(mapped_host(io->context_lens_host));
   float *out = static_cast<float *>(mapped_host(io->out_host));
+  const size_t q_bytes = rows * kHeadDim * elem_bytes(shape->dtype);
+  if (io->k > 0 && q && ctx && io->q && io->context_lens && al16(q) && al16(io->q) &&
+      al4(io->context_lens)) {
+    if (launch_stage_inputs(q, io->q, q_bytes, ctx, io->context_lens, shape->batch, st) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return KV_ERR_CUDA;
+    }
+    q = io->q;
+    ctx = io->context_lens;
+  }
   if (!q) {
     if (!al16(io->q)) return KV_ERR_INVALID_ARG;
-    if (cudaMemcpyAsync(io->q, io->q_host, rows * kHeadDim * elem_bytes(shape->dtype),
-                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    if (cudaMemcpyAsync(io->q, io->q_host, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
       cudaGetLastError();
       return KV_ERR_CUDA;
     }

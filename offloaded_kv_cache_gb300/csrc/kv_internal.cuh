@@ -278,6 +278,10 @@ cudaError_t launch_window_update(const int32_t *indices, const float *scores, co
                                  int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
                                  int32_t *stats, int *status, cudaStream_t st);
 cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
+// one decode step's q and context lengths, mapped host -> device buffers
+cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
+                                const int32_t *ctx_src, int32_t *ctx_dst, int B,
+                                cudaStream_t st);
 cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
                               const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
                               int Hkv, int ps, int maxP, long long nphys, int *status,

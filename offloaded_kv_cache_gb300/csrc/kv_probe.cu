@@ -1,10 +1,15 @@
-// kv_probe.cu -- streaming-read bandwidth probe: the denominator of the
-// roofline for K/V that the GPU reads in place from pinned host memory.
+// kv_probe.cu -- reads across the host link that are not K/V:
+//  * the streaming-read bandwidth probe, the denominator of the roofline for
+//    K/V that the GPU reads in place from pinned host memory;
+//  * the staging of one decode step's inputs (q, context lengths) from mapped
+//    host memory into device buffers.
 //
 // DirectKV (No Buffer, No Bottleneck: Efficient Zero-Copy KV Cache Offloading
 // for Long-Context LLMs), observation 4: long-context access through the
 // host link is bound by its sustained bandwidth, so that bandwidth, measured,
 // is what host-resident attention is compared against.
+#include <algorithm>
+
 #include "kv_internal.cuh"
 
 namespace kvs {
@@ -42,7 +47,53 @@ __global__ void __launch_bounds__(512)
   }
 }
 
+// One decode step's inputs, mapped host -> device: each thread loads its
+// context lengths and 16-byte chunks of q from host memory before waiting
+// for the previous kernel in the stream (the host wrote them before the
+// call), so the host-link latency overlaps that kernel's tail; after the wait
+// (the previous step may still read the device copies) it stores them.  It
+// never releases its dependents early: the next kernels may read q before
+// their own wait, so they must start only once these stores are complete
+// and visible, which the end of this grid guarantees.
+constexpr int kStageThreads = 256;
+constexpr int kStageChunks = 4;  // 16-byte chunks of q per thread
+__global__ void __launch_bounds__(kStageThreads)
+    stage_inputs_kernel(const uint4 *__restrict__ q_src, uint4 *__restrict__ q_dst, long long n16,
+                        const int32_t *__restrict__ ctx_src, int32_t *__restrict__ ctx_dst,
+                        int B) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nt = (long long)gridDim.x * blockDim.x;
+  uint4 v[kStageChunks];
+#pragma unroll
+  for (int c = 0; c < kStageChunks; ++c) {
+    const long long i = t + c * nt;
+    if (i < n16) v[c] = q_src[i];
+  }
+  int32_t len = 0;
+  if (t < B) len = ctx_src[t];
+  pdl_wait();
+#pragma unroll
+  for (int c = 0; c < kStageChunks; ++c) {
+    const long long i = t + c * nt;
+    if (i < n16) q_dst[i] = v[c];
+  }
+  if (t < B) ctx_dst[t] = len;
+}
+
 }  // namespace
+
+cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
+                                const int32_t *ctx_src, int32_t *ctx_dst, int B,
+                                cudaStream_t st) {
+  const long long n16 = (long long)(q_bytes / 16);
+  const long long per_cta = (long long)kStageThreads * kStageChunks;
+  long long blocks = (n16 + per_cta - 1) / per_cta;
+  blocks = std::max(blocks, ((long long)B + kStageThreads - 1) / kStageThreads);
+  blocks = std::max(blocks, 1LL);
+  return launch_pdl(stage_inputs_kernel, dim3((unsigned)blocks), dim3(kStageThreads), 0, st,
+                    static_cast<const uint4 *>(q_src), static_cast<uint4 *>(q_dst), n16, ctx_src,
+                    ctx_dst, B);
+}
 }  // namespace kvs
 
 extern "C" int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,

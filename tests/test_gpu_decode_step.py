@@ -37,15 +37,17 @@ def test_host_step_equals_separate_calls_and_oracle(dtype, sparse, kv_loc, pinne
     q_host = storage_to_torch(q2, dtype).clone()
     ctx_host = torch.from_numpy(ctx2).clone()
     out_host = torch.full(layer.out.shape, np.nan, dtype=torch.float32)
-    if pinned:      # mapped: the kernels use the host buffers in place
+    if pinned:      # mapped: staged by one kernel into the device buffers, out in place
         q_host, ctx_host, out_host = q_host.pin_memory(), ctx_host.pin_memory(), out_host.pin_memory()
-    q_before = layer.q.cpu().clone()
     layer.host_step(layer.host_io(q_host, ctx_host, out_host, sparse))
     torch.cuda.synchronize()
     assert kv.kv_device_status() == kv.KV_OK
     got = out_host.numpy().copy()
-    # in place: the device buffers were not used; copied: they hold the inputs
-    assert torch.equal(layer.q.cpu(), q_before if pinned else q_host)
+    # copied, or staged (a sparse step on mapped buffers): the device buffers
+    # hold this step's inputs; a dense step on mapped buffers reads them in place
+    if sparse or not pinned:
+        assert torch.equal(layer.q.cpu(), q_host)
+        assert torch.equal(layer.context_lens.cpu(), ctx_host)
     # the separate calls on the same inputs give the same bits
     layer.q.copy_(q_host)
     layer.context_lens.copy_(ctx_host)
@@ -68,6 +70,33 @@ def test_host_step_equals_separate_calls_and_oracle(dtype, sparse, kv_loc, pinne
     else:
         ref = oracle.attention(dtype, q2, wl.k_cache, wl.v_cache, wl.block_table, ctx2, wl.scale)
         assert np.abs(got - ref).max() <= ATOL[dtype]
+
+
+@pytest.mark.parametrize("sparse", [True, False])
+def test_host_step_in_place_without_device_buffers(sparse):
+    # mapped q and lengths with no device copies given: the kernels read them
+    # in place across the host link; the same bits as the staged step
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=2, context=16 * 9 + 3, ps=16, topk=3,
+                       index=132)
+    wl = W.generate(spec, context_lens=[16 * 9 + 3, 16 * 4])
+    layer = DecodeLayer(wl, topk=3)
+    layer.build_index()
+    q2 = W.drifting_queries(spec, wl.q, 1, 0.5)[0]
+    q_host = storage_to_torch(q2, "bf16").clone().pin_memory()
+    ctx_host = torch.from_numpy(wl.context_lens.astype(np.int32)).clone().pin_memory()
+    outs = []
+    for staged in (True, False):
+        out_host = torch.full(layer.out.shape, np.nan, dtype=torch.float32).pin_memory()
+        io = layer.host_io(q_host, ctx_host, out_host, sparse)
+        if not staged:
+            io.q = None
+            io.context_lens = None
+        layer.host_step(io)
+        torch.cuda.synchronize()
+        assert kv.kv_device_status() == kv.KV_OK
+        outs.append(out_host.numpy().copy())
+    assert not np.isnan(outs[1]).any()
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_host_step_rejects_missing_sparse_buffers():
