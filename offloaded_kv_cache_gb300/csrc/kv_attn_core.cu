@@ -2,6 +2,7 @@
 // kernel: fp32 data, and 16-bit data whose GQA group is too small (1 or 2
 // query heads per CTA) for a tokens x heads tile to be a real contraction.
 #include "kv_attn.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 

@@ -2,6 +2,7 @@
 // kernel: 16-bit data with 4 or 8 query heads per CTA, where q . K^T over a
 // 16-token tile and V^T . P^T are dense tokens x heads contractions.
 #include "kv_attn.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 

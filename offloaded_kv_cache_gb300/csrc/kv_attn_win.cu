@@ -5,6 +5,7 @@
 // instantiations: tensor cores for 16-bit data with 4 or 8 heads per CTA,
 // CUDA cores otherwise.
 #include "kv_attn.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 

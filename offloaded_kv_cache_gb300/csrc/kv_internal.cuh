@@ -264,49 +264,4 @@ constexpr int kMaxStages = 16;
 // page to fetch in the window instantiations.
 __host__ __device__ constexpr int attn_entry_bytes(bool win) { return win ? 16 : 8; }
 
-// launchers (return a cudaError_t)
-cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
-                                void *minmax, int B, int Hkv, int ps, int maxP, long long nphys,
-                                int *status, cudaStream_t st);
-cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void *k_cache,
-                          void *v_cache, const int32_t *bt, const int32_t *ctx,
-                          int32_t *ctx_out, void *minmax, int B, int Hkv, int ps, int maxP,
-                          long long nphys, int *status, cudaStream_t st);
-size_t window_update_smem(int maxP, int C);
-cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
-                                 int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
-                                 int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
-                                 int32_t *stats, int *status, cudaStream_t st);
-cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
-// one decode step's q and context lengths, mapped host -> device buffers
-cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
-                                const int32_t *ctx_src, int32_t *ctx_dst, int B,
-                                cudaStream_t st);
-cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
-                              const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
-                              int Hkv, int ps, int maxP, long long nphys, int *status,
-                              cudaStream_t st);
-cudaError_t launch_mean_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
-                              void *mean, int B, int Hkv, int ps, int maxP, long long nphys,
-                              bool last_only, int *status, cudaStream_t st);
-cudaError_t launch_topk(const float *scores, const int32_t *ctx, int B, int Hq, int ps, int maxP,
-                        int k, int sink_tokens, int local_tokens, int32_t *indices, int *status,
-                        cudaStream_t st);
-cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int Hq, int Hkv,
-                         int gc, int ps, int maxP, int k, int umax, int32_t *upages,
-                         uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st);
-cudaError_t launch_attn_core(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
-                             const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
-cudaError_t launch_attn_mma(int dtype, int gc, const AttnArgs &a, const CUtensorMap *tk,
-                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
-// the window instantiations: attention that also fetches the step's misses
-cudaError_t launch_attn_win(int dtype, int gc, bool mma, const AttnArgs &a, const CUtensorMap *tk,
-                            const CUtensorMap *tv, dim3 grid, size_t smem, cudaStream_t st);
-// resident attention CTAs per SM for a launch shape (0 when unknown)
-int attn_occupancy_core(int dtype, int gc, int threads, size_t smem);
-int attn_occupancy_mma(int dtype, int gc, int threads, size_t smem);
-int attn_occupancy_win(int dtype, int gc, bool mma, int threads, size_t smem);
-cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
-                           int Hq, cudaStream_t st);
-
 }  // namespace kvs

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "kv_internal.cuh"
+#include "kv_launch.h"
 
 namespace {
 

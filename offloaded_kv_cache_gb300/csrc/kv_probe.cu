@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "kv_internal.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 namespace {

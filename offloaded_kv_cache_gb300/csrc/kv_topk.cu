@@ -6,6 +6,7 @@
 // blocks are retrieved.  Ties go to the lower page index; pages come out
 // ascending.
 #include "kv_internal.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 namespace {

@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "kv_select.cuh"
+#include "kv_launch.h"
 
 namespace kvs {
 namespace {
