@@ -451,17 +451,11 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   uint32_t *fbits = nullptr;
   const void *src_k = kd, *src_v = vd;
   if (wc) {
-    // the window step: update the state and mark this step's fetches; the
-    // attention below reads the window, and the fetched pages from the cache
+    // the attention below reads the window, and this step's fetched pages
+    // from the cache
     fbits = reinterpret_cast<uint32_t *>(w + pl.total);
-    const kv_window *win = wc->win;
-    cudaError_t e = launch_window_update(indices, wc->scores, ctx, s->batch, s->num_q_heads,
-                                         s->num_kv_heads, s->page_size, s->max_pages_per_seq, k,
-                                         C, win->slot_page, win->page_slot, fbits, win->stats,
-                                         status, st);
-    if (e != cudaSuccess) return KV_ERR_CUDA;
-    kd = win->cache_k;
-    vd = win->cache_v;
+    kd = wc->win->cache_k;
+    vd = wc->win->cache_v;
   }
 
   AttnArgs a{};
@@ -505,11 +499,23 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
     a.union_masks = reinterpret_cast<uint32_t *>(w + pl.off_umasks);
     a.union_count = reinterpret_cast<int32_t *>(w + pl.off_ucount);
     a.umax = pl.umax;
-    cudaError_t e = launch_union(indices, ctx, s->batch, s->num_q_heads, s->num_kv_heads, pl.gc,
-                                 s->page_size, s->max_pages_per_seq, k, pl.umax,
-                                 const_cast<int32_t *>(a.union_pages),
-                                 const_cast<uint32_t *>(a.union_masks),
-                                 const_cast<int32_t *>(a.union_count), status, st);
+    cudaError_t e;
+    if (wc) {
+      // the window step: update the state and mark this step's fetches, and,
+      // in the same launch beside it, build the union lists
+      const kv_window *win = wc->win;
+      e = launch_window_step(indices, wc->scores, ctx, s->batch, s->num_q_heads, s->num_kv_heads,
+                             s->page_size, s->max_pages_per_seq, k, C, win->slot_page,
+                             win->page_slot, fbits, win->stats, pl.gc, pl.umax,
+                             const_cast<int32_t *>(a.union_pages),
+                             const_cast<uint32_t *>(a.union_masks),
+                             const_cast<int32_t *>(a.union_count), status, st);
+    } else {
+      e = launch_union(indices, ctx, s->batch, s->num_q_heads, s->num_kv_heads, pl.gc,
+                       s->page_size, s->max_pages_per_seq, k, pl.umax,
+                       const_cast<int32_t *>(a.union_pages), const_cast<uint32_t *>(a.union_masks),
+                       const_cast<int32_t *>(a.union_count), status, st);
+    }
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
   CUtensorMap tk, tv;

@@ -15,10 +15,12 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new, void 
                           int32_t *ctx_out, void *minmax, int B, int Hkv, int ps, int maxP,
                           long long nphys, int *status, cudaStream_t st);
 size_t window_update_smem(int maxP, int C);
-cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
-                                 int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
-                                 int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
-                                 int32_t *stats, int *status, cudaStream_t st);
+// the window update and, beside it in the same launch, the union lists
+cudaError_t launch_window_step(const int32_t *indices, const float *scores, const int32_t *ctx,
+                               int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
+                               int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
+                               int32_t *stats, int gc, int umax, int32_t *upages,
+                               uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st);
 cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
 // one decode step's q and context lengths, mapped host -> device buffers
 cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,

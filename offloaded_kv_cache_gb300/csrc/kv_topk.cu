@@ -7,6 +7,7 @@
 // ascending.
 #include "kv_internal.cuh"
 #include "kv_launch.h"
+#include "kv_union.cuh"
 
 namespace kvs {
 namespace {
@@ -201,10 +202,8 @@ __global__ void __launch_bounds__(kTopkThreads)
 // ---------------------------------------------------------------------------
 // union of the selected pages of the gc heads of one (b, kv head, head chunk)
 // ---------------------------------------------------------------------------
-// One CTA per group: head bits per page by shared atomics, then each thread
-// owns a run of consecutive 4-page words, counts its union pages and, after
-// one block scan, writes them in page order.  512 threads (1024 measured the
-// same, 256 slower on 8192-page rows).
+// One CTA per group runs union_group (kv_union.cuh).  512 threads (1024
+// measured the same, 256 slower on 8192-page rows).
 constexpr int kUnionThreads = 512;
 
 __global__ void __launch_bounds__(kUnionThreads)
@@ -212,75 +211,10 @@ __global__ void __launch_bounds__(kUnionThreads)
                  int gc, int ps, int maxP, int K, int umax, int32_t *__restrict__ upages,
                  uint32_t *__restrict__ umasks, int32_t *__restrict__ ucount, int *status) {
   pdl_wait();
-  constexpr int kUnionWarps = kUnionThreads / 32;
   extern __shared__ uint32_t words[];  // one byte of head bits per page, 4 pages a word
-  __shared__ uint32_t wsum[kUnionWarps];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int grp = blockIdx.x, b = blockIdx.y;
-  const int nchunk = G / gc;
-  const int kvh = grp / nchunk, chunk = grp % nchunk;
-  const int head0 = kvh * G + chunk * gc;
-  const long long gbase = ((long long)b * gridDim.x + grp);
-  const int len = ctx[b];
-  if (len < 1 || len > maxP * ps) {
-    if (tid == 0) {
-      flag_error(status, KV_ERR_BOUNDS);
-      ucount[gbase] = 0;
-    }
-    return;
-  }
-  const int P = (len + ps - 1) / ps;
-  const int nw = (P + 3) / 4;
-  for (int i = tid; i < nw; i += kUnionThreads) words[i] = 0u;
-  __syncthreads();
-  for (int i = tid; i < gc * K; i += kUnionThreads) {
-    const int g = i / K, j = i % K;
-    const int p = idx[((long long)b * Hq + head0 + g) * K + j];
-    if (p < 0) continue;
-    if (p >= P) {
-      flag_error(status, KV_ERR_BOUNDS);
-      continue;
-    }
-    atomicOr(&words[p >> 2], (1u << g) << ((p & 3) * 8));
-  }
-  __syncthreads();
-  pdl_trigger();
-  const int per = (nw + kUnionThreads - 1) / kUnionThreads;  // words per thread
-  const int lo = min(nw, tid * per), hi = min(nw, lo + per);
-  uint32_t n = 0;
-  for (int i = lo; i < hi; ++i) {
-    uint32_t t = words[i];
-    t |= t >> 4;
-    t |= t >> 2;
-    t |= t >> 1;
-    n += __popc(t & 0x01010101u);  // pages of the word some head selected
-  }
-  uint32_t ni = n;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, ni, off);
-    if (lane >= off) ni += t;
-  }
-  if (lane == 31) wsum[warp] = ni;
-  __syncthreads();
-  const uint32_t ws = lane < kUnionWarps ? wsum[lane] : 0u;
-  uint32_t pos = __reduce_add_sync(0xFFFFFFFFu, lane < warp ? ws : 0u) + ni - n;
-  const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, ws);
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t w = words[i];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t m = (w >> (8 * e)) & 0xFFu;
-      if (m != 0u) {
-        if (pos < (uint32_t)umax) {
-          upages[gbase * umax + pos] = 4 * i + e;
-          umasks[gbase * umax + pos] = m;
-        }
-        ++pos;
-      }
-    }
-  }
-  if (tid == 0) ucount[gbase] = (int)min(tot, (uint32_t)umax);
+  __shared__ uint32_t wsum[kUnionThreads / 32];
+  union_group<kUnionThreads>(idx, ctx, Hq, G, gc, ps, maxP, K, umax, upages, umasks, ucount,
+                             status, blockIdx.x, blockIdx.y, gridDim.x, words, wsum);
 }
 
 // ---------------------------------------------------------------------------

@@ -11,8 +11,10 @@
 // One group per (sequence b, kv head) owns C slots of the cache arrays
 // [B*C][Hkv][ps][d]: slot s of group (b, kvh) is page b*C + s, kv head kvh,
 // so the attention kernel addresses the window exactly like a K/V cache.
-//   window_update_kernel  one CTA per group: need set, hits, lookahead
-//                         eviction, slot assignment, fetch bits, stats;
+//   window_step_kernel  one CTA per group: need set, hits, lookahead
+//                       eviction, slot assignment, fetch bits, stats; and,
+//                       in the same launch, one CTA per head chunk building
+//                       the attention's union lists;
 // then the window instantiation of the sparse attention reads the hits from
 // the window and the fetched pages from the (host) cache, and stores each
 // fetched page's valid tokens into its slot as it goes.
@@ -20,6 +22,7 @@
 
 #include "kv_select.cuh"
 #include "kv_launch.h"
+#include "kv_union.cuh"
 
 namespace kvs {
 namespace {
@@ -48,23 +51,23 @@ __device__ __forceinline__ int page_run(int P) {
   return (per + 31) & ~31;
 }
 
-// Dynamic shared memory: need[maxP] bytes (0 none, 1 miss, 2 hit), then
-// skey[C] (slot keys), then aux[C] (each slot's page until the eviction,
-// then the freed slots in ascending order).
-__global__ void __launch_bounds__(kWinThreads)
-    window_update_kernel(const int32_t *__restrict__ indices, const float *__restrict__ scores,
-                         const int32_t *__restrict__ ctx, int Hq, int Hkv, int ps, int maxP,
-                         int K, int C, int32_t *slot_page, int32_t *page_slot,
-                         uint32_t *fetch_bits, int32_t *stats, int *status) {
-  pdl_wait();
-  extern __shared__ uint8_t wsm[];
+// The window update of group g = (b, kv head), one CTA.  Shared memory at
+// wsm: need[maxP] bytes (0 none, 1 miss, 2 hit), then skey[C] (slot keys),
+// then aux[C] (each slot's page until the eviction, then the freed slots in
+// ascending order).
+__device__ __forceinline__ void update_group(const int32_t *__restrict__ indices,
+                                             const float *__restrict__ scores,
+                                             const int32_t *__restrict__ ctx, int Hq, int Hkv,
+                                             int ps, int maxP, int K, int C, int32_t *slot_page,
+                                             int32_t *page_slot, uint32_t *fetch_bits,
+                                             int32_t *stats, int *status, long long g,
+                                             uint8_t *wsm) {
   uint8_t *need = wsm;
   uint32_t *skey = reinterpret_cast<uint32_t *>(wsm + ((maxP + 15) & ~15));
   int32_t *aux = reinterpret_cast<int32_t *>(skey + C);
   __shared__ RadixScratch sc;
   __shared__ uint32_t wred[9][kWinWarps];  // per-warp partials; row 8: the freed scan
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long g = blockIdx.x;
   const int b = (int)(g / Hkv), kvh = (int)(g % Hkv);
   const int G = Hq / Hkv;
   int32_t *sp = slot_page + g * C;
@@ -246,6 +249,31 @@ __global__ void __launch_bounds__(kWinThreads)
   }
 }
 
+// One launch, two roles: CTAs [0, n_update) run the window update of group
+// blockIdx.x; the others build the union lists of the attention's head
+// chunks (u = blockIdx.x - n_update: sequence u / groups, chunk group
+// u % groups).  Both only read the selection and they write disjoint
+// outputs, so they run side by side instead of one after the other.
+__global__ void __launch_bounds__(kWinThreads)
+    window_step_kernel(const int32_t *__restrict__ indices, const float *__restrict__ scores,
+                       const int32_t *__restrict__ ctx, int Hq, int Hkv, int ps, int maxP, int K,
+                       int C, int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
+                       int32_t *stats, int *status, int n_update, int G, int gc, int umax,
+                       int groups, int32_t *upages, uint32_t *umasks, int32_t *ucount) {
+  pdl_wait();
+  extern __shared__ uint8_t wsm[];
+  if ((int)blockIdx.x < n_update) {
+    update_group(indices, scores, ctx, Hq, Hkv, ps, maxP, K, C, slot_page, page_slot, fetch_bits,
+                 stats, status, (long long)blockIdx.x, wsm);
+  } else {
+    __shared__ uint32_t uwsum[kWinWarps];
+    const int u = (int)blockIdx.x - n_update;
+    union_group<kWinThreads>(indices, ctx, Hq, G, gc, ps, maxP, K, umax, upages, umasks, ucount,
+                             status, u % groups, u / groups, groups,
+                             reinterpret_cast<uint32_t *>(wsm), uwsum);
+  }
+}
+
 __global__ void fill_kernel(int32_t *p, long long n, int32_t v) {
   pdl_wait();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -259,23 +287,28 @@ size_t window_update_smem(int maxP, int C) {
   return (size_t)((maxP + 15) & ~15) + (size_t)C * 8;
 }
 
-cudaError_t launch_window_update(const int32_t *indices, const float *scores, const int32_t *ctx,
-                                 int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
-                                 int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
-                                 int32_t *stats, int *status, cudaStream_t st) {
-  const size_t smem = window_update_smem(maxP, C);
+cudaError_t launch_window_step(const int32_t *indices, const float *scores, const int32_t *ctx,
+                               int B, int Hq, int Hkv, int ps, int maxP, int K, int C,
+                               int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
+                               int32_t *stats, int gc, int umax, int32_t *upages,
+                               uint32_t *umasks, int32_t *ucount, int *status, cudaStream_t st) {
+  const size_t smem = std::max(window_update_smem(maxP, C), (size_t)((maxP + 3) / 4) * 4);
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || !attr_done[dev])) {
-    cudaError_t e = cudaFuncSetAttribute(window_update_kernel,
+    cudaError_t e = cudaFuncSetAttribute(window_step_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  return launch_pdl(window_update_kernel, dim3((unsigned)((long long)B * Hkv)), dim3(kWinThreads),
-                    smem, st, indices, scores, ctx, Hq, Hkv, ps, maxP, K, C, slot_page, page_slot,
-                    fetch_bits, stats, status);
+  const int G = Hq / Hkv;
+  const int groups = Hkv * (G / gc);
+  const int n_update = B * Hkv;
+  const unsigned blocks = (unsigned)(n_update + B * groups);
+  return launch_pdl(window_step_kernel, dim3(blocks), dim3(kWinThreads), smem, st, indices,
+                    scores, ctx, Hq, Hkv, ps, maxP, K, C, slot_page, page_slot, fetch_bits, stats,
+                    status, n_update, G, gc, umax, groups, upages, umasks, ucount);
 }
 
 cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st) {
