@@ -28,7 +28,7 @@ namespace {
 // is large enough.
 template <class T>
 __global__ void __launch_bounds__(1024)
-    append_kernel(const T *__restrict__ k_new, const T *__restrict__ v_new, T *k_cache,
+    append_kernel(const T *k_new, const T *v_new, T *k_cache,
                   T *v_cache, const int32_t *bt, const int32_t *ctx, int32_t *ctx_out, T *mm,
                   int Hkv, int ps, int maxP, long long nphys, int *status) {
   pdl_wait();

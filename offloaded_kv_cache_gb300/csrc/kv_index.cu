@@ -25,8 +25,8 @@ namespace {
 // exact and does not depend on the order of the reduction (-0.0 < +0.0).
 template <class T>
 __global__ void __launch_bounds__(256)
-    minmax_build_kernel(const T *__restrict__ k, const int32_t *__restrict__ bt,
-                        const int32_t *__restrict__ ctx, T *__restrict__ mm, int B, int Hkv,
+    minmax_build_kernel(const T *k, const int32_t *bt,
+                        const int32_t *ctx, T *mm, int B, int Hkv,
                         int ps, int maxP, long long nphys, int *status) {
   pdl_wait();
   constexpr int C = kHeadDim * (int)sizeof(T) / 16;  // 16-byte chunks per row
@@ -140,9 +140,9 @@ constexpr int kScorePagesPerWarp = 8;
 // MEAN: the table row is the page's mean key and the score is q . mean.
 template <class T, int GS, bool MEAN>
 __global__ void __launch_bounds__(32 * kScoreWarps)
-    page_score_kernel(const T *__restrict__ q, const T *__restrict__ mm,
-                      const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
-                      float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
+    page_score_kernel(const T *q, const T *mm,
+                      const int32_t *bt, const int32_t *ctx,
+                      float *scores, int Hq, int Hkv, int ps, int maxP,
                       long long nphys, int nchunk, int *status) {
   pdl_wait();
   constexpr int PPW = kScorePagesPerWarp;
@@ -265,9 +265,9 @@ constexpr int kScoreMmaWarps = 8;
 // coefficients (4 chunks per lane instead of 8).
 template <class T, int GS, bool MEAN>
 __global__ void __launch_bounds__(32 * kScoreMmaWarps)
-    page_score_mma_kernel(const T *__restrict__ q, const T *__restrict__ mm,
-                          const int32_t *__restrict__ bt, const int32_t *__restrict__ ctx,
-                          float *__restrict__ scores, int Hq, int Hkv, int ps, int maxP,
+    page_score_mma_kernel(const T *q, const T *mm,
+                          const int32_t *bt, const int32_t *ctx,
+                          float *scores, int Hq, int Hkv, int ps, int maxP,
                           long long nphys, int nchunk, int *status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -467,8 +467,8 @@ __device__ __forceinline__ void store_mean(T *dst, const float (&s)[16 / sizeof(
 
 template <class T>
 __global__ void __launch_bounds__(256)
-    mean_build_kernel(const T *__restrict__ k, const int32_t *__restrict__ bt,
-                      const int32_t *__restrict__ ctx, T *__restrict__ mean, int B, int Hkv,
+    mean_build_kernel(const T *k, const int32_t *bt,
+                      const int32_t *ctx, T *mean, int B, int Hkv,
                       int ps, int maxP, long long nphys, int last_only, int *status) {
   pdl_wait();
   constexpr int C = kHeadDim * (int)sizeof(T) / 16;  // 16-byte chunks per row

@@ -82,11 +82,15 @@ __device__ __forceinline__ float ex2(float x) {
 // ---------------------------------------------------------------------------
 // programmatic dependent launch.  Every kernel of the path waits for its
 // predecessor in the stream to finish (and its writes to be visible) before
-// it reads any global input (pdl_wait, its first statement), and lets the
-// next kernel be scheduled once its own main loop is done (pdl_trigger), so
-// the next kernel's launch and prologue overlap this kernel's tail.  No data
-// dependence changes: a kernel that never reaches pdl_trigger releases its
-// dependent when it exits.
+// it reads anything a kernel of the library may have written (pdl_wait), and
+// lets the next kernel be scheduled once its own main loop is done
+// (pdl_trigger), so the next kernel's launch and prologue overlap this
+// kernel's tail.  Only inputs no kernel of the library writes (q, the block
+// table) are read before the wait.  No data dependence changes: a kernel
+// that never reaches pdl_trigger releases its dependent when it exits.
+// Kernel parameters are not declared __restrict__: the compiler may treat a
+// load through a const __restrict__ pointer as invariant and schedule it
+// above the wait, which returned stale split partials in the combine.
 //   KVS_PDL 0: plain stream order; 1: trigger at entry; 2: trigger late.
 // ---------------------------------------------------------------------------
 #ifndef KVS_PDL

@@ -20,7 +20,7 @@ namespace {
 // grid-stride range and folds them with XOR, so the loads cannot be elided;
 // one word per thread block is written.
 __global__ void __launch_bounds__(512)
-    stream_read_kernel(const uint4 *__restrict__ src, size_t n16, unsigned long long *sink) {
+    stream_read_kernel(const uint4 *src, size_t n16, unsigned long long *sink) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint4 acc = make_uint4(0u, 0u, 0u, 0u);
@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(512)
 constexpr int kStageThreads = 256;
 constexpr int kStageChunks = 4;  // 16-byte chunks of q per thread
 __global__ void __launch_bounds__(kStageThreads)
-    stage_inputs_kernel(const uint4 *__restrict__ q_src, uint4 *__restrict__ q_dst, long long n16,
-                        const int32_t *__restrict__ ctx_src, int32_t *__restrict__ ctx_dst,
+    stage_inputs_kernel(const uint4 *q_src, uint4 *q_dst, long long n16,
+                        const int32_t *ctx_src, int32_t *ctx_dst,
                         int B) {
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nt = (long long)gridDim.x * blockDim.x;

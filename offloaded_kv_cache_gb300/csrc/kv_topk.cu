@@ -37,9 +37,9 @@ constexpr uint32_t kForcedKey = 0xFFFFFFFFu;
 // selected first, lower index first among themselves.
 template <int kTopkThreads>
 __global__ void __launch_bounds__(kTopkThreads)
-    topk_kernel(const float *__restrict__ scores, const int32_t *__restrict__ ctx, int Hq, int ps,
+    topk_kernel(const float *scores, const int32_t *ctx, int Hq, int ps,
                 int maxP, int K, int keys_in_smem, int sink_tokens, int local_tokens,
-                int32_t *__restrict__ out, int *status) {
+                int32_t *out, int *status) {
   pdl_wait();
   constexpr int kTopkWarps = kTopkThreads / 32;
   extern __shared__ uint32_t skeys[];
@@ -207,9 +207,9 @@ __global__ void __launch_bounds__(kTopkThreads)
 constexpr int kUnionThreads = 512;
 
 __global__ void __launch_bounds__(kUnionThreads)
-    union_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ ctx, int Hq, int G,
-                 int gc, int ps, int maxP, int K, int umax, int32_t *__restrict__ upages,
-                 uint32_t *__restrict__ umasks, int32_t *__restrict__ ucount, int *status) {
+    union_kernel(const int32_t *idx, const int32_t *ctx, int Hq, int G,
+                 int gc, int ps, int maxP, int K, int umax, int32_t *upages,
+                 uint32_t *umasks, int32_t *ucount, int *status) {
   pdl_wait();
   extern __shared__ uint32_t words[];  // one byte of head bits per page, 4 pages a word
   __shared__ uint32_t wsum[kUnionThreads / 32];
@@ -221,14 +221,18 @@ __global__ void __launch_bounds__(kUnionThreads)
 // split-K combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
 // ---------------------------------------------------------------------------
 // One CTA per (b, q head), one thread per output channel.  The split maxima
-// and weights are staged once in shared memory; the first 16 partial outputs
-// of the channel are loaded before the reductions (Llama-3.1-8B 32k call
-// 43.1 -> 41.2 us), the rest with independent loads after them.
+// and weights are staged once in shared memory; the first kPre partial
+// outputs of the channel are loaded before the reductions, all in flight at
+// once, the rest with independent loads after them.  kPre = 16 up to 16
+// splits (it took the Llama-3.1-8B 32k call from 43.1 to 41.2 us; 64 there
+// cost 1.6 us), else 64 (the 57 splits of the 128k-token rows: the x1 page
+// window step 0.0749 -> 0.0735 ms).
 constexpr int kMaxCombineSplits = 1024;
 
+template <int kPre>
 __global__ void __launch_bounds__(kHeadDim)
-    combine_kernel(const float *__restrict__ part_o, const float *__restrict__ part_ml,
-                   float *__restrict__ out, int S, long long rows) {
+    combine_kernel(const float *part_o, const float *part_ml,
+                   float *out, int S, long long rows) {
   pdl_wait();
   __shared__ float w[kMaxCombineSplits];
   __shared__ float red[kHeadDim / 32];
@@ -237,7 +241,6 @@ __global__ void __launch_bounds__(kHeadDim)
   const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
   // the first kPre partial outputs of this channel are loaded up front, in
   // parallel with the split maxima, off the reductions' critical path
-  constexpr int kPre = 16;
   const float *po = part_o + r * kHeadDim + c;
   const long long stride = rows * kHeadDim;
   float pre[kPre];
@@ -331,8 +334,9 @@ cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int 
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st) {
   const long long rows = (long long)B * Hq;
-  return launch_pdl(combine_kernel, dim3((unsigned)rows), dim3(kHeadDim), 0, st, part_o, part_ml,
-                    out, S, rows);
+  auto kern = S <= 16 ? combine_kernel<16> : combine_kernel<64>;
+  return launch_pdl(kern, dim3((unsigned)rows), dim3(kHeadDim), 0, st, part_o, part_ml, out, S,
+                    rows);
 }
 
 }  // namespace kvs

@@ -19,12 +19,12 @@ namespace kvs {
 // scan, writes them in page order.  `wsum` holds THREADS / 32 words of shared
 // memory.  Calls pdl_trigger once the selection has been read.
 template <int THREADS>
-__device__ __forceinline__ void union_group(const int32_t *__restrict__ idx,
-                                            const int32_t *__restrict__ ctx, int Hq, int G,
+__device__ __forceinline__ void union_group(const int32_t *idx,
+                                            const int32_t *ctx, int Hq, int G,
                                             int gc, int ps, int maxP, int K, int umax,
-                                            int32_t *__restrict__ upages,
-                                            uint32_t *__restrict__ umasks,
-                                            int32_t *__restrict__ ucount, int *status, int grp,
+                                            int32_t *upages,
+                                            uint32_t *umasks,
+                                            int32_t *ucount, int *status, int grp,
                                             int b, int groups, uint32_t *words, uint32_t *wsum) {
   constexpr int WARPS = THREADS / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

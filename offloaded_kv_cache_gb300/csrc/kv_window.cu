@@ -55,9 +55,9 @@ __device__ __forceinline__ int page_run(int P) {
 // wsm: need[maxP] bytes (0 none, 1 miss, 2 hit), then skey[C] (slot keys),
 // then aux[C] (each slot's page until the eviction, then the freed slots in
 // ascending order).
-__device__ __forceinline__ void update_group(const int32_t *__restrict__ indices,
-                                             const float *__restrict__ scores,
-                                             const int32_t *__restrict__ ctx, int Hq, int Hkv,
+__device__ __forceinline__ void update_group(const int32_t *indices,
+                                             const float *scores,
+                                             const int32_t *ctx, int Hq, int Hkv,
                                              int ps, int maxP, int K, int C, int32_t *slot_page,
                                              int32_t *page_slot, uint32_t *fetch_bits,
                                              int32_t *stats, int *status, long long g,
@@ -255,8 +255,8 @@ __device__ __forceinline__ void update_group(const int32_t *__restrict__ indices
 // u % groups).  Both only read the selection and they write disjoint
 // outputs, so they run side by side instead of one after the other.
 __global__ void __launch_bounds__(kWinThreads)
-    window_step_kernel(const int32_t *__restrict__ indices, const float *__restrict__ scores,
-                       const int32_t *__restrict__ ctx, int Hq, int Hkv, int ps, int maxP, int K,
+    window_step_kernel(const int32_t *indices, const float *scores,
+                       const int32_t *ctx, int Hq, int Hkv, int ps, int maxP, int K,
                        int C, int32_t *slot_page, int32_t *page_slot, uint32_t *fetch_bits,
                        int32_t *stats, int *status, int n_update, int G, int gc, int umax,
                        int groups, int32_t *upages, uint32_t *umasks, int32_t *ucount) {
