@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   if constexpr (!MMA) {
     // CUDA-core path: the barriers and q in shared memory before waiting for
     // the previous kernel in the stream (no kernel of the path writes q), so
-    // that this overlaps that kernel's tail (OPT-6.7B dense 46.7 -> 46.0 us).
+    // that this overlaps that kernel's tail (OPT-6.7B dense 46.7 -> 46.0 us;
+    // the block table below, 46.33 -> 46.20 us).
     if (threadIdx.x == 0) {
       for (int s = 0; s < a.nstages; ++s) {
         mbar_init(smem_u32(&full[s]), a.use_tma && !WIN ? 1u : 32u);
@@ -173,6 +174,13 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       const int g = i / kHeadDim, c = i % kHeadDim;
       const T *qrow = static_cast<const T *>(a.q) + ((long long)b * a.Hq + head0 + g) * kHeadDim;
       q_s[(g * SL + c / EPS) * QSTR + (c % EPS)] = Elem<T>::to_f32(qrow[c]);
+    }
+    // A dense CTA with the whole row (one split) lists pages [0, P), P <= maxP:
+    // their block-table entries load before the wait too (no kernel writes
+    // the table), into the entries the same thread resolves after it.
+    if (!WIN && a.union_pages == nullptr && a.num_splits == 1) {
+      for (int j = threadIdx.x; j < min(a.maxP, kMaxListPages); j += blockDim.x)
+        plist[j].phys = a.block_table[(long long)b * a.maxP + j];
     }
     pdl_wait();
   }
@@ -227,6 +235,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           if (sp >= 0 && sp < a.src_nphys) ent.src = (int)sp;
           else ph = -1;
         }
+      } else if (!MMA && !sparse && a.num_splits == 1) {
+        ph = plist[j].phys;  // loaded before the wait (p == j)
       } else {
         ph = a.block_table[(long long)b * a.maxP + p];
       }
