@@ -340,7 +340,10 @@ int kv_window_reset(const kv_shape *shape, const kv_window *win, void *stream);
  * page several head chunks need is read from k_cache once per chunk.
  * C must hold every needed page: C >= min(G * k, maxP), else
  * KV_ERR_INVALID_ARG.  cache_k / cache_v must be device memory
- * (KV_ERR_LOCATION).  The workspace must hold kv_window_workspace_bytes. */
+ * (KV_ERR_LOCATION).  The workspace must hold kv_window_workspace_bytes.
+ * The window state marks a fetched page as cached before the attention has
+ * stored it into its slot: after a call whose device status reports an error
+ * (kv_device_status), reset the window (kv_window_reset) before the next. */
 int kv_sparse_decode_attn_window(const kv_shape *shape, const void *q, const void *k_cache,
                                  const void *v_cache, const int32_t *block_table,
                                  const int32_t *context_lens, const int32_t *indices, int32_t k,
