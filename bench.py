@@ -576,10 +576,12 @@ def main():
     value = replicas.whole_job_rate(step_bytes, ms_per_step * 1e-3, ws) / 1e9
     qps = replicas.whole_job_rate(spec.batch * spec.num_q_heads, ms_per_step * 1e-3, ws)
 
-    # sustained window for the clock record when the timed region is short
-    if rank == 0 and total_ms < 500:
+    # sustained window for the clock record when the timed region is short;
+    # every rank runs it (its barriers must pair with the other ranks'), sized
+    # from the slowest rank's time so that all ranks make the same calls
+    if t_local < 500:
         clocks.mark_on()
-        timed(stages, max(20, int(args.steps * 600 / max(total_ms, 1e-3))), 3)
+        timed(stages, max(20, int(args.steps * 600 / max(t_local, 1e-3))), 3)
         clocks.mark_off()
     clocks.stop()
 
