@@ -544,6 +544,7 @@ extern "C" {
 
 int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
                          const int32_t *context_lens, void *minmax, void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!al16(minmax) || !al4(block_table) || !al4(context_lens)) return KV_ERR_INVALID_ARG;
@@ -563,6 +564,7 @@ int kv_page_minmax_build(const kv_shape *shape, const void *k_cache, const int32
 int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new, void *k_cache,
                     void *v_cache, const int32_t *block_table, const int32_t *context_lens,
                     int32_t *context_lens_out, void *minmax, void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!al16(k_new) || !al16(v_new) || !al4(block_table) || !al4(context_lens) ||
@@ -586,6 +588,7 @@ int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new,
 int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
                   const int32_t *block_table, const int32_t *context_lens, float *scores,
                   void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!al16(q) || !al16(minmax) || !al16(scores) || !al4(block_table) || !al4(context_lens))
@@ -622,17 +625,20 @@ static int mean_build_common(const kv_shape *shape, const void *k_cache, const i
 
 int kv_page_mean_build(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
                        const int32_t *context_lens, void *mean, void *stream) {
+  KV_API_RANGE();
   return mean_build_common(shape, k_cache, block_table, context_lens, mean, false, stream);
 }
 
 int kv_page_mean_refresh(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
                          const int32_t *context_lens, void *mean, void *stream) {
+  KV_API_RANGE();
   return mean_build_common(shape, k_cache, block_table, context_lens, mean, true, stream);
 }
 
 int kv_page_score_mean(const kv_shape *shape, const void *q, const void *mean,
                        const int32_t *block_table, const int32_t *context_lens, float *scores,
                        void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!al16(q) || !al16(mean) || !al16(scores) || !al4(block_table) || !al4(context_lens))
@@ -659,6 +665,7 @@ int kv_topk_select_forced(const kv_shape *shape, const float *scores,
                           const int32_t *context_lens, int32_t k, int32_t sink_tokens,
                           int32_t local_tokens, int32_t *indices, void *workspace,
                           size_t workspace_bytes, void *stream) {
+  KV_API_RANGE();
   (void)workspace;
   (void)workspace_bytes;
   int rc = check_shape(shape);
@@ -679,6 +686,7 @@ int kv_topk_select_forced(const kv_shape *shape, const float *scores,
 int kv_topk_select(const kv_shape *shape, const float *scores, const int32_t *context_lens,
                    int32_t k, int32_t *indices, void *workspace, size_t workspace_bytes,
                    void *stream) {
+  KV_API_RANGE();
   return kv_topk_select_forced(shape, scores, context_lens, k, 0, 0, indices, workspace,
                                workspace_bytes, stream);
 }
@@ -698,6 +706,7 @@ int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_ca
                           const int32_t *context_lens, const int32_t *indices, int32_t k,
                           float scale, float *out, void *workspace, size_t workspace_bytes,
                           void *stream) {
+  KV_API_RANGE();
   if (!indices) return KV_ERR_INVALID_ARG;
   return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, indices, k, scale, out,
                      workspace, workspace_bytes, stream);
@@ -707,6 +716,7 @@ int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cac
                          const void *v_cache, const int32_t *block_table,
                          const int32_t *context_lens, float scale, float *out, void *workspace,
                          size_t workspace_bytes, void *stream) {
+  KV_API_RANGE();
   return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, nullptr, 0, scale,
                      out, workspace, workspace_bytes, stream);
 }
@@ -723,6 +733,7 @@ static void *mapped_host(const void *p) {
 }
 
 int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!io || !io->q_host || !io->context_lens_host || !io->out_host || io->k < 0)
@@ -817,6 +828,7 @@ static int check_window(const kv_shape *s, const kv_window *win, int32_t k) {
 }
 
 int kv_window_reset(const kv_shape *shape, const kv_window *win, void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!win || win->cache_pages < 1 || !al4(win->slot_page) || !al4(win->page_slot))
@@ -835,6 +847,7 @@ int kv_sparse_decode_attn_window(const kv_shape *shape, const void *q, const voi
                                  const float *scores, float scale, float *out,
                                  const kv_window *win, void *workspace, size_t workspace_bytes,
                                  void *stream) {
+  KV_API_RANGE();
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!indices || k < 1 || !al16(scores)) return KV_ERR_INVALID_ARG;

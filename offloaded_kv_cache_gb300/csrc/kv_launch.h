@@ -3,9 +3,22 @@
 // only what the kernels are compiled from.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kv_internal.cuh"
 
 namespace kvs {
+
+// An NVTX range over one call of the C ABI, named after the call, so that a
+// profiler's timeline shows which call each kernel launch belongs to.  With no
+// profiler attached a range costs a few nanoseconds.
+struct ApiRange {
+  explicit ApiRange(const char *name) { nvtxRangePushA(name); }
+  ~ApiRange() { nvtxRangePop(); }
+  ApiRange(const ApiRange &) = delete;
+  ApiRange &operator=(const ApiRange &) = delete;
+};
+#define KV_API_RANGE() ::kvs::ApiRange kv_api_range_(__func__)
 
 cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
                                 void *minmax, int B, int Hkv, int ps, int maxP, long long nphys,

@@ -51,6 +51,7 @@ extern "C" int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q
                                             const int32_t *block_table,
                                             const int32_t *context_lens, float scale,
                                             float *out, void *stream) {
+  KV_API_RANGE();
   if (!shape) return KV_ERR_INVALID_ARG;
   // size check first: a shape whose partials do not fit is refused before any
   // other work (kv_attn_workspace_bytes returns 0 for an invalid shape, and

@@ -99,6 +99,7 @@ cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
 
 extern "C" int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
                                     int32_t sink_words, void *stream) {
+  KV_API_RANGE();
   using namespace kvs;
   if (!src || !sink || ((uintptr_t)src & 15u) || ((uintptr_t)sink & 7u) || bytes < 16 ||
       (bytes & 15u) || sink_words < 1)
