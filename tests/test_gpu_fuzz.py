@@ -8,6 +8,8 @@ attention (as in test_gpu_parity), and in half of the cases also the
 forced-page selection and two page-window steps.  Same bars as the parity
 tests; the oracle never sees a GPU value.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -21,7 +23,7 @@ from test_gpu_parity import run_pipeline_and_check
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 64
+N_CASES = int(os.environ.get("KVS_FUZZ_CASES", "64"))  # more for a longer stress run
 
 
 def draw_case(i):
