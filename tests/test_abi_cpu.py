@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from offloaded_kv_cache_gb300 import kvsparse as kv
@@ -138,3 +139,43 @@ def test_workspace_sizes_follow_the_plan(kvlib):
             groups = spec.batch * spec.num_kv_heads * (G // gc)
             assert sparse >= 2 * groups * umax * 4 + groups * 4
         assert kv.kv_topk_workspace_bytes(s, max(1, spec.topk)) == 0
+
+
+def test_launch_plans_keep_their_invariants(kvlib):
+    # seeded random shapes through the planner (the occupancy estimate when
+    # no device is present): every split count covers its pages with at most
+    # 512 per CTA and at most 1024 CTAs per (sequence, kv head, head chunk),
+    # and the workspace holds the split partials, the union lists and, for
+    # the page window, the fetch bits
+    rng = np.random.default_rng(20261202)
+    for _ in range(300):
+        dtype = ["f32", "f16", "bf16"][rng.integers(3)]
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        g = int(rng.choice([1, 2, 3, 4, 8, 16]))
+        ps = int(rng.choice([16, 32, 64, 128]))
+        B = int(rng.integers(1, 65))
+        maxP = int(rng.choice([1, 7, 34, 256, 2048, 8192, 70000]))
+        k = int(rng.choice([0, 1, 32, 256, 512, 5000]))
+        s = kv.make_shape(B, hkv * g, hkv, 128, ps, maxP, B * maxP, dtype)
+        S = kv.kv_attn_num_splits(s, k)
+        if S == 0:  # refused (e.g. more cache rows than 32-bit TMA coordinates address)
+            assert kv.kv_attn_workspace_bytes(s, k) == 0
+            continue
+        gc = (4 if g % 4 == 0 else 2 if g % 2 == 0 else 1) if dtype == "f32" else \
+             (8 if g % 8 == 0 else 4 if g % 4 == 0 else 2 if g % 2 == 0 else 1)
+        work = min(gc * k, maxP) if k > 0 else maxP
+        assert 1 <= S <= 1024, (dtype, hkv, g, ps, B, maxP, k, S)
+        assert -(-work // S) <= 512, (work, S)
+        ws = kv.kv_attn_workspace_bytes(s, k)
+        rows = B * hkv * g
+        need = S * rows * (128 + 2) * 4 if S > 1 else 0
+        if k > 0:
+            groups = B * hkv * (g // gc)
+            need += 2 * groups * work * 4 + groups * 4
+        assert ws >= need, (ws, need)
+        if k > 0:
+            C = min(g * k, maxP) + 5
+            wws = kv.kv_window_workspace_bytes(s, k, C)
+            bits = B * hkv * -(-maxP // 32) * 4
+            if wws:  # 0: the window's shared-memory bound refuses this shape
+                assert wws >= bits + 2 * B * hkv * (g // gc) * work * 4
