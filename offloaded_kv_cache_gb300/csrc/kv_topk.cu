@@ -220,74 +220,68 @@ __global__ void __launch_bounds__(kUnionThreads)
 // ---------------------------------------------------------------------------
 // split-K combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
 // ---------------------------------------------------------------------------
-// One CTA per (b, q head), one thread per output channel.  The split maxima
-// and weights are staged once in shared memory; the first kPre partial
-// outputs of the channel are loaded before the reductions, all in flight at
-// once, the rest with independent loads after them.  kPre = 16 up to 16
-// splits (it took the Llama-3.1-8B 32k call from 43.1 to 41.2 us; 64 there
-// cost 1.6 us), else 64 (the 57 splits of the 128k-token rows: the x1 page
-// window step 0.0749 -> 0.0735 ms).
+// One CTA per (b, q head), one thread per output channel.  Every warp finds M
+// and the weight sum itself, lane s holding split s, 32 splits a round, so
+// the split maxima and weights load together, once, and no block barrier
+// waits on them; the first kPre partial outputs of the channel load before
+// that, all in flight at once (16 up to 16 splits, else 64: the 57 splits of
+// the 128k-token rows), the rest with independent loads after it.
 constexpr int kMaxCombineSplits = 1024;
 
 template <int kPre>
 __global__ void __launch_bounds__(kHeadDim)
-    combine_kernel(const float *part_o, const float *part_ml,
-                   float *out, int S, long long rows) {
+    combine_kernel(const float *part_o, const float *part_ml, float *out, int S, long long rows) {
   pdl_wait();
-  __shared__ float w[kMaxCombineSplits];
-  __shared__ float red[kHeadDim / 32];
-  __shared__ float s_M, s_l;
+  constexpr int R = (kPre + 31) / 32;  // rounds of 32 splits whose values stay in registers
   const long long r = blockIdx.x;
-  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
-  // the first kPre partial outputs of this channel are loaded up front, in
-  // parallel with the split maxima, off the reductions' critical path
+  const int c = threadIdx.x, lane = c & 31;
   const float *po = part_o + r * kHeadDim + c;
   const long long stride = rows * kHeadDim;
-  float pre[kPre];
+  // all the first 32 R splits need, loaded at once: this channel's first kPre
+  // partial outputs, and split 32 q + lane's maximum and weight per round q
+  float pre[kPre], mr[R], lr[R];
 #pragma unroll
   for (int s = 0; s < kPre; ++s) pre[s] = s < S ? po[s * stride] : 0.f;
-  float m_loc = -INFINITY;
-  for (int s = c; s < S; s += kHeadDim) {
-    const float m = part_ml[(s * rows + r) * 2];
-    w[s] = m;
-    m_loc = fmaxf(m_loc, m);
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int s = 32 * q + lane;
+    mr[q] = s < S ? part_ml[(s * rows + r) * 2] : -INFINITY;
+    lr[q] = s < S ? part_ml[(s * rows + r) * 2 + 1] : 0.f;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < R; ++q) M = fmaxf(M, mr[q]);
+  for (int s = 32 * R + lane; s < S; s += 32) M = fmaxf(M, part_ml[(s * rows + r) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  auto weight = [M](float m) { return (M == -INFINITY || m == -INFINITY) ? 0.f : ex2(m - M); };
+  float l = 0.f, o = 0.f, fr[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    fr[q] = weight(mr[q]);
+    l = fmaf(fr[q], lr[q], l);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m_loc = fmaxf(m_loc, __shfl_xor_sync(0xFFFFFFFFu, m_loc, off));
-  if (lane == 0) red[warp] = m_loc;
-  __syncthreads();
-  if (c == 0) {
-    float M = red[0];
-    for (int i = 1; i < kHeadDim / 32; ++i) M = fmaxf(M, red[i]);
-    s_M = M;
+  for (int s = 0; s < kPre; ++s) {
+    const float ft = __shfl_sync(0xFFFFFFFFu, fr[s / 32], s % 32);
+    if (s < S) o = fmaf(ft, pre[s], o);
   }
-  __syncthreads();
-  const float M = s_M;
-  float l_loc = 0.f;
-  for (int s = c; s < S; s += kHeadDim) {
-    const float m = w[s];
-    const float f = (M == -INFINITY || m == -INFINITY) ? 0.f : ex2(m - M);
-    w[s] = f;
-    l_loc = fmaf(f, part_ml[(s * rows + r) * 2 + 1], l_loc);
+  // splits kPre .. 32 R - 1 (only when kPre = 16): weights in round R - 1
+  for (int s = kPre; s < min(S, 32 * R); ++s)
+    o = fmaf(__shfl_sync(0xFFFFFFFFu, fr[R - 1], s & 31), po[s * stride], o);
+  for (int s0 = 32 * R; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    float f = 0.f;
+    if (s < S) {
+      f = weight(part_ml[(s * rows + r) * 2]);
+      l = fmaf(f, part_ml[(s * rows + r) * 2 + 1], l);
+    }
+    const int n = min(32, S - s0);
+    for (int t = 0; t < n; ++t) o = fmaf(__shfl_sync(0xFFFFFFFFu, f, t), po[(s0 + t) * stride], o);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l_loc += __shfl_xor_sync(0xFFFFFFFFu, l_loc, off);
-  __syncthreads();
-  if (lane == 0) red[warp] = l_loc;
-  __syncthreads();
-  if (c == 0) {
-    float l = 0.f;
-    for (int i = 0; i < kHeadDim / 32; ++i) l += red[i];
-    s_l = l;
-  }
-  __syncthreads();
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
   pdl_trigger();
-  float o = 0.f;
-#pragma unroll
-  for (int s = 0; s < kPre; ++s) o = s < S ? fmaf(w[s], pre[s], o) : o;
-#pragma unroll 8
-  for (int s = kPre; s < S; ++s) o = fmaf(w[s], po[s * stride], o);
-  const float l = s_l;
   out[r * kHeadDim + c] = l > 0.f ? o / l : 0.f;
 }
 
