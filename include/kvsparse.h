@@ -135,7 +135,10 @@ int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new,
  * sum_c max(q_c * min_c, q_c * max_c) over the minmax entry of page
  * block_table[b][p], kv head h / G -- an upper bound on q . k for every key of
  * the page.  fp32 arithmetic (the products of 16-bit inputs are exact); no
- * 1/sqrt(d) factor, since it does not change the ranking.  p >= P_b -> -inf. */
+ * 1/sqrt(d) factor, since it does not change the ranking.  p >= P_b -> -inf.
+ * The index rows load together with context_lens, so block-table entries
+ * past P_b that hold an in-range physical page are read (never used); a
+ * caller with short rows avoids those reads by setting such entries to -1. */
 int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
                   const int32_t *block_table, const int32_t *context_lens, float *scores,
                   void *stream);

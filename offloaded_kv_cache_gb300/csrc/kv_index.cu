@@ -301,22 +301,13 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
   long long bt_lane = -1;
   if (lane < 16 && p0 + lane < maxP) bt_lane = bt[(long long)b * maxP + p0 + lane];
   pdl_wait();
-  const int len = ctx[b];
-  if (len < 1 || len > maxP * ps) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
-    return;
-  }
-  const int P = (len + ps - 1) / ps;
-  if (p0 >= maxP) return;
-
-  // physical pages of rows gid and gid + 8 (lanes 0..15 hold the 16 entries)
-  long long ph_lane = -1;
-  if (lane < 16 && p0 + lane < P) {
-    if (bt_lane >= 0 && bt_lane < nphys) ph_lane = bt_lane;
-    else flag_error(status, KV_ERR_BOUNDS);
-  }
-  const long long ph_a = __shfl_sync(0xFFFFFFFFu, ph_lane, gid);
-  const long long ph_b = __shfl_sync(0xFFFFFFFFu, ph_lane, gid + 8);
+  // Index rows of the warp's in-range physical pages load together with the
+  // context length (their addresses need only the block table); pages past
+  // the context are masked once the length is known.  Lanes 0..15 hold the
+  // 16 entries; rows gid and gid + 8 are this lane's.
+  const long long cand = (lane < 16 && bt_lane >= 0 && bt_lane < nphys) ? bt_lane : -1;
+  const long long ph_a = __shfl_sync(0xFFFFFFFFu, cand, gid);
+  const long long ph_b = __shfl_sync(0xFFFFFFFFu, cand, gid + 8);
   constexpr int kRowElems = MEAN ? kHeadDim : 2 * kHeadDim;
   uint4 ra[NCH], rb[NCH];
   const uint4 *rowa = reinterpret_cast<const uint4 *>(mm + ((ph_a < 0 ? 0 : ph_a) * Hkv + kvh) * kRowElems);
@@ -326,6 +317,15 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
     ra[i] = ph_a >= 0 ? rowa[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
     rb[i] = ph_b >= 0 ? rowb[tig + 4 * i] : make_uint4(0u, 0u, 0u, 0u);
   }
+  const int len = ctx[b];
+  if (len < 1 || len > maxP * ps) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag_error(status, KV_ERR_BOUNDS);
+    return;
+  }
+  const int P = (len + ps - 1) / ps;
+  if (p0 >= maxP) return;
+  // a page of the context whose block-table entry is out of range
+  if (lane < 16 && p0 + lane < P && cand < 0) flag_error(status, KV_ERR_BOUNDS);
   pdl_trigger();
   float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
   for (int e = 0; e < 4; ++e) {
     const int h = 2 * tig + (e & 1);
     const int p = (e < 2) ? pa : pb;
-    const bool ok = (e < 2) ? ph_a >= 0 : ph_b >= 0;
+    const bool ok = p < P && ((e < 2) ? ph_a >= 0 : ph_b >= 0);
     if (h < GS && p < maxP)
       scores[((long long)b * Hq + head0 + h) * maxP + p] = ok ? c[e] : -INFINITY;
   }

@@ -53,6 +53,16 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int b = (int)(row / Hq);
   int32_t *orow = out + row * K;
   const float *srow = scores + row * maxP;
+  // the row's first scores load together with the context length (every
+  // one of the row's maxP entries is allocated); entries past the row's
+  // pages are masked once the length is known
+  constexpr int kSpec = 4;
+  float spec[kSpec];
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int p = tid + u * kTopkThreads;
+    spec[u] = p < maxP ? srow[p] : 0.f;
+  }
   const int len = ctx[b];
   if (len < 1 || len > maxP * ps) {
     if (tid == 0) flag_error(status, KV_ERR_BOUNDS);
@@ -75,7 +85,17 @@ __global__ void __launch_bounds__(kTopkThreads)
   // keys (into shared memory when they fit), their minimum and maximum
   if (tid < 256) hist[0][tid] = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int p = tid; p < P; p += kTopkThreads) {
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int p = tid + u * kTopkThreads;
+    if (p < P) {
+      const uint32_t k = (p < f_sink || p >= f_local) ? kForcedKey : score_key(spec[u]);
+      if (keys_in_smem) skeys[p] = k;
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+  }
+  for (int p = tid + kSpec * kTopkThreads; p < P; p += kTopkThreads) {
     const uint32_t k = raw_key(p);
     if (keys_in_smem) skeys[p] = k;
     kmin = min(kmin, k);
@@ -226,7 +246,6 @@ __global__ void __launch_bounds__(kUnionThreads)
 // waits on them; the first kPre partial outputs of the channel load before
 // that, all in flight at once (16 up to 16 splits, else 64: the 57 splits of
 // the 128k-token rows), the rest with independent loads after it.
-constexpr int kMaxCombineSplits = 1024;
 
 template <int kPre>
 __global__ void __launch_bounds__(kHeadDim)

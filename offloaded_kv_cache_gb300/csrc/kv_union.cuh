@@ -32,6 +32,14 @@ __device__ __forceinline__ void union_group(const int32_t *idx,
   const int kvh = grp / nchunk, chunk = grp % nchunk;
   const int head0 = kvh * G + chunk * gc;
   const long long gbase = (long long)b * groups + grp;
+  // the first selections load together with the context length
+  constexpr int kSpec = 4;
+  int32_t sel[kSpec];
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int i = tid + u * THREADS;
+    sel[u] = i < gc * K ? idx[((long long)b * Hq + head0 + i / K) * K + i % K] : -1;
+  }
   const int len = ctx[b];
   if (len < 1 || len > maxP * ps) {
     if (tid == 0) {
@@ -45,16 +53,18 @@ __device__ __forceinline__ void union_group(const int32_t *idx,
   const int nw = (P + 3) / 4;
   for (int i = tid; i < nw; i += THREADS) words[i] = 0u;
   __syncthreads();
-  for (int i = tid; i < gc * K; i += THREADS) {
-    const int g = i / K, j = i % K;
-    const int p = idx[((long long)b * Hq + head0 + g) * K + j];
-    if (p < 0) continue;
+  auto mark = [&](int i, int p) {
+    if (p < 0) return;
     if (p >= P) {
       flag_error(status, KV_ERR_BOUNDS);
-      continue;
+      return;
     }
-    atomicOr(&words[p >> 2], (1u << g) << ((p & 3) * 8));
-  }
+    atomicOr(&words[p >> 2], (1u << (i / K)) << ((p & 3) * 8));
+  };
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) mark(tid + u * THREADS, sel[u]);
+  for (int i = tid + kSpec * THREADS; i < gc * K; i += THREADS)
+    mark(i, idx[((long long)b * Hq + head0 + i / K) * K + i % K]);
   __syncthreads();
   pdl_trigger();
   const int per = (nw + THREADS - 1) / THREADS;  // words per thread
