@@ -235,6 +235,26 @@ def test_out_of_range_device_data_is_flagged_not_read():
     assert kv.kv_device_status() == kv.KV_OK
 
 
+@pytest.mark.parametrize("dtype,hq,hkv", [("bf16", 8, 2), ("f16", 4, 1), ("f32", 2, 1)])
+def test_block_table_entries_past_the_context_are_ignored(dtype, hq, hkv):
+    # entries past each row's pages hold other rows' pages, pages past the
+    # cache and negative values: none is used, none is an error
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=hq, hkv=hkv, context=16 * 20, ps=16, topk=4,
+                       index=2900 + hq)
+    wl = W.generate(spec, context_lens=[16 * 20, 16 * 3 + 5, 1])
+    rng = np.random.default_rng(2901)
+    for b in range(spec.batch):
+        P = -(-int(wl.context_lens[b]) // spec.page_size)
+        n = spec.max_pages - P
+        junk = rng.choice([0, 1, 2], size=n)
+        wl.block_table[b, P:] = np.where(
+            junk == 0, rng.integers(0, spec.num_phys_pages, size=n),
+            np.where(junk == 1, spec.num_phys_pages + rng.integers(0, 1 << 20, size=n),
+                     -rng.integers(1, 1 << 20, size=n))).astype(np.int32)
+    run_pipeline_and_check(wl, 4)
+    assert kv.kv_device_status() == kv.KV_OK
+
+
 # ---------------------------------------------------------------- wide block table
 
 @pytest.mark.parametrize("dtype,hq,hkv", [("bf16", 8, 2), ("f16", 4, 4)])
