@@ -74,6 +74,16 @@ __device__ __forceinline__ void update_group(const int32_t *indices,
   int32_t *pslot = page_slot + g * maxP;
   const int W = (maxP + 31) / 32;  // fetch-bit words per group
   uint32_t *fbits = fetch_bits + g * W;
+  // the first selections and slot pages load together with the context length
+  const int32_t *sel = indices + ((long long)b * Hq + (long long)kvh * G) * K;
+  constexpr int kSpec = 4;
+  int32_t sel_r[kSpec], sp_r[kSpec];
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int i = tid + u * kWinThreads;
+    sel_r[u] = i < G * K ? sel[i] : -1;
+    sp_r[u] = i < C ? sp[i] : -1;
+  }
   const int len = ctx[b];
   if (len < 1 || len > maxP * ps) {
     if (tid == 0) flag_error(status, KV_ERR_BOUNDS);
@@ -85,16 +95,23 @@ __device__ __forceinline__ void update_group(const int32_t *indices,
   // need set of the group's G query heads
   for (int i = tid; i < (maxP + 3) / 4; i += kWinThreads) reinterpret_cast<uint32_t *>(need)[i] = 0u;
   __syncthreads();
-  for (int i = tid; i < G * K; i += kWinThreads) {
-    const int p = indices[((long long)b * Hq + (long long)kvh * G) * K + i];
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u)
+    if (sel_r[u] >= 0 && sel_r[u] < P) need[sel_r[u]] = 1;
+  for (int i = tid + kSpec * kWinThreads; i < G * K; i += kWinThreads) {
+    const int p = sel[i];
     if (p >= 0 && p < P) need[p] = 1;
   }
   __syncthreads();
 
   // classify the slots: free, hit (need -> 2), or an eviction candidate
   uint32_t hit = 0, fre = 0, cand = 0, cmin = 0xFFFFFFFFu, cmax = 0u;
-  for (int s = tid; s < C; s += kWinThreads) {
-    const int p = sp[s];
+  for (int s = tid, u = 0; s < C; s += kWinThreads, ++u) {
+    int p = 0;
+#pragma unroll
+    for (int v = 0; v < kSpec; ++v)
+      if (u == v) p = sp_r[v];  // static register indexing
+    if (u >= kSpec) p = sp[s];
     uint32_t key;
     if (p < 0 || p >= maxP) {
       key = kSlotFree;
