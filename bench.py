@@ -40,13 +40,13 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
 NCU_TRAFFIC = {
-    "opt6.7b-b32-ctx544": {"bytes": 289.406464e6, "src": "5228a6f62cbab6e2"},
-    "llama3.1-8b-b4-ctx32k": {"bytes": 192.258304e6, "src": "5228a6f62cbab6e2"},
+    "opt6.7b-b32-ctx544": {"bytes": 289.127680e6, "src": "5228a6f62cbab6e2"},
+    "llama3.1-8b-b4-ctx32k": {"bytes": 192.197376e6, "src": "5228a6f62cbab6e2"},
     # from the one-pass DRAM-bytes capture of every kernel at full size
-    "70b-gqa-b8-ctx64k-ps64": {"bytes": 1086.441728e6, "src": "5228a6f62cbab6e2"},
+    "70b-gqa-b8-ctx64k-ps64": {"bytes": 1086.374400e6, "src": "5228a6f62cbab6e2"},
     # host-resident K/V: DRAM carries only q and the lists; the K/V bytes
     # arrive over the host link (ctc__rx_bytes_data_user.sum)
-    "llama3.1-8b-b1-ctx128k-host": {"bytes": 190208.0, "link_bytes": 105.728000e6,
+    "llama3.1-8b-b1-ctx128k-host": {"bytes": 190720.0, "link_bytes": 105.728000e6,
                                     "src": "5228a6f62cbab6e2"},
 }
 
