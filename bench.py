@@ -33,7 +33,9 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-DEFAULT_WORKLOAD = "opt6.7b-b32-ctx544"
+DEFAULT_WORKLOAD = "70b-gqa-b8-ctx64k-ps64"
+# sparse workloads also measured (shorter) beside the default one
+SIDE_WORKLOADS = ("llama3.1-8b-b4-ctx32k", "llama3.1-8b-b1-ctx128k-host")
 METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/sec"
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
@@ -359,6 +361,142 @@ def host_link_gbs(kv, torch, nbytes=512 << 20, reps=10):
     return {"zero_copy": zc, "h2d": h2d, "peak": max(zc, h2d)}
 
 
+
+R_GRAPH = 10  # steps per captured graph (amortises the graph launch itself)
+
+
+def _capture(layer, copies, fn, n):
+    """A CUDA graph of n consecutive calls of fn, K/V copies rotating (after
+    eager warm-up calls of every copy)."""
+    import torch
+    for c in range(copies):
+        layer.use_copy(c)
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for i in range(n):
+            layer.use_copy(i)
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_graph_steps(layer, copies, fn, k, warm, ws=1):
+    """Exactly k calls of fn on the device (graphs of R_GRAPH calls, then
+    single calls), after warm calls; returns device ms for the k calls."""
+    import torch
+    from offloaded_kv_cache_gb300 import replicas
+    stream = torch.cuda.current_stream()
+    g_r = _capture(layer, copies, fn, R_GRAPH)
+    g_1 = _capture(layer, copies, fn, 1)
+    for _ in range(max(1, warm // R_GRAPH)):
+        g_r.replay()
+    torch.cuda.synchronize()
+    replicas.barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k // R_GRAPH):
+        g_r.replay()
+    for _ in range(k % R_GRAPH):
+        g_1.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    replicas.barrier(ws)
+    return e0.elapsed_time(e1)
+
+
+def timed_stages(layer, copies, fns, k, warm, ws=1):
+    """The step (every stage once) k times, then each stage alone k times
+    (its mean duration); returns (total ms of the k steps, {stage: ms})."""
+    def step_fn():
+        for _, f in fns:
+            f()
+    total = run_graph_steps(layer, copies, step_fn, k, warm, ws)
+    per = {n: run_graph_steps(layer, copies, f, k, warm, ws) / k for n, f in fns} \
+        if len(fns) > 1 else {fns[0][0]: total / k}
+    return total, per
+
+
+def kv_copies_for(spec):
+    """Rotating K/V copies so that one pass over them exceeds 4x the L2."""
+    l2_bytes = 129 * 2**20
+    if spec.kv_loc != "hbm":
+        return 1
+    return max(1, min(8, math.ceil(4 * l2_bytes / spec.kv_bytes())))
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(l.split(":", 1) for l in out.splitlines() if ":" in l)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        name = fields.get("Model name") or fields.get("BIOS Model name")
+        if name:
+            vendor = fields.get("Vendor ID", "")
+            return f"{vendor} {name}".strip()
+    except (OSError, subprocess.SubprocessError, ValueError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def side_workload(name, steps, warm):
+    """The sparse step (score + top-K + sparse attention) of another workload,
+    timed like the default one, with its attention call against its own
+    roofline (HBM, or the pinned-host link measured in this run)."""
+    import torch
+    from offloaded_kv_cache_gb300 import kvsparse as kv
+    from offloaded_kv_cache_gb300 import workloads as W
+    from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+    spec = W.WORKLOADS[name]
+    wl = W.generate(spec)
+    copies = kv_copies_for(spec)
+    layer = DecodeLayer(wl, kv_copies=copies)
+    layer.build_index()
+    layer.score()
+    layer.select()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    step_bytes, attn_bytes = sparse_bytes(spec, wl.context_lens, layer.indices.cpu().numpy())
+    stages = [("page_score", layer.score), ("topk_select", layer.select),
+              ("sparse_attn", lambda: layer.sparse_attn())]
+    total, per = timed_stages(layer, copies, stages, steps, warm)
+    ms = total / steps
+    if spec.kv_loc == "host":
+        link = host_link_gbs(kv, torch)
+        peak, bound = link["peak"], "host-link"
+        peak_source = (f"pinned-host read bandwidth measured in this run: max of zero-copy "
+                       f"streaming read {link['zero_copy']:.1f} GB/s and cudaMemcpyAsync H2D "
+                       f"{link['h2d']:.1f} GB/s")
+    else:
+        peak, kind = measured_peaks()
+        bound, peak_source = "hbm", f"MEASURED_PEAKS.json hbm_gbs ({kind})"
+    achieved = attn_bytes / (per["sparse_attn"] * 1e-3) / 1e9
+    res = {"step": "score + top-K + sparse attention", "steps": steps,
+           "ms_per_step": round(ms, 5),
+           "value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "step_bytes": int(step_bytes),
+           "stages_ms": {n: round(v, 5) for n, v in per.items()},
+           "attention_call": {"bound": bound, "achieved": round(achieved, 1),
+                              "peak": round(peak, 1), "unit": "GB/s",
+                              "frac": round(achieved / peak, 4), "bytes": int(attn_bytes),
+                              "peak_source": peak_source},
+           "l2": (f"{copies} rotating K/V copies" if copies > 1 else
+                  ("K/V in pinned host memory" if spec.kv_loc == "host" else "K/V larger than L2"))}
+    del layer
+    torch.cuda.empty_cache()
+    return res
+
 # ---------------------------------------------------------------------------
 
 def run_reference(args, spec_name):
@@ -392,7 +530,7 @@ def run_reference(args, spec_name):
                        "topk": spec.topk, "kv_loc": spec.kv_loc, "parallelism": "replicas"},
             "queries_per_s": round(qps, 2),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
-                             "kind": "oracle", "sample": what},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": what},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -407,6 +545,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--side-workloads", default=",".join(SIDE_WORKLOADS),
+                    help="comma-separated sparse workloads also timed (shorter) and reported "
+                         "under `workloads`; empty for none")
     ap.add_argument("--window-steps", type=int, default=0,
                     help="profiling aid: run this many eager page-window decode steps "
                          "(x1 window, drifting queries) on the workload and exit")
@@ -437,10 +578,7 @@ def main():
     spec = W.WORKLOADS[args.workload]
     wl = W.generate(spec)
     ctx = wl.context_lens
-    l2_bytes = 129 * 2**20
-    copies = 1
-    if spec.kv_loc == "hbm":
-        copies = max(1, min(8, math.ceil(4 * l2_bytes / spec.kv_bytes())))
+    copies = kv_copies_for(spec)
     layer = DecodeLayer(wl, kv_copies=copies)
     stream = torch.cuda.current_stream()
     sparse = spec.topk > 0
@@ -517,54 +655,11 @@ def main():
         attn_bytes = step_bytes
         dominant = "dense_attn"
 
-    R = 10  # steps per captured graph (amortises the graph launch itself)
-
-    def capture(fn, n):
-        """A CUDA graph of n consecutive calls of fn, K/V copies rotating
-        (after eager warm-up calls of every copy)."""
-        for c in range(copies):
-            layer.use_copy(c)
-            fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="relaxed"):
-            for i in range(n):
-                layer.use_copy(i)
-                fn()
-        torch.cuda.synchronize()
-        return g
-
     def run_steps(fn, k, warm):
-        """Exactly k calls of fn on the device (graphs of R calls, then single
-        calls), after warm calls; returns device ms for the k calls."""
-        g_r = capture(fn, R)
-        g_1 = capture(fn, 1)
-        for _ in range(max(1, warm // R)):
-            g_r.replay()
-        torch.cuda.synchronize()
-        replicas.barrier(ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(k // R):
-            g_r.replay()
-        for _ in range(k % R):
-            g_1.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        replicas.barrier(ws)
-        return e0.elapsed_time(e1)
+        return run_graph_steps(layer, copies, fn, k, warm, ws)
 
     def timed(fns, k, warm):
-        """The step (every stage once) k times, then each stage alone k times
-        (its mean duration); returns (total ms of the k steps, {stage: ms})."""
-        def step_fn():
-            for _, f in fns:
-                f()
-        total = run_steps(step_fn, k, warm)
-        per = {n: run_steps(f, k, warm) / k for n, f in fns} if len(fns) > 1 else \
-            {fns[0][0]: total / k}
-        return total, per
+        return timed_stages(layer, copies, fns, k, warm, ws)
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -683,6 +778,13 @@ def main():
                        "bytes": a_bytes}
     assert kv.kv_device_status() == kv.KV_OK
 
+    # other sparse workloads, shorter runs, after the default one
+    side = {}
+    for name in [n for n in args.side_workloads.split(",") if n and n != spec.name]:
+        side[name] = side_workload(name, max(10, min(args.steps, 200)), args.warmup)
+    if side:
+        extra["workloads"] = side
+
     peak, peak_kind = measured_peaks()
     bound = "hbm"
     peak_source = f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"
@@ -706,7 +808,7 @@ def main():
         gbs, cq, dt, what = oracle_sample(spec, wl, 2.0, cores)
         gbs1, cq1, dt1, what1 = oracle_sample(spec, wl, 2.0, 1)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": what, "seconds": round(dt, 3), "queries_per_s": round(cq, 2),
+               "cpu_model": cpu_model(), "sample": what, "seconds": round(dt, 3), "queries_per_s": round(cq, 2),
                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "sample": what1,
                                  "seconds": round(dt1, 3), "queries_per_s": round(cq1, 2)}}
 
@@ -727,7 +829,7 @@ def main():
                               "K/V larger than L2"),
                        "splits": splits,
                        "timing": ("CUDA events around exactly K steps replayed as CUDA graphs of "
-                                  f"{R} steps; per-kernel times from graphs of each stage alone"),
+                                  f"{R_GRAPH} steps; per-kernel times from graphs of each stage alone"),
                        "parallelism": f"replicas x{ws}"},
             "queries_per_s": round(qps, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
