@@ -33,7 +33,12 @@
  *    kv_device_status, which synchronises the given stream.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Calls are asynchronous on it and write only their named outputs and
- *    their workspace.
+ *    their workspace.  Kernels are launched with programmatic dependent
+ *    launch: a call's first kernel may start while the stream's previous
+ *    kernel finishes, but it reads no input before griddepcontrol.wait, so a
+ *    preceding kernel (of any library) that releases its dependents early and
+ *    writes q, the block table or any other input afterwards is still seen
+ *    complete.
  *  - Return value: KV_OK, or a negative kv_status.  Argument checks run on the
  *    host before any launch; a call that fails them launches nothing.  Checks
  *    on device-resident data (context lengths, block-table entries, selected

@@ -490,6 +490,10 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.debug_skip_page = g_debug_skip_page.load();
+  // the sparse and window calls launch their union (or window update) kernel
+  // first, which writes neither q nor the block table; a dense call's
+  // attention kernel is the first of the call
+  a.early_inputs = indices ? 1 : 0;
   if (pl.S > 1) {
     a.part_o = reinterpret_cast<float *>(w + pl.off_part_o);
     a.part_ml = reinterpret_cast<float *>(w + pl.off_part_ml);
@@ -585,10 +589,11 @@ int kv_append_token(const kv_shape *shape, const void *k_new, const void *v_new,
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
-int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
-                  const int32_t *block_table, const int32_t *context_lens, float *scores,
-                  void *stream) {
-  KV_API_RANGE();
+// early_inputs: the kernel before this one in the stream is the library's
+// own (see launch_page_score)
+static int page_score_common(const kv_shape *shape, const void *q, const void *minmax,
+                             const int32_t *block_table, const int32_t *context_lens,
+                             float *scores, int early_inputs, void *stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   if (!al16(q) || !al16(minmax) || !al16(scores) || !al4(block_table) || !al4(context_lens))
@@ -600,9 +605,16 @@ int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
   cudaError_t e = launch_page_score(shape->dtype, false, q, minmax, block_table, context_lens,
                                     scores, shape->batch, shape->num_q_heads,
                                     shape->num_kv_heads, shape->page_size,
-                                    shape->max_pages_per_seq, shape->num_phys_pages, status,
-                                    static_cast<cudaStream_t>(stream));
+                                    shape->max_pages_per_seq, shape->num_phys_pages,
+                                    early_inputs, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+int kv_page_score(const kv_shape *shape, const void *q, const void *minmax,
+                  const int32_t *block_table, const int32_t *context_lens, float *scores,
+                  void *stream) {
+  KV_API_RANGE();
+  return page_score_common(shape, q, minmax, block_table, context_lens, scores, 0, stream);
 }
 
 static int mean_build_common(const kv_shape *shape, const void *k_cache, const int32_t *block_table,
@@ -650,7 +662,7 @@ int kv_page_score_mean(const kv_shape *shape, const void *q, const void *mean,
   cudaError_t e = launch_page_score(shape->dtype, true, q, mean, block_table, context_lens,
                                     scores, shape->batch, shape->num_q_heads,
                                     shape->num_kv_heads, shape->page_size,
-                                    shape->max_pages_per_seq, shape->num_phys_pages, status,
+                                    shape->max_pages_per_seq, shape->num_phys_pages, 0, status,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
@@ -747,12 +759,15 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
   // first staged into the device buffers by one kernel whose host reads
   // overlap the previous kernel, so the score, top-K, union and attention
   // kernels each read device memory instead of paying a host round trip
-  // (Llama-3.1-8B 32k step 61.3 -> 59.5 us).  A dense step is one attention
-  // kernel that already reads q before its PDL wait: it reads them in place.
+  // (Llama-3.1-8B 32k step 61.3 -> 59.5 us).  That staging kernel never
+  // releases its dependents early, so the score kernel after it may load q
+  // and the block table before its own PDL wait.  A dense step is one
+  // attention kernel: it reads q and the lengths in place.
   const void *q = mapped_host(io->q_host);
   const int32_t *ctx = static_cast<const int32_t *>(mapped_host(io->context_lens_host));
   float *out = static_cast<float *>(mapped_host(io->out_host));
   const size_t q_bytes = rows * kHeadDim * elem_bytes(shape->dtype);
+  int staged = 0;
   if (io->k > 0 && q && ctx && io->q && io->context_lens && al16(q) && al16(io->q) &&
       al4(io->context_lens)) {
     if (launch_stage_inputs(q, io->q, q_bytes, ctx, io->context_lens, shape->batch, st) !=
@@ -762,6 +777,7 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
     }
     q = io->q;
     ctx = io->context_lens;
+    staged = 1;
   }
   if (!q) {
     if (!al16(io->q)) return KV_ERR_INVALID_ARG;
@@ -786,8 +802,8 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
     out = io->out;
   }
   if (io->k > 0) {
-    if ((rc = kv_page_score(shape, q, io->minmax, io->block_table, ctx, io->scores, stream)) !=
-        KV_OK)
+    if ((rc = page_score_common(shape, q, io->minmax, io->block_table, ctx, io->scores, staged,
+                                stream)) != KV_OK)
       return rc;
     if ((rc = kv_topk_select(shape, io->scores, ctx, io->k, io->indices, nullptr, 0, stream)) !=
         KV_OK)

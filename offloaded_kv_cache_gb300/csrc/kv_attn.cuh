@@ -159,9 +159,10 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   const int head0 = kvh * a.G + chunk * GC;
 
   if constexpr (!MMA) {
-    // CUDA-core path: the barriers and q in shared memory before waiting for
-    // the previous kernel in the stream (no kernel of the path writes q), so
-    // that this overlaps that kernel's tail (OPT-6.7B dense 46.7 -> 46.0 us;
+    // CUDA-core path: the barriers before waiting for the previous kernel in
+    // the stream, and, when that kernel is known to be one of the library's
+    // (a.early_inputs), q in shared memory and the block table too, so that
+    // they overlap that kernel's tail (OPT-6.7B dense 46.7 -> 46.0 us for q;
     // the block table below, 46.33 -> 46.20 us).
     if (threadIdx.x == 0) {
       for (int s = 0; s < a.nstages; ++s) {
@@ -170,19 +171,20 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       }
       fence_mbar_init();
     }
+    if (!a.early_inputs) pdl_wait();
     for (int i = threadIdx.x; i < GC * kHeadDim; i += blockDim.x) {
       const int g = i / kHeadDim, c = i % kHeadDim;
       const T *qrow = static_cast<const T *>(a.q) + ((long long)b * a.Hq + head0 + g) * kHeadDim;
       q_s[(g * SL + c / EPS) * QSTR + (c % EPS)] = Elem<T>::to_f32(qrow[c]);
     }
     // A dense CTA with the whole row (one split) lists pages [0, P), P <= maxP:
-    // their block-table entries load before the wait too (no kernel writes
-    // the table), into the entries the same thread resolves after it.
+    // their block-table entries load here too, into the entries the same
+    // thread resolves below.
     if (!WIN && a.union_pages == nullptr && a.num_splits == 1) {
       for (int j = threadIdx.x; j < min(a.maxP, kMaxListPages); j += blockDim.x)
         plist[j].phys = a.block_table[(long long)b * a.maxP + j];
     }
-    pdl_wait();
+    if (a.early_inputs) pdl_wait();
   }
   const bool sparse = a.union_pages != nullptr;
   const long long gidx = (long long)b * gridDim.y + grp;

@@ -268,15 +268,18 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
     page_score_mma_kernel(const T *q, const T *mm,
                           const int32_t *bt, const int32_t *ctx,
                           float *scores, int Hq, int Hkv, int ps, int maxP,
-                          long long nphys, int nchunk, int *status) {
+                          long long nphys, int nchunk, int early_inputs, int *status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int b = blockIdx.z;
   const int kvh = blockIdx.y / nchunk, chunk = blockIdx.y % nchunk;
   const int G = Hq / Hkv;
   const int head0 = kvh * G + chunk * GS;
-  // q's coefficients first: no kernel of the path writes q, so they load
-  // before the wait for the previous kernel, overlapping its tail
+  // q's coefficients first.  When the previous kernel in the stream is one
+  // of the library's (early_inputs), which write neither q nor the block
+  // table, they load before the wait for it, overlapping its tail; as the
+  // first kernel of a call, after the wait.
+  if (!early_inputs) pdl_wait();
   // coefficients of head gid in the same k order: [q- | q+] (min/max) or q (mean)
   constexpr int NCH = MEAN ? 4 : 8;       // 16-byte chunks per lane per row
   uint4 cf[NCH];
@@ -297,10 +300,10 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
     }
   }
   const int p0 = (blockIdx.x * kScoreMmaWarps + warp) * 16;  // this warp's 16 pages
-  // the block-table entries too (no kernel of the path writes them)
+  // the block-table entries too
   long long bt_lane = -1;
   if (lane < 16 && p0 + lane < maxP) bt_lane = bt[(long long)b * maxP + p0 + lane];
-  pdl_wait();
+  if (early_inputs) pdl_wait();
   // Index rows of the warp's in-range physical pages load together with the
   // context length (their addresses need only the block table); pages past
   // the context are masked once the length is known.  Lanes 0..15 hold the
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(32 * kScoreMmaWarps)
 template <class T, bool MEAN>
 cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, const int32_t *ctx,
                            float *scores, int B, int Hq, int Hkv, int ps, int maxP,
-                           long long nphys, int *status, cudaStream_t st) {
+                           long long nphys, int early_inputs, int *status, cudaStream_t st) {
   const int G = Hq / Hkv;
   const int gs = (G % 8 == 0) ? 8 : (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
   const int nchunk = G / gs;
@@ -361,7 +364,7 @@ cudaError_t score_dispatch(const void *q, const void *mm, const int32_t *bt, con
       const T *m = static_cast<const T *>(mm);
       auto kern = gs == 8 ? page_score_mma_kernel<T, 8, MEAN> : page_score_mma_kernel<T, 4, MEAN>;
       return launch_pdl(kern, g, dim3(32 * kScoreMmaWarps), 0, st, qq, m, bt, ctx, scores, Hq,
-                        Hkv, ps, maxP, nphys, nchunk, status);
+                        Hkv, ps, maxP, nphys, nchunk, early_inputs, status);
     }
   }
   dim3 grid((maxP + kScoreWarps * kScorePagesPerWarp - 1) / (kScoreWarps * kScorePagesPerWarp),
@@ -401,10 +404,11 @@ cudaError_t launch_minmax_build(int dtype, const void *k, const int32_t *bt, con
 
 cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
                               const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
-                              int Hkv, int ps, int maxP, long long nphys, int *status,
-                              cudaStream_t st) {
-#define KVS_SCORE(T, M) \
-  score_dispatch<T, M>(q, table, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, status, st)
+                              int Hkv, int ps, int maxP, long long nphys, int early_inputs,
+                              int *status, cudaStream_t st) {
+#define KVS_SCORE(T, M)                                                                     \
+  score_dispatch<T, M>(q, table, bt, ctx, scores, B, Hq, Hkv, ps, maxP, nphys, early_inputs, \
+                       status, st)
   switch (dtype) {
     case KV_F32: return mean ? KVS_SCORE(float, true) : KVS_SCORE(float, false);
     case KV_F16: return mean ? KVS_SCORE(__half, true) : KVS_SCORE(__half, false);

@@ -85,9 +85,13 @@ __device__ __forceinline__ float ex2(float x) {
 // it reads anything a kernel of the library may have written (pdl_wait), and
 // lets the next kernel be scheduled once its own main loop is done
 // (pdl_trigger), so the next kernel's launch and prologue overlap this
-// kernel's tail.  Only inputs no kernel of the library writes (q, the block
-// table) are read before the wait.  No data dependence changes: a kernel
-// that never reaches pdl_trigger releases its dependent when it exits.
+// kernel's tail.  Inputs no kernel of the library writes (q, the block table)
+// are read before the wait only by a kernel whose predecessor in the stream
+// is known to be one of the library's own (a later kernel of the same call):
+// the first kernel of a call may follow a kernel of another library that
+// releases its dependents before it writes them, so it reads every input
+// after its wait.  No data dependence changes: a kernel that never reaches
+// pdl_trigger releases its dependent when it exits.
 // Kernel parameters are not declared __restrict__: the compiler may treat a
 // load through a const __restrict__ pointer as invariant and schedule it
 // above the wait, which returned stale split partials in the combine.
@@ -246,6 +250,32 @@ struct AttnArgs {
   float scale_log2;
   unsigned long long wait_limit_ns;
   int debug_skip_page;  // >= 0: the producer never fills that page (timeout test)
+  // 1: the kernel before this one in the stream is one of this library's that
+  // writes neither q nor the block table, so they may load before the PDL
+  // wait; 0 (the first kernel of a call): they load after it, since a kernel
+  // of another library may release its dependents before it writes them
+  int early_inputs;
+  // sparse: 1 when the union lists hold resolved entries (physical page;
+  // valid tokens | head mask << 8), as the fused selection writes them
+  int union_resolved;
+};
+
+// Arguments of the fused selection kernel (page score + top-K + union).
+struct SelectArgs {
+  const void *q;               // [B][Hq][d]
+  const void *table;           // min/max index [N_phys][Hkv][2][d]
+  const int32_t *block_table;  // [B][maxP]
+  const int32_t *context_lens; // [B]
+  int32_t *indices;            // [B][Hq][K]
+  int32_t *upages;             // [B][Hkv][umax]: physical page (-1: bad entry)
+  uint32_t *umasks;            // [B][Hkv][umax]: valid tokens | head mask << 8
+  int32_t *ucount;             // [B][Hkv]
+  int *status;
+  long long nphys;
+  int Hq, Hkv, ps, maxP, K, umax;
+  int PC;                      // pages each CTA scores (a multiple of 32)
+  int sink_tokens, local_tokens;
+  int early_inputs;            // as AttnArgs::early_inputs
 };
 
 // Attention CTA shape: one producer warp plus 1..kMaxConsumerWarps consumer

@@ -39,10 +39,12 @@ cudaError_t launch_fill(int32_t *p, long long n, int32_t v, cudaStream_t st);
 cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
                                 const int32_t *ctx_src, int32_t *ctx_dst, int B,
                                 cudaStream_t st);
+// early_inputs: the previous kernel in the stream is one of the library's,
+// so q and the block table may load before the PDL wait
 cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *table,
                               const int32_t *bt, const int32_t *ctx, float *scores, int B, int Hq,
-                              int Hkv, int ps, int maxP, long long nphys, int *status,
-                              cudaStream_t st);
+                              int Hkv, int ps, int maxP, long long nphys, int early_inputs,
+                              int *status, cudaStream_t st);
 cudaError_t launch_mean_build(int dtype, const void *k, const int32_t *bt, const int32_t *ctx,
                               void *mean, int B, int Hkv, int ps, int maxP, long long nphys,
                               bool last_only, int *status, cudaStream_t st);
@@ -63,6 +65,11 @@ cudaError_t launch_attn_win(int dtype, int gc, bool mma, const AttnArgs &a, cons
 int attn_occupancy_core(int dtype, int gc, int threads, size_t smem);
 int attn_occupancy_mma(int dtype, int gc, int threads, size_t smem);
 int attn_occupancy_win(int dtype, int gc, bool mma, int threads, size_t smem);
+// the fused selection: page score + top-K + group union in one cluster launch
+// (16-bit data, G = 4 or 8 query heads per kv head)
+int select_fused_pages_per_cta(int G, int maxP);
+size_t select_fused_smem(int G, int maxP);
+cudaError_t launch_select_fused(int dtype, const SelectArgs &a, int B, cudaStream_t st);
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st);
 

@@ -8,6 +8,8 @@
 // allocation itself, or a latency-critical loop where a cudaMalloc would
 // synchronise the device.  kv_dense_decode_attn_noalloc serves them with a
 // fixed scratch array that lives in this library's device image instead.
+// Every call on a device shares that one array, so calls that overlap on the
+// GPU (on different streams, or from several host threads) race on it.
 #include <atomic>
 #include <mutex>
 
