@@ -418,55 +418,211 @@ cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *t
 }
 
 // ---------------------------------------------------------------------------
-// mean-key index: per (page, kv head), the mean of the valid keys
+// mean-key index: per (page, kv head), the mean of the valid keys, rounded
+// once (to nearest, ties to even) from the exact mean
 // ---------------------------------------------------------------------------
 // Same lane layout as the min/max build (lane = 16-byte column chunk x row
-// group).  Sums accumulate in fp32 (exact for the usual 16-bit keys: the
-// values of one page span few enough binades).  The quotient by the token
-// count is rounded once to the storage type, ties to even: for a full page
-// (n a power of two) the fp32 division is exact, otherwise it runs in fp64
-// (fp64 is slow on this part, so only partial pages take that route).
+// group).  Each lane sums its channels in fp32 from -0.0 (so the sum of
+// keys that are all -0.0 stays -0.0, as IEEE addition of the keys gives),
+// and sums |k| beside it.  Any summation order of n terms in fp32 is within
+// (n - 1) 2^-24 sum|k| of the exact sum; the candidate -- the fp32 sum over
+// n, rounded to the storage type -- is the correctly rounded mean when that
+// whole interval lies strictly inside the candidate's rounding cell (between
+// the midpoints to its neighbours).  That holds for all but a tiny share of
+// channels; the others (a mean near a midpoint, sums that cancel, overflow)
+// are recomputed exactly: the channel's keys re-read, summed as integers in
+// units of 2^-149 (every fp32, f16 and bf16 value is a whole number of
+// them), divided by n by long division, rounded once.
 // last_only: one item per (b, kv head), the page holding the row's last
 // token -- the refresh after an append.
 namespace {
 
+// storage format: significand bits (with the implicit one), and the
+// exponent of the smallest spacing in units of 2^-149
+template <class T> struct Fmt;
+template <> struct Fmt<float> { static constexpr int kP = 24, kTmin = 0; };
+template <> struct Fmt<__half> { static constexpr int kP = 11, kTmin = 125; };
+template <> struct Fmt<__nv_bfloat16> { static constexpr int kP = 8, kTmin = 16; };
+
+// value of a stored key as (sign, integer magnitude, shift): |k| = mag 2^shift
+// units of 2^-149
 template <class T>
-__device__ __forceinline__ uint16_t round16(float x) {
-  if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__float2half_rn(x));
-  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+__device__ __forceinline__ void key_parts(uint32_t bits, uint32_t &neg, uint32_t &mag, int &sh) {
+  if constexpr (sizeof(T) == 4) {
+    const int e = (bits >> 23) & 0xFF;
+    neg = bits >> 31;
+    mag = (bits & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+    sh = max(e, 1) - 1;
+  } else if constexpr (std::is_same<T, __half>::value) {
+    const int e = (bits >> 10) & 0x1F;
+    neg = (bits >> 15) & 1u;
+    mag = (bits & 0x3FFu) | (e ? 0x400u : 0u);
+    sh = max(e, 1) + 124;
+  } else {
+    const int e = (bits >> 7) & 0xFF;
+    neg = (bits >> 15) & 1u;
+    mag = (bits & 0x7Fu) | (e ? 0x80u : 0u);
+    sh = max(e, 1) + 15;
+  }
 }
+
+// exact integer sums: 9 digits of 32 bits (288 bits; n <= 128 keys below
+// 2^128 need 284 bits above 2^-149)
+constexpr int kMeanDigits = 9;
+
+__device__ __noinline__ void digits_add(uint32_t *acc, uint32_t mag, int sh) {
+  const int i = sh >> 5;
+  uint64_t v = (uint64_t)mag << (sh & 31);
+  uint64_t carry = 0;
+  for (int j = i; j < kMeanDigits; ++j) {
+    const uint64_t t = (uint64_t)acc[j] + (v & 0xFFFFFFFFull) + carry;
+    acc[j] = (uint32_t)t;
+    carry = t >> 32;
+    v >>= 32;
+    if (v == 0 && carry == 0) break;
+  }
+}
+
+// 16-bit (or 32-bit) pattern of sign * keep * 2^(t - 149), which is a value of
+// the storage type
 template <class T>
-__device__ __forceinline__ uint16_t round16(double x) {
-  if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__double2half(x));
-  else return __bfloat16_as_ushort(__double2bfloat16(x));
+__device__ __forceinline__ uint32_t pack_value(bool neg, uint32_t keep, int t) {
+  float v = 0.f;
+  if (keep != 0u) {
+    const int k = t - 149;
+    const float p2 = k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+    v = (float)keep * p2;  // exact: the product is a value of the type
+  }
+  if (neg) v = -v;
+  if constexpr (sizeof(T) == 4) return __float_as_uint(v);
+  else if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__float2half_rn(v));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// The exact mean of channel c of the page's n keys, correctly rounded (the
+// rare path: kept out of line).
+template <class T>
+__device__ __noinline__ uint32_t exact_mean(const T *page, int c, int n) {
+  uint32_t pos[kMeanDigits], negd[kMeanDigits];
+  for (int j = 0; j < kMeanDigits; ++j) pos[j] = negd[j] = 0u;
+  bool any_pos_zero = false;
+  for (int r = 0; r < n; ++r) {
+    uint32_t bits;
+    if constexpr (sizeof(T) == 4) bits = __float_as_uint(page[(long long)r * kHeadDim + c]);
+    else bits = reinterpret_cast<const uint16_t *>(page)[(long long)r * kHeadDim + c];
+    uint32_t ng, mag;
+    int sh;
+    key_parts<T>(bits, ng, mag, sh);
+    if (mag == 0u) {
+      any_pos_zero |= ng == 0u;
+      continue;
+    }
+    digits_add(ng ? negd : pos, mag, sh);
+  }
+  // |pos - neg| and its sign
+  int cmp = 0;
+  for (int j = kMeanDigits - 1; j >= 0 && cmp == 0; --j)
+    cmp = pos[j] > negd[j] ? 1 : pos[j] < negd[j] ? -1 : 0;
+  if (cmp == 0) {  // an exact zero: -0 only if every key was -0 (none positive)
+    bool all_neg_zero = !any_pos_zero;
+    for (int r = 0; r < n && all_neg_zero; ++r) {
+      uint32_t bits;
+      if constexpr (sizeof(T) == 4) bits = __float_as_uint(page[(long long)r * kHeadDim + c]);
+      else bits = reinterpret_cast<const uint16_t *>(page)[(long long)r * kHeadDim + c];
+      uint32_t ng, mag;
+      int sh;
+      key_parts<T>(bits, ng, mag, sh);
+      all_neg_zero = mag == 0u && ng;
+    }
+    return pack_value<T>(all_neg_zero, 0u, 0);
+  }
+  const bool neg = cmp < 0;
+  uint32_t *a = neg ? negd : pos;
+  const uint32_t *b = neg ? pos : negd;
+  uint64_t borrow = 0;
+  for (int j = 0; j < kMeanDigits; ++j) {
+    const uint64_t t = (uint64_t)a[j] - b[j] - borrow;
+    a[j] = (uint32_t)t;
+    borrow = (t >> 63) & 1u;
+  }
+  // quotient by n, remainder
+  uint64_t rem = 0;
+  for (int j = kMeanDigits - 1; j >= 0; --j) {
+    const uint64_t cur = (rem << 32) | a[j];
+    a[j] = (uint32_t)(cur / (uint64_t)n);
+    rem = cur % (uint64_t)n;
+  }
+  int bitlen = 0;
+  for (int j = kMeanDigits - 1; j >= 0; --j)
+    if (a[j]) {
+      bitlen = 32 * j + 32 - __clz(a[j]);
+      break;
+    }
+  auto qbit = [&](int i) -> uint32_t { return i < 0 ? 0u : (a[i >> 5] >> (i & 31)) & 1u; };
+  const int t = max(Fmt<T>::kTmin, bitlen - Fmt<T>::kP);
+  uint32_t keep = 0u;
+  for (int i = bitlen - 1; i >= t; --i) keep = (keep << 1) | qbit(i);
+  bool up;
+  if (t == 0) {  // the spacing is the unit: the remainder decides
+    up = 2 * rem > (uint64_t)n || (2 * rem == (uint64_t)n && (keep & 1u));
+  } else {
+    bool sticky = rem != 0;
+    for (int i = t - 2; i >= 0 && !sticky; --i) sticky = qbit(i) != 0u;
+    up = qbit(t - 1) && (sticky || (keep & 1u));
+  }
+  return pack_value<T>(neg, keep + (up ? 1u : 0u), t);
 }
 
 template <class T>
-__device__ __forceinline__ void store_mean(T *dst, const float (&s)[16 / sizeof(T)], int n) {
-  constexpr int E = 16 / sizeof(T);
+__device__ __forceinline__ double stored_value(uint32_t bits) {
+  if constexpr (sizeof(T) == 4) return (double)__uint_as_float(bits);
+  else if constexpr (std::is_same<T, __half>::value)
+    return (double)__half2float(__ushort_as_half((unsigned short)bits));
+  else return (double)__uint_as_float(bits << 16);
+}
+
+// the adjacent pattern of the type towards +inf (up) or -inf (down)
+template <class T>
+__device__ __forceinline__ uint32_t neighbour(uint32_t bits, bool up) {
+  constexpr uint32_t kSign = sizeof(T) == 4 ? 0x80000000u : 0x8000u;
+  if (bits == kSign) return up ? 1u : kSign | 1u;  // -0
+  if (bits == 0u) return up ? 1u : kSign | 1u;      // +0
+  const bool neg = (bits & kSign) != 0u;
+  return (up != neg) ? bits + 1u : bits - 1u;
+}
+
+// The mean of one channel from its fp32 sum s and sum of magnitudes a: the
+// correctly rounded pattern when the error bound settles it, else ~0u (the
+// exact path decides).  Patterns of the type never equal ~0u (it would be a
+// NaN of fp32, and 16-bit patterns are below 2^16).
+template <class T>
+__device__ __forceinline__ uint32_t fast_mean(float s, float a, int n) {
+  if (!isfinite(s) || !isfinite(a)) return ~0u;
+  if (a == 0.f) return pack_value<T>(signbit(s), 0u, 0);  // every key is a zero
   const bool pow2 = (n & (n - 1)) == 0;
-  const float inv = 1.0f / (float)n;  // exact for a power of two
+  uint32_t r;
   if constexpr (sizeof(T) == 4) {
-    float o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = pow2 ? s[j] * inv : (float)((double)s[j] / n);
-    *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+    r = __float_as_uint(pow2 ? s * (1.0f / (float)n) : (float)((double)s / n));
+  } else if constexpr (std::is_same<T, __half>::value) {
+    r = __half_as_ushort(pow2 ? __float2half_rn(s * (1.0f / (float)n))
+                              : __double2half((double)s / n));
   } else {
-    uint32_t w[E / 2];
-#pragma unroll
-    for (int j = 0; j < E / 2; ++j) {
-      uint16_t lo, hi;
-      if (pow2) {
-        lo = round16<T>(s[2 * j] * inv);
-        hi = round16<T>(s[2 * j + 1] * inv);
-      } else {
-        lo = round16<T>((double)s[2 * j] / n);
-        hi = round16<T>((double)s[2 * j + 1] / n);
-      }
-      w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
-    }
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    r = __bfloat16_as_ushort(pow2 ? __float2bfloat16_rn(s * (1.0f / (float)n))
+                                  : __double2bfloat16((double)s / n));
   }
+  const double sd = (double)s;
+  // error bound of the fp32 sums, with room for this check's own roundings
+  const double err = (double)a * (n * 0x1p-24) * (1.0 + 0x1p-10) + fabs(sd) * 0x1p-50;
+  const double rv = stored_value<T>(r);
+  const double lo = n * ((rv + stored_value<T>(neighbour<T>(r, false))) * 0.5);
+  const double hi = n * ((rv + stored_value<T>(neighbour<T>(r, true))) * 0.5);
+  if (!(sd - err > lo && sd + err < hi)) return ~0u;
+  if (rv == 0.0) {  // a zero: its sign is the exact mean's, which must be settled
+    if (sd > err) return pack_value<T>(false, 0u, 0);
+    if (sd < -err) return pack_value<T>(true, 0u, 0);
+    return ~0u;
+  }
+  return r;
 }
 
 template <class T>
@@ -499,10 +655,14 @@ __global__ void __launch_bounds__(256)
     return;
   }
   const int chunk = lane % C, rg = lane / C;
-  const uint4 *src = reinterpret_cast<const uint4 *>(k) + ((phys * Hkv + kvh) * ps) * C + chunk;
-  float s[E];
+  const T *page = k + ((phys * Hkv + kvh) * ps) * kHeadDim;
+  const uint4 *src = reinterpret_cast<const uint4 *>(page) + chunk;
+  float s[E], a[E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) s[e] = 0.f;
+  for (int e = 0; e < E; ++e) {
+    s[e] = -0.f;
+    a[e] = 0.f;
+  }
 #pragma unroll 4
   for (int r = rg; r < n; r += RG) {
     const uint4 x = src[(long long)r * C];
@@ -513,19 +673,42 @@ __global__ void __launch_bounds__(256)
         const float2 f = unpack2(w[j], T());
         s[2 * j] += f.x;
         s[2 * j + 1] += f.y;
+        a[2 * j] += fabsf(f.x);
+        a[2 * j + 1] += fabsf(f.y);
       }
     } else {
-      s[0] += __uint_as_float(x.x); s[1] += __uint_as_float(x.y);
-      s[2] += __uint_as_float(x.z); s[3] += __uint_as_float(x.w);
+      const float f[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                          __uint_as_float(x.w)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s[j] += f[j];
+        a[j] += fabsf(f[j]);
+      }
     }
   }
   pdl_trigger();
   if constexpr (RG == 2) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) s[e] += __shfl_xor_sync(0xFFFFFFFFu, s[e], 16);
+    for (int e = 0; e < E; ++e) {
+      s[e] += __shfl_xor_sync(0xFFFFFFFFu, s[e], 16);
+      a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
+    }
   }
-  if (rg == 0)
-    store_mean<T>(mean + (phys * Hkv + kvh) * kHeadDim + chunk * E, s, n);
+  if (rg != 0) return;
+  uint32_t out[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    out[e] = fast_mean<T>(s[e], a[e], n);
+    if (out[e] == ~0u) out[e] = exact_mean<T>(page, chunk * E + e, n);
+  }
+  T *dst = mean + (phys * Hkv + kvh) * kHeadDim + chunk * E;
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+  } else {
+    *reinterpret_cast<uint4 *>(dst) =
+        make_uint4(out[0] | (out[1] << 16), out[2] | (out[3] << 16), out[4] | (out[5] << 16),
+                   out[6] | (out[7] << 16));
+  }
 }
 
 }  // namespace

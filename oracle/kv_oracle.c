@@ -148,16 +148,108 @@ double okv_round_to_dtype(int dtype, double x) {
   return ldexp(r, qexp);
 }
 
-/* Mean of the page's n valid keys, channel by channel, in fp64 (the sums of
- * stored elements are exact here), then rounded once to the storage type.
+/* Exact sums of stored keys.  Every finite fp32, f16 and bf16 value is an
+ * integer multiple of 2^-160 (the smallest subnormals are 2^-149, 2^-24 and
+ * 2^-133) and below 2^128 in magnitude, so a sum of at most 128 of them is
+ * an integer multiple of 2^-160 below 2^135: 295 bits.  It is held in ten
+ * base-2^32 digits; a digit (an int64) takes at most 3 * 128 additions of
+ * values below 2^32 before its carries are propagated, so it cannot
+ * overflow. */
+#define OKV_DIGITS 10
+#define OKV_UNIT 160 /* the fixed point: value = sum_i digit[i] 2^(32 i - 160) */
+
+static void fix_add(int64_t *dig, double x) {
+  if (x == 0.0) return;
+  int e;
+  double f = frexp(fabs(x), &e);           /* |x| = f 2^e, f in [0.5, 1) */
+  uint64_t m = (uint64_t)ldexp(f, 53);     /* |x| = m 2^(e - 53), m < 2^53 */
+  int k = e - 53 + OKV_UNIT;               /* |x| = m 2^k units */
+  while (k < 0) {                          /* only zero bits fall off (see above) */
+    m >>= 1;
+    ++k;
+  }
+  const int i = k / 32, r = k % 32;
+  const int64_t sgn = x < 0 ? -1 : 1;
+  const uint64_t lo = m & 0xFFFFFFFFull, hi = m >> 32; /* hi < 2^21 */
+  const uint64_t a = lo << r, b = hi << r;             /* a < 2^63, b < 2^52 */
+  dig[i] += sgn * (int64_t)(a & 0xFFFFFFFFull);
+  dig[i + 1] += sgn * (int64_t)(a >> 32);
+  dig[i + 1] += sgn * (int64_t)(b & 0xFFFFFFFFull);
+  dig[i + 2] += sgn * (int64_t)(b >> 32);
+}
+
+/* Correctly rounded (to nearest, ties to even) mean sum / n of the exact
+ * sum in dig, in the storage type: the magnitude by long division, then one
+ * rounding to the type's significand at the exponent of the quotient (not
+ * below the type's smallest subnormal spacing).  An exact zero sum gives
+ * +0.0, or -0.0 when every summed key was -0.0 (IEEE addition's rule). */
+static double fix_mean(int64_t *dig, int n, int dtype, int all_neg_zero) {
+  /* carries: digits 0..8 into [0, 2^32), digit 9 signed */
+  for (int i = 0; i < OKV_DIGITS - 1; ++i) {
+    const int64_t low = dig[i] & 0xFFFFFFFFll;
+    const int64_t carry = (dig[i] - low) / 4294967296ll;
+    dig[i] = low;
+    dig[i + 1] += carry;
+  }
+  const int neg = dig[OKV_DIGITS - 1] < 0;
+  uint64_t mag[OKV_DIGITS];
+  if (neg) { /* magnitude = two's complement of the digits */
+    uint64_t carry = 1;
+    for (int i = 0; i < OKV_DIGITS; ++i) {
+      const uint64_t v = (~(uint64_t)dig[i] & 0xFFFFFFFFull) + carry;
+      mag[i] = v & 0xFFFFFFFFull;
+      carry = v >> 32;
+    }
+  } else {
+    for (int i = 0; i < OKV_DIGITS; ++i) mag[i] = (uint64_t)dig[i];
+  }
+  /* quotient and remainder of the magnitude by n */
+  uint64_t q[OKV_DIGITS], rem = 0;
+  for (int i = OKV_DIGITS - 1; i >= 0; --i) {
+    const uint64_t cur = (rem << 32) | mag[i];
+    q[i] = cur / (uint64_t)n;
+    rem = cur % (uint64_t)n;
+  }
+  int bits = 0; /* bit length of q */
+  for (int i = OKV_DIGITS - 1; i >= 0 && bits == 0; --i)
+    for (int j = 31; j >= 0; --j)
+      if ((q[i] >> j) & 1u) {
+        bits = 32 * i + j + 1;
+        break;
+      }
+  if (bits == 0 && rem == 0) return (all_neg_zero) ? -0.0 : 0.0;
+  /* significand bits p and the smallest spacing 2^(emin - p + 1) */
+  const int p = dtype == OKV_F32 ? 24 : dtype == OKV_F16 ? 11 : 8;
+  const int emin = dtype == OKV_F16 ? -14 : -126;
+  int t = emin - p + 1 + OKV_UNIT; /* spacing of the result, in units: 2^t */
+  if (bits - p > t) t = bits - p;
+#define QBIT(b) ((int)((q[(b) / 32] >> ((b) % 32)) & 1u))
+  uint64_t keep = 0;
+  for (int b = bits - 1; b >= t; --b) keep = (keep << 1) | (uint64_t)QBIT(b);
+  const int round = QBIT(t - 1);
+  int sticky = rem != 0;
+  for (int b = t - 2; b >= 0 && !sticky; --b) sticky = QBIT(b);
+#undef QBIT
+  if (round && (sticky || (keep & 1u))) keep += 1;
+  const double v = ldexp((double)keep, t - OKV_UNIT);
+  return neg ? -v : v;
+}
+
+/* Mean of the page's n valid keys, channel by channel: the exact sum of the
+ * stored elements, divided by n and rounded once to the storage type.
  * ShadowKV-style spatial chunking (KVDrive, sections 2.3 and 3, and the
  * design overview: each page's mean key is its representative, half the
  * index bytes of the min/max pair). */
 void okv_page_mean(int dtype, int d, int n, const void *k, int64_t off, double *mean) {
   for (int c = 0; c < d; ++c) {
-    double sum = 0.0;
-    for (int t = 0; t < n; ++t) sum += okv_decode(dtype, k, off + (int64_t)t * d + c);
-    mean[c] = okv_round_to_dtype(dtype, sum / n);
+    int64_t dig[OKV_DIGITS] = {0};
+    int all_neg_zero = 1;
+    for (int t = 0; t < n; ++t) {
+      const double x = okv_decode(dtype, k, off + (int64_t)t * d + c);
+      if (!(x == 0.0 && signbit(x))) all_neg_zero = 0;
+      fix_add(dig, x);
+    }
+    mean[c] = fix_mean(dig, n, dtype, all_neg_zero);
   }
 }
 

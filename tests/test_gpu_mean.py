@@ -1,12 +1,13 @@
 """GPU parity of the mean-key page index against the fp64 oracle.
 
 Bars:
-  * mean table: each entry is the oracle's correctly rounded mean or one unit
-    in the last place of the storage type away (the GPU sums in fp32, the
-    oracle in fp64); for 16-bit keys at least 99.9% of the entries are
-    bit-exact.  fp32 keys add the fp32 summation bound n * 2^-24 * mean |k|;
-  * scores: |gpu - oracle| <= 1e-5 * sum_c |q_c m_c| + sum_c |q_c| * |dm_c|,
-    dm the table difference;
+  * mean table: bit-exact -- every entry is the exact mean of the page's valid
+    keys rounded once to the storage type, as the oracle computes it with
+    integer arithmetic -- for every storage type, on the workloads' values and
+    on adversarial pages (keys spanning every binade of the type, sums that
+    cancel, ties, signed zeros, partial pages);
+  * scores: |gpu - oracle| <= 1e-5 * sum_c |q_c m_c| (+ sum_c |q_c| |dm_c|,
+    dm the table difference, which the table bar makes zero);
   * top-K through the pipeline: sets differ only by pages whose oracle score
     is within the two pages' score tolerances of the K-th score;
   * sparse attention over the oracle's selection: the usual 2e-3 / 1e-5.
@@ -59,15 +60,8 @@ def check_mean_table(layer, wl, rows=None):
     gpu = bits_to_f64(layer.mean_bits(), dtype)
     pages = referenced_pages(wl, rows)
     r, g = ref[pages], gpu[pages]
-    exact = g == r
-    tol = ulp(r, dtype)
-    if dtype == "f32":
-        kabs = np.abs(W.storage_to_f64(wl.k_cache[pages], dtype)).mean(axis=2)   # [pages][Hkv][d]
-        tol = tol + spec.page_size * 2.0 ** -24 * kabs
-    assert (np.abs(g - r) <= tol).all()
-    if dtype != "f32":
-        print(f"mean table {dtype}: {exact.mean():.6f} of {exact.size} entries bit-exact")
-        assert exact.mean() >= 0.999, exact.mean()
+    # bit for bit, signed zeros included
+    assert np.array_equal(g, r) and np.array_equal(np.signbit(g), np.signbit(r))
     return ref, gpu
 
 
@@ -155,6 +149,73 @@ def test_mean_index_host_pinned():
     wl = W.generate(spec, context_lens=[16 * 40 + 9, 16 * 7])
     layer = run_mean_pipeline(wl, 5, kv_loc="host")
     assert not layer.k_cache.is_cuda
+
+
+def _wide_keys(rng, dtype, shape):
+    """Keys whose magnitudes span every binade of the type, in the storage
+    type; a page's first and last tokens cancel each other around the rest."""
+    lo, hi = {"f16": (-24, 15), "bf16": (-133, 127), "f32": (-149, 127)}[dtype]
+    e = rng.integers(lo, hi + 1, shape)
+    x = np.ldexp(rng.uniform(1.0, 2.0, shape), e) * rng.choice([-1.0, 1.0], shape)
+    cap = 6e4 if dtype == "f16" else 3e38
+    x = np.clip(x, -cap, cap)
+    big = np.ldexp(1.5, hi - 2)
+    x[..., 0, :] = big * np.sign(x[..., 0, :])
+    x[..., -1, :] = -x[..., 0, :]
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "f32":
+        return x.astype(np.float32)
+    return W.f32_to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("ps", [16, 64])
+def test_mean_table_is_exact_on_adversarial_pages(dtype, ps):
+    # every page of every row gets wide-range keys; the rows' lengths leave
+    # partial last pages (n = 1, a ragged n, a full page)
+    rng = np.random.default_rng(4000 + ps)
+    ctx = [ps * 5 + 1, ps * 3 + ps // 2 + 3, ps * 2]
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=4, hkv=2, context=max(ctx), ps=ps,
+                       index=4000 + ps)
+    wl = W.generate(spec, context_lens=ctx)
+    wl.k_cache[...] = _wide_keys(rng, dtype, wl.k_cache.shape)
+    # hand-made channels: f16 subnormals next to +-6e4, exact ties, signed zeros
+    ph = int(wl.block_table[0, 0])
+    special = {
+        "f16": [65504.0, 2.0 ** -24, 3 * 2.0 ** -24, -65504.0],
+        "bf16": [2.0 ** 120, 2.0 ** -130, 2.0 ** -100, -(2.0 ** 120)],
+        "f32": [2.0 ** 100, 2.0 ** -149, 1.0, -(2.0 ** 100)],
+    }[dtype]
+    col = np.zeros(ps)
+    col[:4] = special
+    wl.k_cache[ph, 0, :, 0] = W.to_storage(col.astype(np.float32), dtype) if dtype != "f16" \
+        else col.astype(np.float16)
+    wl.k_cache[ph, 0, :, 1] = W.to_storage(np.full(ps, -0.0, dtype=np.float32), dtype) \
+        if dtype != "f16" else np.full(ps, -0.0, dtype=np.float16)
+    tie = np.zeros(ps)         # mean 1.5 smallest subnormals: a tie, to the even 2
+    tie[0] = 1.5 * ps * {"f16": 2.0 ** -24, "bf16": 2.0 ** -133, "f32": 2.0 ** -149}[dtype]
+    wl.k_cache[ph, 0, :, 2] = W.to_storage(tie.astype(np.float32), dtype) if dtype != "f16" \
+        else tie.astype(np.float16)
+    layer = DecodeLayer(wl, topk=2)
+    layer.build_mean_index()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    ref, gpu = check_mean_table(layer, wl)
+    r0 = ref[ph, 0]
+    assert np.signbit(r0[1]) and r0[1] == 0.0             # all -0 keys: -0
+    assert r0[2] == 2 * {"f16": 2.0 ** -24, "bf16": 2.0 ** -133, "f32": 2.0 ** -149}[dtype]
+    # refresh of the last pages after the keys change agrees too
+    wl.k_cache[...] = _wide_keys(rng, dtype, wl.k_cache.shape)
+    layer.k_cache.copy_(storage_to_torch(wl.k_cache, dtype).cuda())
+    layer.build_mean_index(last_only=True)
+    torch.cuda.synchronize()
+    full = oracle.mean_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
+    gpu = bits_to_f64(layer.mean_bits(), dtype)
+    for b, L in enumerate(ctx):
+        p_last = int(wl.block_table[b, (L - 1) // ps])
+        assert np.array_equal(gpu[p_last], full[p_last])
+        assert np.array_equal(np.signbit(gpu[p_last]), np.signbit(full[p_last]))
 
 
 def test_mean_refresh_after_appends():

@@ -617,6 +617,102 @@ def test_page_mean_matches_numpy_mean_then_rounding(dtype):
         assert np.array_equal(got, ref), (ps, n)
 
 
+def _format_table(dtype):
+    """Every finite value of a 16-bit format as exact fp64, sorted, with its
+    bit pattern (-0.0 dropped: +0.0 stands for zero)."""
+    bits = np.arange(65536, dtype=np.uint32)
+    if dtype == "bf16":
+        finite = ((bits >> 7) & 0xFF) != 0xFF
+        vals = (bits[finite] << 16).view(np.float32).astype(np.float64)
+    else:
+        finite = ((bits >> 10) & 0x1F) != 0x1F
+        vals = bits[finite].astype(np.uint16).view(np.float16).astype(np.float64)
+    b = bits[finite]
+    keep = ~((vals == 0) & (b >= 0x8000))
+    order = np.argsort(vals[keep], kind="stable")
+    return vals[keep][order], b[keep][order]
+
+
+def _exact_mean_rounded(dtype, xs, table=None):
+    """The mean of xs (exact stored values) from rational arithmetic, rounded
+    to the nearest value of the type by brute force over its neighbours, ties
+    to the even bit pattern; an exact zero is +0 unless every x is -0, a
+    non-zero mean that rounds to zero keeps its sign."""
+    from fractions import Fraction
+    import math
+    mu = sum(Fraction(float(x)) for x in xs) / len(xs)
+    if mu == 0:
+        return -0.0 if all(x == 0 and math.copysign(1.0, x) < 0 for x in xs) else 0.0
+    if dtype == "f32":
+        c = np.float32(float(mu))
+        cands = {c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(-np.inf))}
+        cands = [(float(v), int(np.float32(v).view(np.uint32))) for v in cands if np.isfinite(v)]
+    else:
+        vals, bits = table
+        j = int(np.searchsorted(vals, float(mu)))
+        cands = [(float(vals[i]), int(bits[i])) for i in range(j - 2, j + 2) if 0 <= i < vals.size]
+    best = min(cands, key=lambda vb: (abs(Fraction(vb[0]) - mu), vb[1] & 1))
+    v = best[0]
+    return math.copysign(0.0, float(mu)) if v == 0 else v
+
+
+def _wide_values(rng, dtype, n):
+    """n stored values whose magnitudes span the type's whole range, with
+    cancelling pairs, as a storage array [n]."""
+    lo, hi = {"f16": (-24, 15), "bf16": (-133, 127), "f32": (-149, 127)}[dtype]
+    e = rng.integers(lo, hi + 1, n)
+    x = np.ldexp(rng.uniform(1.0, 2.0, n), e) * rng.choice([-1.0, 1.0], n)
+    if n >= 3:                       # a large pair that cancels exactly, around the rest
+        x[0] = np.ldexp(1.5, hi - 2) * np.sign(x[0])
+        x[-1] = -x[0]
+    x = np.clip(x, -6e4 if dtype == "f16" else -3e38, 6e4 if dtype == "f16" else 3e38)
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "f32":
+        return x.astype(np.float32)
+    return W.f32_to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_page_mean_is_the_correctly_rounded_exact_mean_on_wide_pages(dtype):
+    # keys spanning every binade of the type, cancelling pairs, partial pages:
+    # an fp32 (or fp64) running sum is not exact here, the exact mean is
+    rng = _rng(83)
+    table = None if dtype == "f32" else _format_table(dtype)
+    for n in (1, 2, 3, 5, 16, 33, 64, 128):
+        cols = np.stack([_wide_values(rng, dtype, n) for _ in range(24)], axis=1)   # [n][24]
+        got = oracle.page_mean(dtype, cols, n)
+        vals = W.storage_to_f64(cols, dtype)
+        for c in range(cols.shape[1]):
+            ref = _exact_mean_rounded(dtype, vals[:, c], table)
+            assert got[c] == ref and np.signbit(got[c]) == np.signbit(ref), (n, c)
+
+
+def test_page_mean_hand_worked_edge_cases():
+    import math
+    f16 = lambda *v: np.array(v, dtype=np.float16).reshape(-1, 1)
+    mean = lambda a, dt="f16": float(oracle.page_mean(dt, a, a.shape[0])[0])
+    # the f16 extremes cancel; a third of the smallest subnormal rounds to +0
+    assert mean(f16(65504, -65504, 2.0 ** -24)) == 0.0
+    # two thirds of it rounds up to the smallest subnormal
+    assert mean(f16(65504, -65504, 2.0 ** -23)) == 2.0 ** -24
+    # halfway between two subnormals: ties to the even one
+    assert mean(f16(2.0 ** -24, 2.0 ** -23)) == 2.0 ** -23     # 1.5 units -> 2 units
+    assert mean(f16(2.0 ** -24, 0.0)) == 0.0                   # 0.5 units -> 0
+    # signed zeros: -0 only when every key is -0; a negative mean keeps its sign
+    assert math.copysign(1.0, mean(f16(-0.0, -0.0))) < 0
+    assert math.copysign(1.0, mean(f16(-0.0, 0.0))) > 0
+    assert math.copysign(1.0, mean(f16(1.0, -1.0))) > 0
+    assert math.copysign(1.0, mean(f16(-(2.0 ** -24), 0.0, 0.0))) < 0
+    # bf16: 2^100 cancels, the 2^-100 terms between survive exactly
+    b = W.f32_to_bf16_bits(np.array([2.0 ** 100, 2.0 ** -100, 2.0 ** -100, -(2.0 ** 100)],
+                                    dtype=np.float32)).reshape(-1, 1)
+    assert mean(b, "bf16") == 2.0 ** -101
+    # fp32: 2^60 + 1 - 2^60 = 1, over 3 tokens; 1/3 to the nearest fp32
+    f = np.array([2.0 ** 80, 1.0, -(2.0 ** 80)], dtype=np.float32).reshape(-1, 1)
+    assert mean(f, "f32") == float(np.float32(1.0 / 3.0))
+
+
 def test_mean_build_indirection_partial_pages_and_identical_keys():
     spec = W.tiny_spec(dtype="f16", batch=3, hq=4, hkv=2, context=70, ps=16, index=82)
     wl = W.generate(spec, context_lens=[70, 33, 16])
