@@ -83,27 +83,38 @@ def dense_bytes(spec, ctx):
     return kv + q + out + 4 * pages + 4 * spec.batch
 
 
-def sparse_bytes(spec, ctx, indices, table_rows=2):
+def sparse_bytes(spec, ctx, indices, table_rows=2, lists=False, scores_in_memory=True):
     """(step bytes, attention bytes): score + select + attention over the union
     of each (sequence, kv head) group's selected pages.  table_rows: 2 for the
-    min/max index, 1 for the mean-key index."""
+    min/max index, 1 for the mean-key index.  lists=False: the separate calls
+    (the attention reads the selection and builds the unions); lists=True:
+    kv_select_pages writes the unions as 8-byte entries that the attention
+    reads instead.  scores_in_memory: the scores pass through memory (written,
+    then read by the select); the one-launch selection keeps them on chip."""
     e = spec.elem_bytes
     B, Hq, Hkv, d, ps = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
     G = spec.group
     P = -(-np.asarray(ctx) // ps)
     table = int(np.sum(P)) * Hkv * table_rows * d * e        # index read by the page score
-    scores = 2 * B * Hq * spec.max_pages * 4                 # written, then read by top-K
+    scores = 2 * B * Hq * spec.max_pages * 4 if scores_in_memory else 0
     idx_w = B * Hq * indices.shape[-1] * 4                   # written by top-K
-    idx_r = B * Hq * indices.shape[-1] * 4                   # read by the union step
     kv = 0
+    upages = 0
     for b in range(B):
         for kvh in range(Hkv):
             sel = indices[b, kvh * G:(kvh + 1) * G].reshape(-1)
             for p in np.unique(sel[sel >= 0]):
                 n = min(ps, int(ctx[b]) - int(p) * ps)
                 kv += 2 * n * d * e
+                upages += 1
     q = B * Hq * d * e
     out = B * Hq * d * 4
+    if lists:
+        # the select also reads each scored page's block-table entry
+        bt = int(np.sum(P)) * 4
+        attn = 8 * upages + kv + q + out
+        return table + bt + q + scores + idx_w + 8 * upages + attn, attn
+    idx_r = B * Hq * indices.shape[-1] * 4                   # read by the union step
     attn = idx_r + kv + q + out
     return table + q + scores + idx_w + attn, attn
 
@@ -419,6 +430,18 @@ def timed_stages(layer, copies, fns, k, warm, ws=1):
     return total, per
 
 
+STEP_NAME = ("kv_select_pages (page score + top-K + group unions) + "
+             "kv_sparse_decode_attn_selected (attention + split combine)")
+
+
+def scores_in_memory(layer):
+    """Whether kv_select_pages passes the scores through its workspace (the
+    page-score kernel first) rather than keeping them on chip."""
+    from offloaded_kv_cache_gb300 import kvsparse as kv
+    k = layer.topk
+    return kv.kv_select_workspace_bytes(layer.shape, k) > kv.kv_attn_workspace_bytes(layer.shape, k)
+
+
 def kv_copies_for(spec):
     """Rotating K/V copies so that one pass over them exceeds 4x the L2."""
     l2_bytes = 129 * 2**20
@@ -467,9 +490,11 @@ def side_workload(name, steps, warm):
     layer.select()
     torch.cuda.synchronize()
     assert kv.kv_device_status() == kv.KV_OK
-    step_bytes, attn_bytes = sparse_bytes(spec, wl.context_lens, layer.indices.cpu().numpy())
-    stages = [("page_score", layer.score), ("topk_select", layer.select),
-              ("sparse_attn", lambda: layer.sparse_attn())]
+    layer.select_fused()
+    torch.cuda.synchronize()
+    step_bytes, attn_bytes = sparse_bytes(spec, wl.context_lens, layer.indices.cpu().numpy(),
+                                          lists=True, scores_in_memory=scores_in_memory(layer))
+    stages = [("select_pages", layer.select_fused), ("sparse_attn", layer.sparse_attn_selected)]
     total, per = timed_stages(layer, copies, stages, steps, warm)
     ms = total / steps
     if spec.kv_loc == "host":
@@ -482,7 +507,7 @@ def side_workload(name, steps, warm):
         peak, kind = measured_peaks()
         bound, peak_source = "hbm", f"MEASURED_PEAKS.json hbm_gbs ({kind})"
     achieved = attn_bytes / (per["sparse_attn"] * 1e-3) / 1e9
-    res = {"step": "score + top-K + sparse attention", "steps": steps,
+    res = {"step": STEP_NAME, "steps": steps,
            "ms_per_step": round(ms, 5),
            "value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "step_bytes": int(step_bytes),
@@ -635,18 +660,21 @@ def main():
     # index (built once per page; timed separately below)
     layer.build_index()
     if sparse:
-        layer.score()
-        layer.select()
+        layer.select_fused()
     torch.cuda.synchronize()
     assert kv.kv_device_status() == kv.KV_OK
 
     splits = kv.kv_attn_num_splits(layer.shape, spec.topk if sparse else 0)
     if sparse:
         idx_np = layer.indices.cpu().numpy()
-        step_bytes, attn_bytes = sparse_bytes(spec, ctx, idx_np)
-        stages = [("page_score", layer.score), ("topk_select", layer.select),
-                  ("sparse_attn", lambda: layer.sparse_attn())]
-        launches_per_step = 2 + 1 + 1 + (1 if splits > 1 else 0)   # score, top-K, union, attn, combine
+        sim = scores_in_memory(layer)
+        step_bytes, attn_bytes = sparse_bytes(spec, ctx, idx_np, lists=True,
+                                              scores_in_memory=sim)
+        stages = [("select_pages", layer.select_fused),
+                  ("sparse_attn", layer.sparse_attn_selected)]
+        # selection (the page-score kernel too when the scores pass through
+        # memory), attention, combine
+        launches_per_step = (2 if sim else 1) + 1 + (1 if splits > 1 else 0)
         dominant = "sparse_attn"
     else:
         step_bytes = dense_bytes(spec, ctx)
@@ -686,6 +714,17 @@ def main():
     extra = {}
     if sparse:
         extra["stages_ms"] = {n: round(v, 5) for n, v in per_stage.items()}
+        # the same step through the separate calls: kv_page_score,
+        # kv_topk_select, kv_sparse_decode_attn (which builds the unions)
+        n_sep = max(3, args.steps // 4)
+        sep_total, sep_per = timed([("page_score", layer.score), ("topk_select", layer.select),
+                                    ("sparse_attn", lambda: layer.sparse_attn())], n_sep, 3)
+        sep_bytes, sep_attn = sparse_bytes(spec, ctx, layer.indices.cpu().numpy())
+        extra["separate_calls"] = {
+            "ms_per_step": round(sep_total / n_sep, 5),
+            "GB_s": round(sep_bytes / (sep_total / n_sep * 1e-3) / 1e9, 2),
+            "stages_ms": {n: round(v, 5) for n, v in sep_per.items()}}
+        layer.select_fused()
         # selection with the sink (first 4 tokens) and local (last 64 tokens)
         # pages forced in, the same budget
         f_total, _ = timed([("topk_forced", lambda: layer.select(sink_tokens=4, local_tokens=64))],
@@ -822,8 +861,7 @@ def main():
                        "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
                        "context": spec.context, "page_size": spec.page_size,
                        "topk": spec.topk, "kv_loc": spec.kv_loc, "accumulate": "f32",
-                       "step": ("score + top-K + sparse attention" if sparse
-                                else "dense attention"),
+                       "step": (STEP_NAME if sparse else "dense attention"),
                        "l2": (f"{copies} rotating K/V copies of {spec.kv_bytes() / 2**20:.0f} MiB "
                               f"each (> 4x the 129 MB L2 in total)" if copies > 1 else
                               "K/V larger than L2"),
@@ -835,7 +873,7 @@ def main():
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          **({"link_traffic": link_traffic} if spec.kv_loc == "host" else {}),
-                         "kernel": ("kv_sparse_decode_attn (union + attention + combine)" if sparse
+                         "kernel": ("kv_sparse_decode_attn_selected (attention + combine)" if sparse
                                     else "kv_dense_decode_attn (attention"
                                     + (" + combine)" if splits > 1 else ")")),
                          "peak_source": peak_source},

@@ -224,6 +224,37 @@ int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_ca
                           float scale, float *out, void *workspace, size_t workspace_bytes,
                           void *stream);
 
+/* Page selection and the attention's page lists in one call: the result of
+ * kv_page_score followed by kv_topk_select_forced (sink_tokens = local_tokens
+ * = 0: plain kv_topk_select) -- the same indices[b][h][0 .. k) -- without the
+ * scores passing through memory (KVDrive, section 2.3 steps (1)-(2): the
+ * selection reads only the GPU-resident index; section 3, finding 2: the
+ * selection is a large share of decode time).  For 16-bit data with G = 4 or
+ * 8 it is one launch: a cluster of G CTAs per (sequence, kv head), each
+ * scoring 1/G of the pages for the whole group, keeping every head's scores
+ * on chip, selecting one head's pages and building the group's union of
+ * selected pages; other shapes run the separate kernels.  The union lists
+ * stay in `workspace` for kv_sparse_decode_attn_selected, which must follow
+ * on the same stream with the same shape, k, block_table, context_lens and
+ * workspace (the lists hold physical pages).  The workspace must hold
+ * kv_select_workspace_bytes(shape, k) bytes (at least
+ * kv_attn_workspace_bytes(shape, k)).  Errors as kv_page_score and
+ * kv_topk_select_forced, and KV_ERR_WORKSPACE. */
+size_t kv_select_workspace_bytes(const kv_shape *shape, int32_t k);
+int kv_select_pages(const kv_shape *shape, const void *q, const void *minmax,
+                    const int32_t *block_table, const int32_t *context_lens, int32_t k,
+                    int32_t sink_tokens, int32_t local_tokens, int32_t *indices,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Sparse decode attention over the pages the preceding kv_select_pages call
+ * chose: the same out as kv_sparse_decode_attn with that call's indices.
+ * The workspace is the one kv_select_pages filled, unchanged since. */
+int kv_sparse_decode_attn_selected(const kv_shape *shape, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_table,
+                                   const int32_t *context_lens, int32_t k, float scale,
+                                   float *out, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
 /* Dense decode attention: as kv_sparse_decode_attn over every page p < P_b
  * (Dual-Blade, "Background and key observations"). */
 int kv_dense_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
@@ -266,9 +297,11 @@ int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink
                          int32_t sink_words, void *stream);
 
 /* One decode step of one layer on host buffers: q and context_lens come from
- * host memory, the path runs (k > 0: kv_page_score, kv_topk_select,
- * kv_sparse_decode_attn; k == 0: kv_dense_decode_attn) and out lands in host
- * memory, all asynchronous on `stream`.  A host buffer the device has mapped
+ * host memory, the path runs (k > 0: kv_select_pages and
+ * kv_sparse_decode_attn_selected when workspace_bytes >=
+ * kv_select_workspace_bytes(shape, k), else kv_page_score into `scores`,
+ * kv_topk_select, kv_sparse_decode_attn; k == 0: kv_dense_decode_attn) and
+ * out lands in host memory, all asynchronous on `stream`.  A host buffer the device has mapped
  * (cudaHostAlloc, or pinned and registered) is accessed across the host
  * link, the zero-copy access DirectKV applies to K/V (core method 1): out is
  * written in place; for a sparse step (k > 0), mapped q and lengths are read
@@ -289,7 +322,9 @@ typedef struct {
   const void *v_cache;
   const int32_t *block_table;       /* device                                  */
   const void *minmax;               /* device; sparse steps only               */
-  float *scores;                    /* device [B][Hq][maxP]; sparse only       */
+  float *scores;                    /* device [B][Hq][maxP]; sparse steps that */
+                                    /* run the separate calls only (may be NULL */
+                                    /* when the workspace holds the selection)  */
   int32_t *indices;                 /* device [B][Hq][k]; sparse only          */
   int32_t k;                        /* 0: dense step; else pages per head      */
   float scale;

@@ -15,7 +15,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvsparse.so")
 
 SOURCES = ["kv_api.cu", "kv_index.cu", "kv_topk.cu", "kv_attn_core.cu", "kv_attn_mma.cu",
-           "kv_attn_win.cu", "kv_noalloc.cu", "kv_probe.cu", "kv_append.cu", "kv_window.cu"]
+           "kv_attn_win.cu", "kv_noalloc.cu", "kv_probe.cu", "kv_append.cu", "kv_window.cu",
+           "kv_select_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

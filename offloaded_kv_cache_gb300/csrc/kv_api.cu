@@ -155,7 +155,8 @@ struct OccEntry {
 };
 std::mutex g_occ_mutex;
 OccEntry g_occ[64];
-int g_occ_n = 0;
+int g_occ_n = 0;     // entries in use (at most 64)
+int g_occ_next = 0;  // the slot the next answer goes to (a ring over the 64)
 
 int cached_occupancy(int dtype, int gc, bool mma, bool win, int threads, size_t smem) {
   const int dev = current_device();
@@ -173,7 +174,8 @@ int cached_occupancy(int dtype, int gc, bool mma, bool win, int threads, size_t 
                       : attn_occupancy_core(dtype, gc, threads, smem);
   if (n > 0) {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
-    g_occ[g_occ_n % 64] = OccEntry{dev, dtype, gc, (int)mma, (int)win, threads, smem, n};
+    g_occ[g_occ_next] = OccEntry{dev, dtype, gc, (int)mma, (int)win, threads, smem, n};
+    g_occ_next = (g_occ_next + 1) % 64;
     if (g_occ_n < 64) ++g_occ_n;
   }
   return n;
@@ -338,9 +340,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [rows = N * Hkv * ps][128 elements]; box = one 128-byte slab x
-// kTileTokens rows (one stage of the kernel's ring), 128-byte swizzle
-// (matching the kernel's shared-memory layout).
+// 3-D view [slab][rows = N * Hkv * ps][128 bytes]: a 128-element row is
+// `elem` slabs of 128 bytes (strides: a row, 128 bytes), so one box of every
+// slab x kTileTokens rows is one K (or V) tile of the kernel's ring, in its
+// [slab][row] layout with the 128-byte swizzle.  (Two boxes per tile instead
+// of one per slab: the 70B-class sparse call 176.7 -> 174.7 us.)
 int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
   auto fn = encode_fn();
   if (!fn) return KV_ERR_CUDA;
@@ -348,12 +352,14 @@ int make_kv_map(const kv_shape *s, const void *base, CUtensorMap *map) {
                                  : s->dtype == KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int eb = elem_bytes(s->dtype);
-  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim,
-                        (cuuint64_t)(s->num_phys_pages * s->num_kv_heads * s->page_size)};
-  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * eb};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)kTileTokens};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+  const int slabs = eb;  // 128-byte slabs per 128-element row
+  cuuint64_t dims[3] = {(cuuint64_t)(128 / eb),
+                        (cuuint64_t)(s->num_phys_pages * s->num_kv_heads * s->page_size),
+                        (cuuint64_t)slabs};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * eb, 128};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)kTileTokens, (cuuint32_t)slabs};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
@@ -420,16 +426,36 @@ int kv_map_cached(const kv_shape *s, const void *base, CUtensorMap *map) {
   return rc;
 }
 
+// The fused selection (page score + top-K + union in one cluster launch)
+// covers 16-bit data with 4 or 8 query heads per kv head, whose attention
+// runs one head chunk per group.
+bool fused_select_ok(const kv_shape *s) {
+  const int G = s->num_q_heads / s->num_kv_heads;
+  // (each thread of the union step owns one 32-page word of its CTA's share)
+  return (s->dtype == KV_F16 || s->dtype == KV_BF16) && (G == 4 || G == 8) &&
+         select_fused_smem(G, s->max_pages_per_seq) <= 200 * 1024 &&
+         select_fused_pages_per_cta(G, s->max_pages_per_seq) / 32 <= 128;
+}
+
+// Attention over union lists a selection call left in the workspace
+// (kv_select_pages), instead of building them from `indices`.
+struct ListsReady {
+  bool resolved;  // entries hold physical pages (the fused selection)
+  int early_inputs;
+};
+
 int attn_common(const kv_shape *s, const void *q, const void *k_cache, const void *v_cache,
                 const int32_t *bt, const int32_t *ctx, const int32_t *indices, int32_t k,
                 float scale, float *out, void *ws, size_t ws_bytes, void *stream,
-                const WindowCall *wc = nullptr) {
+                const WindowCall *wc = nullptr, const ListsReady *ready = nullptr) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!al16(q) || !al16(out) || !al4(bt) || !al4(ctx)) return KV_ERR_INVALID_ARG;
+  if (ready && (k < 1 || wc)) return KV_ERR_INVALID_ARG;
   if (indices && (!al4(indices) || k < 1)) return KV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
-  if (indices && (long long)(s->max_pages_per_seq + 3) / 4 * 4 > 200 * 1024)
+  const bool sparse_call = indices != nullptr || ready != nullptr;
+  if (sparse_call && (long long)(s->max_pages_per_seq + 3) / 4 * 4 > 200 * 1024)
     return KV_ERR_UNSUPPORTED;
   // a row's pages are spread over at most 1024 splits of at most
   // kMaxListPages pages each
@@ -440,7 +466,7 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   if ((rc = resolve_kv(s, k_cache, &kd)) != KV_OK) return rc;
   if ((rc = resolve_kv(s, v_cache, &vd)) != KV_OK) return rc;
   const kv_shape *as = wc ? &wc->wshape : s;  // the shape the attention reads
-  const Plan pl = cached_plan(as, indices ? k : 0, wc != nullptr);
+  const Plan pl = cached_plan(as, sparse_call ? k : 0, wc != nullptr);
   const int C = wc ? wc->win->cache_pages : 0;
   const size_t need_ws = pl.total + (wc ? window_bits_bytes(s) : 0);
   if (need_ws > 0 && (ws == nullptr || ws_bytes < need_ws || !al16(ws))) return KV_ERR_WORKSPACE;
@@ -493,16 +519,19 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   // the sparse and window calls launch their union (or window update) kernel
   // first, which writes neither q nor the block table; a dense call's
   // attention kernel is the first of the call
-  a.early_inputs = indices ? 1 : 0;
+  a.early_inputs = ready ? ready->early_inputs : indices ? 1 : 0;
+  a.union_resolved = ready && ready->resolved ? 1 : 0;
   if (pl.S > 1) {
     a.part_o = reinterpret_cast<float *>(w + pl.off_part_o);
     a.part_ml = reinterpret_cast<float *>(w + pl.off_part_ml);
   }
-  if (indices) {
+  if (sparse_call) {
     a.union_pages = reinterpret_cast<int32_t *>(w + pl.off_upages);
     a.union_masks = reinterpret_cast<uint32_t *>(w + pl.off_umasks);
     a.union_count = reinterpret_cast<int32_t *>(w + pl.off_ucount);
     a.umax = pl.umax;
+  }
+  if (indices) {
     cudaError_t e;
     if (wc) {
       // the window step: update the state and mark this step's fetches, and,
@@ -713,6 +742,142 @@ int32_t kv_attn_num_splits(const kv_shape *shape, int32_t k) {
   return cached_plan(shape, k).S;
 }
 
+// The cluster scores the pages itself while each CTA's share is short (one
+// launch for the whole selection); with longer rows its few CTAs read the
+// index too slowly, so the page-score kernel's wide grid scores them first
+// (128k-token rows: 22.6 us fused against 13.3 us for score + top-K).
+#ifndef KVS_SELECT_SCORE_MAX_PAGES
+#define KVS_SELECT_SCORE_MAX_PAGES 512
+#endif
+bool select_scores_in_cluster(const kv_shape *s) {
+  const int G = s->num_q_heads / s->num_kv_heads;
+  return select_fused_pages_per_cta(G, s->max_pages_per_seq) <= KVS_SELECT_SCORE_MAX_PAGES;
+}
+
+static size_t select_ws_bytes(const kv_shape *shape, int32_t k) {
+  size_t n = cached_plan(shape, k).total;
+  if (!fused_select_ok(shape) || !select_scores_in_cluster(shape))  // scores kept there
+    n += align256((size_t)shape->batch * shape->num_q_heads * shape->max_pages_per_seq * 4);
+  return n;
+}
+
+size_t kv_select_workspace_bytes(const kv_shape *shape, int32_t k) {
+  if (check_shape(shape) != KV_OK || k < 1) return 0;
+  return select_ws_bytes(shape, k);
+}
+
+// early_inputs: as for the score kernel (the previous kernel in the stream is
+// the library's own)
+static int select_common(const kv_shape *shape, const void *q, const void *minmax,
+                         const int32_t *block_table, const int32_t *context_lens, int32_t k,
+                         int32_t sink_tokens, int32_t local_tokens, int32_t *indices,
+                         void *workspace, size_t workspace_bytes, int early_inputs,
+                         void *stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (k < 1 || sink_tokens < 0 || local_tokens < 0 || !al16(q) || !al16(minmax) ||
+      !al4(block_table) || !al4(context_lens) || !al4(indices))
+    return KV_ERR_INVALID_ARG;
+  if ((long long)(shape->max_pages_per_seq + 3) / 4 * 4 > 200 * 1024) return KV_ERR_UNSUPPORTED;
+  const int dev = current_device();
+  if (dev < 0) return KV_ERR_CUDA;
+  const Plan pl = cached_plan(shape, k);
+  const size_t need = select_ws_bytes(shape, k);
+  if (workspace == nullptr || workspace_bytes < need || !al16(workspace)) return KV_ERR_WORKSPACE;
+  int *status = status_ptr(dev);
+  if (!status) return KV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *w = static_cast<char *>(workspace);
+  int32_t *upages = reinterpret_cast<int32_t *>(w + pl.off_upages);
+  uint32_t *umasks = reinterpret_cast<uint32_t *>(w + pl.off_umasks);
+  int32_t *ucount = reinterpret_cast<int32_t *>(w + pl.off_ucount);
+  cudaError_t e;
+  if (fused_select_ok(shape)) {
+    SelectArgs a{};
+    a.q = q;
+    a.table = minmax;
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.indices = indices;
+    a.upages = upages;
+    a.umasks = umasks;
+    a.ucount = ucount;
+    a.status = status;
+    a.nphys = shape->num_phys_pages;
+    a.Hq = shape->num_q_heads;
+    a.Hkv = shape->num_kv_heads;
+    a.ps = shape->page_size;
+    a.maxP = shape->max_pages_per_seq;
+    a.K = k;
+    a.umax = pl.umax;
+    a.PC = select_fused_pages_per_cta(shape->num_q_heads / shape->num_kv_heads, a.maxP);
+    a.sink_tokens = sink_tokens;
+    a.local_tokens = local_tokens;
+    a.early_inputs = early_inputs;
+    e = cudaSuccess;
+    if (!select_scores_in_cluster(shape)) {
+      float *scores = reinterpret_cast<float *>(w + pl.total);
+      e = launch_page_score(shape->dtype, false, q, minmax, block_table, context_lens, scores,
+                            shape->batch, shape->num_q_heads, shape->num_kv_heads,
+                            shape->page_size, shape->max_pages_per_seq, shape->num_phys_pages,
+                            early_inputs, status, st);
+      a.scores = scores;
+      a.early_inputs = 1;  // after the score kernel, which writes neither q nor the table
+    }
+    if (e == cudaSuccess) e = launch_select_fused(shape->dtype, a, shape->batch, st);
+  } else {
+    float *scores = reinterpret_cast<float *>(w + pl.total);
+    e = launch_page_score(shape->dtype, false, q, minmax, block_table, context_lens, scores,
+                          shape->batch, shape->num_q_heads, shape->num_kv_heads,
+                          shape->page_size, shape->max_pages_per_seq, shape->num_phys_pages,
+                          early_inputs, status, st);
+    if (e == cudaSuccess)
+      e = launch_topk(scores, context_lens, shape->batch, shape->num_q_heads, shape->page_size,
+                      shape->max_pages_per_seq, k, sink_tokens, local_tokens, indices, status,
+                      st);
+    if (e == cudaSuccess)
+      e = launch_union(indices, context_lens, shape->batch, shape->num_q_heads,
+                       shape->num_kv_heads, pl.gc, shape->page_size, shape->max_pages_per_seq,
+                       k, pl.umax, upages, umasks, ucount, status, st);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KV_ERR_CUDA;
+  }
+  return KV_OK;
+}
+
+int kv_select_pages(const kv_shape *shape, const void *q, const void *minmax,
+                    const int32_t *block_table, const int32_t *context_lens, int32_t k,
+                    int32_t sink_tokens, int32_t local_tokens, int32_t *indices, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  KV_API_RANGE();
+  return select_common(shape, q, minmax, block_table, context_lens, k, sink_tokens, local_tokens,
+                       indices, workspace, workspace_bytes, 0, stream);
+}
+
+static int attn_selected_common(const kv_shape *shape, const void *q, const void *k_cache,
+                                const void *v_cache, const int32_t *block_table,
+                                const int32_t *context_lens, int32_t k, float scale, float *out,
+                                void *workspace, size_t workspace_bytes, int early_inputs,
+                                void *stream) {
+  if (check_shape(shape) != KV_OK) return check_shape(shape);
+  if (k < 1) return KV_ERR_INVALID_ARG;
+  const ListsReady ready{fused_select_ok(shape), early_inputs};
+  return attn_common(shape, q, k_cache, v_cache, block_table, context_lens, nullptr, k, scale,
+                     out, workspace, workspace_bytes, stream, nullptr, &ready);
+}
+
+int kv_sparse_decode_attn_selected(const kv_shape *shape, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_table,
+                                   const int32_t *context_lens, int32_t k, float scale,
+                                   float *out, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+  KV_API_RANGE();
+  return attn_selected_common(shape, q, k_cache, v_cache, block_table, context_lens, k, scale,
+                              out, workspace, workspace_bytes, 0, stream);
+}
+
 int kv_sparse_decode_attn(const kv_shape *shape, const void *q, const void *k_cache,
                           const void *v_cache, const int32_t *block_table,
                           const int32_t *context_lens, const int32_t *indices, int32_t k,
@@ -750,7 +915,9 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
   if (rc) return rc;
   if (!io || !io->q_host || !io->context_lens_host || !io->out_host || io->k < 0)
     return KV_ERR_INVALID_ARG;
-  if (io->k > 0 && (!io->minmax || !io->scores || !io->indices)) return KV_ERR_INVALID_ARG;
+  if (io->k > 0 && (!io->minmax || !io->indices)) return KV_ERR_INVALID_ARG;
+  if (io->k > 0 && !io->scores && io->workspace_bytes < select_ws_bytes(shape, io->k))
+    return KV_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)shape->batch * shape->num_q_heads;
   // Host buffers the device has mapped are read (q, lengths) and written
@@ -801,7 +968,17 @@ int kv_decode_step(const kv_shape *shape, const kv_step_io *io, void *stream) {
     if (!al16(io->out)) return KV_ERR_INVALID_ARG;
     out = io->out;
   }
-  if (io->k > 0) {
+  if (io->k > 0 && io->workspace_bytes >= select_ws_bytes(shape, io->k)) {
+    // selection and the group unions in one launch where the shape allows,
+    // then the attention over those lists; the selection kernel writes
+    // neither q nor the block table, so the attention may load them early
+    if ((rc = select_common(shape, q, io->minmax, io->block_table, ctx, io->k, 0, 0,
+                            io->indices, io->workspace, io->workspace_bytes, staged, stream)) !=
+        KV_OK)
+      return rc;
+    rc = attn_selected_common(shape, q, io->k_cache, io->v_cache, io->block_table, ctx, io->k,
+                              io->scale, out, io->workspace, io->workspace_bytes, 1, stream);
+  } else if (io->k > 0) {
     if ((rc = page_score_common(shape, q, io->minmax, io->block_table, ctx, io->scores, staged,
                                 stream)) != KV_OK)
       return rc;

@@ -21,8 +21,9 @@
 //    rows x 128 elements, stored as 128-byte slabs in the 128B-swizzled
 //    layout, so ldmatrix and 16-byte shared loads are bank-conflict free.  A
 //    page of ps tokens is ps / 16 consecutive tiles.
-//  * Producer: HBM -> TMA tiled loads (cp.async.bulk.tensor) completing on
-//    a full mbarrier with a transaction count; pinned host memory -> 16-byte
+//  * Producer: HBM -> TMA tiled loads (cp.async.bulk.tensor, one 3-D box of
+//    every slab of the tile for K and one for V) completing on a full
+//    mbarrier with a transaction count; pinned host memory -> 16-byte
 //    cp.async issued by the 32 producer lanes (same layout, same barrier).
 //    Stage s always belongs to consumer warp s % nw, which arrives on the
 //    stage's empty mbarrier when done.  The number of consumer warps nw and
@@ -188,17 +189,48 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   }
   const bool sparse = a.union_pages != nullptr;
   const long long gidx = (long long)b * gridDim.y + grp;
+  // (launch plans use 128 or 160 threads; the page list needs at least 128)
+  if (blockDim.x < 128) {
+    if (threadIdx.x == 0) flag_error(a.status, KV_ERR_BOUNDS);
+    return;
+  }
 
   // ---- this CTA's share of the page list ---------------------------------
+  // Sparse: split s of S takes union entries s, s + S, s + 2S, ... (still in
+  // page order), so its entries load together with the length and the union
+  // count instead of after them (a contiguous share needs the count first).
+  // Dense: a contiguous range of pages.  kSpec entries per thread cover
+  // kMaxListPages with the smallest CTA (128 threads).
+  constexpr int kSpec = (kMaxListPages + 127) / 128;
+  const int S = a.num_splits;
+  int32_t sp_page[kSpec];
+  uint32_t sp_mask[kSpec];
+  if (sparse) {
+#pragma unroll
+    for (int u = 0; u < kSpec; ++u) {
+      const int j = threadIdx.x + u * blockDim.x;
+      const long long e = split + (long long)j * S;
+      sp_page[u] = -1;
+      sp_mask[u] = 0u;
+      if (j < kMaxListPages && e < a.umax) {
+        sp_page[u] = a.union_pages[gidx * a.umax + e];
+        sp_mask[u] = a.union_masks[gidx * a.umax + e];
+      }
+    }
+  }
   const int len = a.context_lens[b];
   const bool bad_len = len < 1 || len > a.maxP * ps;
   const int P = bad_len ? 0 : (len + ps - 1) / ps;
-  int total = P;
-  if (sparse) total = bad_len ? 0 : min(a.union_count[gidx], a.umax);
-  const int per = (total + a.num_splits - 1) / a.num_splits;
   PageRange rng;
-  rng.lo = min(total, split * per);
-  rng.n = max(0, min(min(total, rng.lo + per) - rng.lo, kMaxListPages));
+  if (sparse) {
+    const int total = bad_len ? 0 : min(a.union_count[gidx], a.umax);
+    rng.lo = split;
+    rng.n = total > split ? min((total - split + S - 1) / S, kMaxListPages) : 0;
+  } else {
+    const int per = (P + S - 1) / S;
+    rng.lo = min(P, split * per);
+    rng.n = max(0, min(min(P, rng.lo + per) - rng.lo, kMaxListPages));
+  }
   const int ntiles = rng.n * UPP;
   if (bad_len && split == 0 && threadIdx.x == 0 && chunk == 0) flag_error(a.status, KV_ERR_BOUNDS);
 
@@ -212,15 +244,33 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   // Resolve this CTA's page list once (block table, union list, valid tokens,
   // head masks), all threads in parallel, so no tile waits on a dependent
   // global load later.
-  for (int j = threadIdx.x; j < rng.n; j += blockDim.x) {
-    const int e = rng.lo + j;
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int j = threadIdx.x + u * blockDim.x;
+    if (j >= rng.n) break;
+    if constexpr (!WIN) {
+      if (sparse && a.union_resolved) {
+        // the fused selection's entries: physical page, valid tokens | mask << 8
+        const int ph = sp_page[u];
+        Ent ent{};
+        ent.phys = -1;
+        if (ph >= 0 && ph < a.nphys) {
+          ent.phys = ph;
+          ent.info = (int)sp_mask[u];
+        } else {
+          flag_error(a.status, KV_ERR_BOUNDS);
+        }
+        plist[j] = ent;
+        continue;
+      }
+    }
     int p;
     uint32_t mask;
     if (sparse) {
-      p = a.union_pages[gidx * a.umax + e];
-      mask = a.union_masks[gidx * a.umax + e];
+      p = sp_page[u];
+      mask = sp_mask[u];
     } else {
-      p = e;
+      p = rng.lo + j;
       mask = (1u << GC) - 1u;
     }
     Ent ent{};
@@ -238,7 +288,7 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           else ph = -1;
         }
       } else if (!MMA && !sparse && a.num_splits == 1) {
-        ph = plist[j].phys;  // loaded before the wait (p == j)
+        ph = plist[j].phys;  // loaded above (p == j)
       } else {
         ph = a.block_table[(long long)b * a.maxP + p];
       }
@@ -291,11 +341,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           const long long phys = max(ent.phys, 0);
           const int row0 = (int)((phys * a.Hkv + kvh) * ps) + (j % UPP) * TT;
           mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
-#pragma unroll
-          for (int h = 0; h < SL; ++h) tma_load_2d(dst + h * slab_bytes, &tk, h * EPS, row0, fb);
-#pragma unroll
-          for (int h = 0; h < SL; ++h)
-            tma_load_2d(dst + kv_off + h * slab_bytes, &tv, h * EPS, row0, fb);
+          tma_load_3d(dst, &tk, 0, row0, 0, fb);  // every slab of the K tile
+          tma_load_3d(dst + kv_off, &tv, 0, row0, 0, fb);
         } else {
           mbar_arrive(fb);
         }
@@ -317,11 +364,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
           const int row0 = (int)((phys * a.Hkv + kvh) * ps) + (j % UPP) * TT;
           mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
-#pragma unroll
-          for (int h = 0; h < SL; ++h) tma_load_2d(dst + h * slab_bytes, &tk, h * EPS, row0, fb);
-#pragma unroll
-          for (int h = 0; h < SL; ++h)
-            tma_load_2d(dst + kv_off + h * slab_bytes, &tv, h * EPS, row0, fb);
+          tma_load_3d(dst, &tk, 0, row0, 0, fb);  // every slab of the K tile
+          tma_load_3d(dst + kv_off, &tv, 0, row0, 0, fb);
         }
       }
     } else {

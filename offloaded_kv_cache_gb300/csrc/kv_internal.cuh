@@ -182,13 +182,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 // ---------------------------------------------------------------------------
 // async copies into shared memory
 // ---------------------------------------------------------------------------
-// TMA tiled load of a 2-D box (x = element column, y = row) completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
+// TMA tiled load of a 3-D box (x = element column within a 128-byte slab,
+// y = row, z = slab) completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 // 16-byte asynchronous global->shared copy (L2 only).
@@ -266,6 +267,8 @@ struct SelectArgs {
   const void *table;           // min/max index [N_phys][Hkv][2][d]
   const int32_t *block_table;  // [B][maxP]
   const int32_t *context_lens; // [B]
+  const float *scores;         // [B][Hq][maxP] page scores already computed, or null:
+                               // the kernel scores the pages itself
   int32_t *indices;            // [B][Hq][K]
   int32_t *upages;             // [B][Hkv][umax]: physical page (-1: bad entry)
   uint32_t *umasks;            // [B][Hkv][umax]: valid tokens | head mask << 8

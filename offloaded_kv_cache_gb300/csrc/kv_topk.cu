@@ -7,32 +7,17 @@
 // ascending.
 #include "kv_internal.cuh"
 #include "kv_launch.h"
+#include "kv_radix.cuh"
 #include "kv_union.cuh"
 
 namespace kvs {
 namespace {
 
 
-__device__ __forceinline__ uint32_t score_key(float s) {
-  // +0.0f folds -0.0 into +0.0 so that equal scores compare equal
-  return key32(__float_as_uint(s + 0.0f));
-}
-
-// Key of a forced page: above every score's key (+inf maps to 0xFF800000;
-// 0xFFFFFFFF is a NaN's key, and scores are never NaN).
-constexpr uint32_t kForcedKey = 0xFFFFFFFFu;
-
-// One CTA per (b, h) row.  Radix select of the K-th largest key, 8 bits per
-// pass from the highest bit where the row's keys differ (the bits above it
-// are common to every key, so a pass spent on them would select nothing):
-// a shared-memory histogram, double-buffered so that a pass needs two block
-// barriers, whose threshold digit one warp finds with a shuffle scan;
-// stopping early once every key of the threshold bin is taken.  The output
-// pass gives each thread a run of consecutive pages, counts its keys above
-// and at the threshold, and after one block scan of those counts places the
-// selected pages in page order.  Equal keys at the threshold go to the lower
-// page index.  (kv_select.cuh holds a generic select for other kernels.)
-// Forced pages (the pages holding the first sink_tokens tokens and the last
+// One CTA per (b, h) row: the radix select of kv_radix.cuh over the row's
+// keys (in shared memory when they fit), then its selected pages in page
+// order.  (kv_select.cuh holds a generic select for other kernels.)  Forced
+// pages (the pages holding the first sink_tokens tokens and the last
 // local_tokens tokens of the row) take a key above every score's, so they are
 // selected first, lower index first among themselves.
 template <int kTopkThreads>
@@ -41,14 +26,9 @@ __global__ void __launch_bounds__(kTopkThreads)
                 int maxP, int K, int keys_in_smem, int sink_tokens, int local_tokens,
                 int32_t *out, int *status) {
   pdl_wait();
-  constexpr int kTopkWarps = kTopkThreads / 32;
   extern __shared__ uint32_t skeys[];
-  __shared__ uint32_t hist[2][256];
-  __shared__ uint32_t wmin[kTopkWarps], wmax[kTopkWarps];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_krem, s_all;
-  __shared__ unsigned long long wsum[kTopkWarps];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ RadixSmem<kTopkThreads> rs;
+  const int tid = threadIdx.x;
   const long long row = blockIdx.x;
   const int b = (int)(row / Hq);
   int32_t *orow = out + row * K;
@@ -83,7 +63,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   auto key_at = [&](int p) -> uint32_t { return keys_in_smem ? skeys[p] : raw_key(p); };
 
   // keys (into shared memory when they fit), their minimum and maximum
-  if (tid < 256) hist[0][tid] = 0;
+  if (tid < 256) rs.hist[0][tid] = 0;
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int u = 0; u < kSpec; ++u) {
@@ -101,121 +81,15 @@ __global__ void __launch_bounds__(kTopkThreads)
     kmin = min(kmin, k);
     kmax = max(kmax, k);
   }
-  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-  if (lane == 0) { wmin[warp] = kmin; wmax[warp] = kmax; }
-  __syncthreads();
-  kmin = __reduce_min_sync(0xFFFFFFFFu, lane < kTopkWarps ? wmin[lane] : 0xFFFFFFFFu);
-  kmax = __reduce_max_sync(0xFFFFFFFFu, lane < kTopkWarps ? wmax[lane] : 0u);
-
-  // radix select from the highest bit where the keys differ (the bits above
-  // it are common to every key), 8 bits per pass
-  const uint32_t diff = kmin ^ kmax;
-  const int top = diff ? 31 - __clz(diff) : -1;
-  uint32_t pmask = top >= 31 ? 0u : (0xFFFFFFFFu << (top + 1));
-  uint32_t prefix = kmin & pmask;
-  int krem = keff;
-  int pass = 0;
-#pragma unroll 1
-  for (int hb = top; hb >= 0; hb -= 8, ++pass) {
-    const int lb = max(hb - 7, 0);
-    const uint32_t dmask = (1u << (hb - lb + 1)) - 1u;
-    uint32_t *h = hist[pass & 1];
-    if (tid < 256) hist[(pass + 1) & 1][tid] = 0;  // the next pass's histogram
-    for (int p = tid; p < P; p += kTopkThreads) {
-      const uint32_t k = key_at(p);
-      if ((k & pmask) == prefix) atomicAdd(&h[(k >> lb) & dmask], 1u);
-    }
-    __syncthreads();
-    if (tid < 32) {
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = (int)h[255 - 8 * tid - j];
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (tid >= off) incl += t;
-      }
-      int above = incl - sum;
-      if (above < krem && krem <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above + c[j] >= krem) {
-            s_digit = (uint32_t)(255 - 8 * tid - j);
-            s_krem = krem - above;
-            s_all = (above + c[j] == krem) ? 1 : 0;
-            break;
-          }
-          above += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= s_digit << lb;
-    pmask |= dmask << lb;
-    krem = s_krem;
-    if (s_all) break;
-  }
+  block_minmax<kTopkThreads>(rs, kmin, kmax);
+  uint32_t prefix, pmask;
+  int krem;
+  radix_threshold<kTopkThreads>(rs, key_at, P, keff, kmin, kmax, prefix, pmask, krem);
   pdl_trigger();
-  // selected: keys above the threshold, then the first krem equal to it in
-  // page order (all of them when the last pass took its whole bin, where
-  // krem is their count).  Each thread owns `per` consecutive pages.
-  const int per = ((P + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
-  const int lo = min(P, tid * per), hi = min(P, lo + per);
-  auto load4 = [&](int p, uint32_t (&kk)[4]) {
-    if (keys_in_smem && p + 4 <= hi) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(skeys + p);
-      kk[0] = v.x; kk[1] = v.y; kk[2] = v.z; kk[3] = v.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) kk[e] = p + e < hi ? key_at(p + e) : 0u;
-    }
-  };
-  uint32_t gt_n = 0, eq_n = 0;
-  for (int p = lo; p < hi; p += 4) {
-    uint32_t kk[4];
-    load4(p, kk);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t k = kk[e] & pmask;
-      const bool in = p + e < hi;
-      gt_n += in && k > prefix;
-      eq_n += in && k == prefix;
-    }
-  }
-  uint32_t gi = gt_n, ei = eq_n;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t tg = __shfl_up_sync(0xFFFFFFFFu, gi, off);
-    const uint32_t te = __shfl_up_sync(0xFFFFFFFFu, ei, off);
-    if (lane >= off) { gi += tg; ei += te; }
-  }
-  if (lane == 31) wsum[warp] = ((unsigned long long)ei << 32) | gi;
-  __syncthreads();
-  const unsigned long long t = lane < kTopkWarps ? wsum[lane] : 0ull;
-  const bool before = lane < warp;
-  int gt_b = (int)(__reduce_add_sync(0xFFFFFFFFu, before ? (uint32_t)t : 0u) + gi - gt_n);
-  int eq_b = (int)(__reduce_add_sync(0xFFFFFFFFu, before ? (uint32_t)(t >> 32) : 0u) + ei - eq_n);
-  for (int p = lo; p < hi; p += 4) {
-    uint32_t kk[4];
-    load4(p, kk);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t k = kk[e] & pmask;
-      const bool in = p + e < hi;
-      const bool is_gt = in && k > prefix, is_eq = in && k == prefix;
-      if (is_gt || (is_eq && eq_b < krem)) {
-        const int pos = gt_b + min(eq_b, krem);
-        if (pos < K) orow[pos] = p + e;
-      }
-      gt_b += is_gt;
-      eq_b += is_eq;
-    }
-  }
+  radix_emit<kTopkThreads>(rs, key_at, keys_in_smem ? skeys : nullptr, P, prefix, pmask, krem,
+                           [&](int pos, int p) {
+                             if (pos < K) orow[pos] = p;
+                           });
   for (int i = keff + tid; i < K; i += kTopkThreads) orow[i] = -1;
 }
 

@@ -88,6 +88,10 @@ def load(path: str = LIB_PATH):
         "kv_topk_select": (ctypes.c_int, [S, P, P, i32, P, P, sz, P]),
         "kv_topk_select_forced": (ctypes.c_int, [S, P, P, i32, i32, i32, P, P, sz, P]),
         "kv_attn_workspace_bytes": (sz, [S, i32]),
+        "kv_select_workspace_bytes": (sz, [S, i32]),
+        "kv_select_pages": (ctypes.c_int, [S, P, P, P, P, i32, i32, i32, P, P, sz, P]),
+        "kv_sparse_decode_attn_selected": (ctypes.c_int, [S, P, P, P, P, P, i32, f32, P, P, sz,
+                                                          P]),
         "kv_attn_num_splits": (i32, [S, i32]),
         "kv_sparse_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, P, i32, f32, P, P, sz, P]),
         "kv_dense_decode_attn": (ctypes.c_int, [S, P, P, P, P, P, f32, P, P, sz, P]),
@@ -250,6 +254,30 @@ def kv_sparse_decode_attn(shape, q, k_cache, v_cache, block_table, context_lens,
                                       _ptr(indices), int(k), float(scale), _ptr(out),
                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
     return _ret(rc, "kv_sparse_decode_attn", check)
+
+
+def kv_select_workspace_bytes(shape, k) -> int:
+    return int(load().kv_select_workspace_bytes(ctypes.byref(shape), int(k)))
+
+
+def kv_select_pages(shape, q, minmax, block_table, context_lens, k, sink_tokens, local_tokens,
+                    indices, workspace, workspace_bytes, stream=None, check=True):
+    rc = load().kv_select_pages(ctypes.byref(shape), _ptr(q), _ptr(minmax), _ptr(block_table),
+                                _ptr(context_lens), int(k), int(sink_tokens), int(local_tokens),
+                                _ptr(indices), _ptr(workspace), int(workspace_bytes),
+                                _stream(stream))
+    return _ret(rc, "kv_select_pages", check)
+
+
+def kv_sparse_decode_attn_selected(shape, q, k_cache, v_cache, block_table, context_lens, k,
+                                   scale, out, workspace, workspace_bytes, stream=None,
+                                   check=True):
+    rc = load().kv_sparse_decode_attn_selected(ctypes.byref(shape), _ptr(q), _ptr(k_cache),
+                                               _ptr(v_cache), _ptr(block_table),
+                                               _ptr(context_lens), int(k), float(scale),
+                                               _ptr(out), _ptr(workspace), int(workspace_bytes),
+                                               _stream(stream))
+    return _ret(rc, "kv_sparse_decode_attn_selected", check)
 
 
 def kv_dense_decode_attn(shape, q, k_cache, v_cache, block_table, context_lens, scale, out,

@@ -8,6 +8,7 @@ binding:
     build_mean_index(), score_mean() -> kv_page_mean_build, kv_page_score_mean
     append()       -> kv_append_token
     sparse_step()  -> kv_page_score, kv_topk_select, kv_sparse_decode_attn
+    sparse_step_fused() -> kv_select_pages, kv_sparse_decode_attn_selected
     enable_window(C), window_attn() -> kv_window_reset, kv_sparse_decode_attn_window
     dense_step()   -> kv_dense_decode_attn
     host_step()    -> kv_decode_step (host q / lengths in, out back)
@@ -90,7 +91,9 @@ class DecodeLayer:
         self.ws_dense_bytes = kv.kv_attn_workspace_bytes(self.shape, 0)
         self.ws_sparse_bytes = kv.kv_attn_workspace_bytes(self.shape, k) if self.topk else 0
         self.ws_topk_bytes = kv.kv_topk_workspace_bytes(self.shape, k)
-        nbytes = max(self.ws_dense_bytes, self.ws_sparse_bytes, self.ws_topk_bytes, 16)
+        self.ws_select_bytes = kv.kv_select_workspace_bytes(self.shape, k) if self.topk else 0
+        nbytes = max(self.ws_dense_bytes, self.ws_sparse_bytes, self.ws_topk_bytes,
+                     self.ws_select_bytes, 16)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     # --- the GPU-resident page window -----------------------------------------
@@ -193,6 +196,28 @@ class DecodeLayer:
         kv.kv_sparse_decode_attn(self.shape, self.q, self.k_cache, self.v_cache, self.block_table,
                                  self.context_lens, idx, idx.shape[-1], self.scale, self.out,
                                  self.workspace, self.workspace.numel(), stream)
+
+    def select_fused(self, stream=None, sink_tokens: int = 0, local_tokens: int = 0):
+        """Page score, top-K and the group unions in one call (kv_select_pages):
+        the selection lands in `indices`, the unions in the workspace for
+        sparse_attn_selected()."""
+        stream = self._st(stream)
+        kv.kv_select_pages(self.shape, self.q, self.minmax, self.block_table, self.context_lens,
+                           self.topk, sink_tokens, local_tokens, self.indices, self.workspace,
+                           self.workspace.numel(), stream)
+
+    def sparse_attn_selected(self, stream=None):
+        """Attention over the pages the last select_fused() chose."""
+        stream = self._st(stream)
+        kv.kv_sparse_decode_attn_selected(self.shape, self.q, self.k_cache, self.v_cache,
+                                          self.block_table, self.context_lens, self.topk,
+                                          self.scale, self.out, self.workspace,
+                                          self.workspace.numel(), stream)
+
+    def sparse_step_fused(self, stream=None):
+        stream = self._st(stream)
+        self.select_fused(stream)
+        self.sparse_attn_selected(stream)
 
     def sparse_step(self, stream=None):
         stream = self._st(stream)

@@ -63,3 +63,21 @@ def test_sparse_bytes_keep_groups_apart():
     # group 0: pages {1, 3}; group 1: page {3}; 16 valid tokens each
     kv = 3 * 2 * 16 * 128 * 2
     assert attn == kv + 4 * 4 + 4 * 128 * 2 + 4 * 128 * 4
+
+
+def test_sparse_bytes_with_the_selection_lists():
+    bm = _bench()
+    # the case above through kv_select_pages: the unions are written as
+    # 8-byte entries and read by the attention; the select reads one
+    # block-table entry per scored page; the scores stay on chip
+    spec = W.tiny_spec(dtype="bf16", batch=1, hq=2, hkv=1, context=40, ps=16, topk=2)
+    idx = np.array([[[0, 2], [2, -1]]], dtype=np.int32)
+    step, attn = bm.sparse_bytes(spec, np.array([40]), idx, lists=True, scores_in_memory=False)
+    # attention: lists 2 * 8 = 16 + K/V 12,288 + q 512 + out 1,024
+    assert attn == 13_840
+    # step: + index 1,536 + block table 3 * 4 = 12 + q 512 + selection 16
+    #       + lists written 16
+    assert step == 15_932
+    # with the scores through memory (the page-score kernel first): + 48
+    step2, _ = bm.sparse_bytes(spec, np.array([40]), idx, lists=True, scores_in_memory=True)
+    assert step2 == 15_932 + 48

@@ -107,5 +107,15 @@ def test_host_step_rejects_missing_sparse_buffers():
     ctx_host = layer.context_lens.cpu().pin_memory()
     out_host = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
     io = layer.host_io(q_host, ctx_host, out_host, True)
-    io.scores = None
+    io.minmax = None
     assert kv.kv_decode_step(layer.shape, io, check=False) == kv.KV_ERR_INVALID_ARG
+    # without a scores buffer the step needs the selection's workspace
+    io = layer.host_io(q_host, ctx_host, out_host, True)
+    io.scores = None
+    io.workspace_bytes = kv.kv_attn_workspace_bytes(layer.shape, 2)
+    if io.workspace_bytes < kv.kv_select_workspace_bytes(layer.shape, 2):
+        assert kv.kv_decode_step(layer.shape, io, check=False) == kv.KV_ERR_INVALID_ARG
+    io.workspace_bytes = kv.kv_select_workspace_bytes(layer.shape, 2)
+    assert kv.kv_decode_step(layer.shape, io, check=False) == kv.KV_OK
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK

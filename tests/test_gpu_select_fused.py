@@ -1,0 +1,200 @@
+"""The one-call selection (kv_select_pages) and the attention over its lists
+(kv_sparse_decode_attn_selected).
+
+For 16-bit data with 4 or 8 query heads per kv head the selection is one
+cluster launch that keeps the scores on chip; other shapes run the separate
+kernels.  Bars:
+  * indices: bit-exact against kv_page_score + kv_topk_select(_forced) on the
+    GPU (the same contraction and the same select), and against the oracle's
+    top-K up to the boundary exemption of the parity rules;
+  * attention: bit-exact against kv_sparse_decode_attn on the same indices
+    (the same pages, head masks and split ranges), and within max-abs 2e-3
+    (16-bit) / 1e-5 (fp32) of the oracle's attention on the oracle's own
+    selection for every row whose selection equals the oracle's;
+  * bad context lengths: flagged as KV_ERR_BOUNDS, selection -1, no page read.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from offloaded_kv_cache_gb300 import kvsparse as kv
+from offloaded_kv_cache_gb300 import workloads as W
+from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+from parity_util import ATOL, check_topk_with_exemption
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(kvlib):
+    kv.kv_debug_config(-1, 2_000_000_000)
+    yield
+
+
+def fused_vs_separate(wl, k, sink=0, local=0, kv_loc=None):
+    """Runs both paths on one layer; returns (layer, fused idx, separate idx,
+    fused out, separate out)."""
+    layer = DecodeLayer(wl, topk=k, kv_loc=kv_loc)
+    layer.build_index()
+    layer.score()
+    layer.select(sink_tokens=sink, local_tokens=local)
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    idx_sep = layer.indices.cpu().numpy().copy()
+    layer.sparse_attn()
+    torch.cuda.synchronize()
+    out_sep = layer.out.cpu().numpy().copy()
+    layer.indices.fill_(-7)
+    layer.out.fill_(float("nan"))
+    layer.select_fused(sink_tokens=sink, local_tokens=local)
+    layer.sparse_attn_selected()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    return layer, layer.indices.cpu().numpy(), idx_sep, layer.out.cpu().numpy(), out_sep
+
+
+def check_against_oracle(wl, k, idx, out):
+    spec = wl.spec
+    dtype = spec.dtype
+    mn, mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
+    ref_s = oracle.scores(dtype, wl.q, mn, mx, wl.block_table, wl.context_lens, spec.page_size)
+    ref_idx = oracle.topk(ref_s, wl.context_lens, spec.page_size, k)
+    check_topk_with_exemption(idx, ref_idx, ref_s, wl.context_lens, spec.page_size, k)
+    same = np.all(idx == ref_idx, axis=-1)          # [B][Hq]
+    rows = [b * spec.num_q_heads + h for b in range(spec.batch)
+            for h in range(spec.num_q_heads) if same[b, h]]
+    assert len(rows) >= 0.9 * spec.batch * spec.num_q_heads
+    ref_o = oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                             wl.context_lens, wl.scale, indices=ref_idx, rows=rows)
+    flat_o = out.reshape(-1, spec.head_dim)[rows]
+    flat_r = ref_o.reshape(-1, spec.head_dim)[rows]
+    err = np.abs(flat_o - flat_r).max()
+    assert err <= ATOL[dtype], f"max-abs {err}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 2), (4, 1), (8, 1)])
+@pytest.mark.parametrize("ps", [16, 64])
+def test_fused_selection_small(dtype, hq, hkv, ps):
+    # several pages per row, a ragged last page, rows of different lengths
+    ctx = [37 * ps + 5, 9 * ps, 3] if ps == 16 else [21 * ps + 33, 4 * ps + 1, 17]
+    spec = W.tiny_spec(dtype=dtype, batch=3, hq=hq, hkv=hkv, context=max(ctx), ps=ps, topk=5,
+                       index=5000 + hq * 3 + hkv + ps)
+    wl = W.generate(spec, context_lens=ctx)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, 5)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+    check_against_oracle(wl, 5, idx, out)
+
+
+@pytest.mark.parametrize("k", [1, 7, 40, 400])
+def test_fused_selection_budgets(k):
+    # k from one page to more than a row holds (all pages, -1 padding)
+    ctx = [300 * 16 + 9, 120 * 16, 40 * 16 + 1, 1]
+    spec = W.tiny_spec(dtype="bf16", batch=4, hq=16, hkv=4, context=max(ctx), ps=16, topk=k,
+                       index=5100 + k)
+    wl = W.generate(spec, context_lens=ctx)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, k)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+    check_against_oracle(wl, k, idx, out)
+
+
+@pytest.mark.parametrize("maxp_pages", [1, 31, 33, 97, 600])
+def test_fused_selection_page_counts(maxp_pages):
+    # page counts around the 32-page words each CTA's share is cut into
+    ctx = [maxp_pages * 16, max(1, maxp_pages * 16 - 23)]
+    spec = W.tiny_spec(dtype="f16", batch=2, hq=8, hkv=1, context=max(ctx), ps=16, topk=6,
+                       index=5200 + maxp_pages)
+    wl = W.generate(spec, context_lens=ctx)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, 6)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+
+
+@pytest.mark.parametrize("sink,local", [(4, 64), (0, 200), (100, 0), (10_000, 0)])
+def test_fused_selection_forced_pages(sink, local):
+    ctx = [150 * 16 + 3, 60 * 16]
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=2, context=max(ctx), ps=16, topk=12,
+                       index=5300 + sink + local)
+    wl = W.generate(spec, context_lens=ctx)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, 12, sink=sink, local=local)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv", [("f32", 4, 1), ("bf16", 4, 2), ("f16", 4, 4),
+                                          ("bf16", 32, 2)])
+def test_separate_kernels_behind_the_same_calls(dtype, hq, hkv):
+    # shapes the cluster launch does not cover run score + top-K + union
+    ctx = [45 * 16 + 2, 17]
+    spec = W.tiny_spec(dtype=dtype, batch=2, hq=hq, hkv=hkv, context=max(ctx), ps=16, topk=6,
+                       index=5400 + hq + hkv)
+    wl = W.generate(spec, context_lens=ctx)
+    layer, idx, idx_sep, out, out_sep = fused_vs_separate(wl, 6)
+    assert layer.ws_select_bytes >= kv.kv_attn_workspace_bytes(layer.shape, 6)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+    check_against_oracle(wl, 6, idx, out)
+
+
+def test_fused_selection_host_resident_kv():
+    ctx = [80 * 16 + 7, 33 * 16]
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=2, context=max(ctx), ps=16, topk=9,
+                       index=5500)
+    wl = W.generate(spec, context_lens=ctx)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, 9, kv_loc="host")
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)
+    check_against_oracle(wl, 9, idx, out)
+
+
+def test_fused_selection_bad_length_is_flagged():
+    spec = W.tiny_spec(dtype="bf16", batch=3, hq=8, hkv=2, context=200, ps=16, topk=4,
+                       index=5600)
+    wl = W.generate(spec)
+    layer = DecodeLayer(wl, topk=4)
+    layer.build_index()
+    torch.cuda.synchronize()
+    bad = layer.context_lens.clone()
+    bad[1] = 0
+    layer.context_lens.copy_(bad)
+    layer.select_fused()
+    layer.sparse_attn_selected()
+    assert kv.kv_device_status() == kv.KV_ERR_BOUNDS
+    idx = layer.indices.cpu().numpy()
+    assert (idx[1] == -1).all()
+    out = layer.out.cpu().numpy()
+    assert (out[1] == 0).all()
+    # the other rows are still right
+    layer.context_lens.copy_(torch.from_numpy(wl.context_lens).cuda())
+    layer.score()
+    layer.select()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    sep = layer.indices.cpu().numpy()
+    assert np.array_equal(idx[[0, 2]], sep[[0, 2]])
+
+
+def test_selection_workspace_too_small_is_refused():
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=2, context=300, ps=16, topk=4,
+                       index=5700)
+    wl = W.generate(spec)
+    layer = DecodeLayer(wl, topk=4)
+    need = kv.kv_select_workspace_bytes(layer.shape, 4)
+    rc = kv.kv_select_pages(layer.shape, layer.q, layer.minmax, layer.block_table,
+                            layer.context_lens, 4, 0, 0, layer.indices, layer.workspace,
+                            need - 1, check=False)
+    assert rc == kv.KV_ERR_WORKSPACE
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama3.1-8b-b4-ctx32k", "70b-gqa-b8-ctx64k-ps64",
+                                  "llama3.1-8b-b1-ctx128k-host"])
+def test_fused_selection_full_size(name):
+    spec = W.WORKLOADS[name]
+    wl = W.generate(spec)
+    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, spec.topk)
+    assert np.array_equal(idx, idx_sep)
+    assert np.array_equal(out, out_sep)

@@ -5,8 +5,8 @@ inputs and outputs, a loop where cudaMalloc would synchronise the device), the
 split-K partials live in a fixed scratch array inside the library.  This test
 calls it through the C ABI and checks it against kv_dense_decode_attn with a
 caller-allocated workspace, on two calls in a row, within the same tolerance
-as the other attention tests; it also checks the size limit.  It sits in a
-file of its own that runs last.
+as the other attention tests, and both against the fp64 oracle; it also
+checks the size limit.  It sits in a file of its own that runs last.
 """
 import ctypes
 
@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from offloaded_kv_cache_gb300 import kvsparse as kv
 from offloaded_kv_cache_gb300 import workloads as W
 from offloaded_kv_cache_gb300.pipeline import DecodeLayer
@@ -55,6 +56,9 @@ def test_noalloc_matches_workspace_call_twice(kvlib, dtype, hq, hkv, ctx):
     stream = torch.cuda.current_stream()
     layer.dense_step(stream)
     ref = layer.out.clone()
+    exact = oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                             wl.context_lens, wl.scale)
+    assert np.abs(ref.cpu().numpy() - exact).max() <= ATOL[dtype]
     for _ in range(2):
         out = torch.full_like(layer.out, float("nan"))
         assert _call(fn, layer, out, stream) == kv.KV_OK
@@ -62,6 +66,7 @@ def test_noalloc_matches_workspace_call_twice(kvlib, dtype, hq, hkv, ctx):
         assert kv.kv_device_status() == kv.KV_OK
         err = (out - ref).abs().max().item()
         assert err <= ATOL[dtype], err
+        assert np.abs(out.cpu().numpy() - exact).max() <= ATOL[dtype]
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(kvlib):
