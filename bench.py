@@ -41,15 +41,15 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
+# "bytes" is a full-size launch; "per_alg_byte" is the ratio of DRAM bytes to
+# algorithmic bytes of a launch of the same kernel on a smaller case of the
+# workload (its batch in "from_batch"), applied to this launch's algorithmic
+# bytes (the traffic grows with the union bytes the launch reads).
 NCU_TRAFFIC = {
-    "opt6.7b-b32-ctx544": {"bytes": 289.127680e6, "src": "5228a6f62cbab6e2"},
-    "llama3.1-8b-b4-ctx32k": {"bytes": 192.197376e6, "src": "5228a6f62cbab6e2"},
-    # from the one-pass DRAM-bytes capture of every kernel at full size
-    "70b-gqa-b8-ctx64k-ps64": {"bytes": 1086.374400e6, "src": "5228a6f62cbab6e2"},
-    # host-resident K/V: DRAM carries only q and the lists; the K/V bytes
-    # arrive over the host link (ctc__rx_bytes_data_user.sum)
-    "llama3.1-8b-b1-ctx128k-host": {"bytes": 190720.0, "link_bytes": 105.728000e6,
-                                    "src": "5228a6f62cbab6e2"},
+    # attention kernel of kv_sparse_decode_attn_selected at batch 1 (two
+    # launches, 135.68 MB read + 0.52 MB written against 135.61 MB)
+    "70b-gqa-b8-ctx64k-ps64": {"per_alg_byte": 1.00431, "from_batch": 1,
+                               "src": "1a68e81670a4ced2"},
 }
 
 
@@ -576,6 +576,9 @@ def main():
     ap.add_argument("--window-steps", type=int, default=0,
                     help="profiling aid: run this many eager page-window decode steps "
                          "(x1 window, drifting queries) on the workload and exit")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: the workload with this batch size instead of its own "
+                         "(a smaller case of the same kernels)")
     ap.add_argument("--kernel-pass", type=int, default=0,
                     help="profiling aid: run this many eager passes over every kernel of "
                          "the path on the workload (no timing) and exit")
@@ -601,6 +604,8 @@ def main():
     kv.load()
 
     spec = W.WORKLOADS[args.workload]
+    if args.batch > 0:
+        spec = spec.with_(batch=args.batch)
     wl = W.generate(spec)
     ctx = wl.context_lens
     copies = kv_copies_for(spec)
@@ -623,9 +628,11 @@ def main():
         return 0
 
     if args.kernel_pass > 0:  # profiling aid, no timing
-        # one pass, in this order: index build, page score, top-K, sparse
-        # attention (union, attention, combine), forced top-K, mean index build
-        # and score, page-window update and attention, dense attention, append
+        # one pass, in this order: index build, the one-call selection and the
+        # attention over its lists (select, attention, combine), page score,
+        # top-K, sparse attention (union, attention, combine), forced top-K,
+        # mean index build and score, page-window update and attention, dense
+        # attention, append
         kn, vn = W.new_tokens(spec, 0)
         kn = storage_to_torch(kn, spec.dtype).cuda()
         vn = storage_to_torch(vn, spec.dtype).cuda()
@@ -635,6 +642,8 @@ def main():
         for _ in range(args.kernel_pass):
             layer.build_index()
             if sparse:
+                layer.select_fused()
+                layer.sparse_attn_selected()
                 layer.score()
                 layer.select()
                 layer.sparse_attn()
@@ -651,8 +660,11 @@ def main():
         assert kv.kv_device_status() == kv.KV_OK
         info = {"kernel_pass": args.kernel_pass, "workload": spec.name}
         if sparse:
+            layer.select_fused()
+            torch.cuda.synchronize()
             idx = layer.indices.cpu().numpy()
-            _, attn_b = sparse_bytes(spec, ctx, idx)
+            _, attn_b = sparse_bytes(spec, ctx, idx, lists=True,
+                                     scores_in_memory=scores_in_memory(layer))
             info["sparse_attention_bytes"] = int(attn_b)
         print(json.dumps(info))
         return 0
@@ -837,8 +849,8 @@ def main():
     traffic = None
     rec = NCU_TRAFFIC.get(spec.name)
     link_traffic = None
-    if rec and rec.get("src") == kernel_source_hash():
-        traffic = rec["bytes"]
+    if rec and rec.get("src") == kernel_source_hash() and args.batch == 0:
+        traffic = rec["bytes"] if "bytes" in rec else round(rec["per_alg_byte"] * attn_bytes)
         link_traffic = rec.get("link_bytes")
 
     cpu = None
@@ -872,6 +884,11 @@ def main():
             "queries_per_s": round(qps, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes": int(attn_bytes),
+                         **({"traffic_source": f"ncu DRAM bytes of a batch-{rec['from_batch']} "
+                                               "launch of the same kernel, scaled by algorithmic "
+                                               "bytes"} if traffic and rec and "per_alg_byte" in rec
+                            else {}),
                          **({"link_traffic": link_traffic} if spec.kv_loc == "host" else {}),
                          "kernel": ("kv_sparse_decode_attn_selected (attention + combine)" if sparse
                                     else "kv_dense_decode_attn (attention"

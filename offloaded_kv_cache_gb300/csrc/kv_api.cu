@@ -431,10 +431,8 @@ int kv_map_cached(const kv_shape *s, const void *base, CUtensorMap *map) {
 // runs one head chunk per group.
 bool fused_select_ok(const kv_shape *s) {
   const int G = s->num_q_heads / s->num_kv_heads;
-  // (each thread of the union step owns one 32-page word of its CTA's share)
   return (s->dtype == KV_F16 || s->dtype == KV_BF16) && (G == 4 || G == 8) &&
-         select_fused_smem(G, s->max_pages_per_seq) <= 200 * 1024 &&
-         select_fused_pages_per_cta(G, s->max_pages_per_seq) / 32 <= 128;
+         select_fused_smem(G, s->max_pages_per_seq) <= 200 * 1024;
 }
 
 // Attention over union lists a selection call left in the workspace

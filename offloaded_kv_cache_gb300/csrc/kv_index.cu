@@ -423,14 +423,19 @@ cudaError_t launch_page_score(int dtype, bool mean, const void *q, const void *t
 // ---------------------------------------------------------------------------
 // Same lane layout as the min/max build (lane = 16-byte column chunk x row
 // group).  Each lane sums its channels in fp32 from -0.0 (so the sum of
-// keys that are all -0.0 stays -0.0, as IEEE addition of the keys gives),
-// and sums |k| beside it.  Any summation order of n terms in fp32 is within
-// (n - 1) 2^-24 sum|k| of the exact sum; the candidate -- the fp32 sum over
-// n, rounded to the storage type -- is the correctly rounded mean when that
-// whole interval lies strictly inside the candidate's rounding cell (between
-// the midpoints to its neighbours).  That holds for all but a tiny share of
-// channels; the others (a mean near a midpoint, sums that cancel, overflow)
-// are recomputed exactly: the channel's keys re-read, summed as integers in
+// keys that are all -0.0 stays -0.0, as IEEE addition of the keys gives)
+// with an error-free transformation per addition (Knuth's TwoSum: the sum s
+// and the exact rounding error of each addition, accumulated in c), and sums
+// |k| beside it.  The only inexact step is the accumulation of the errors in
+// c, within (n + 2)^2 2^-48 sum|k| of its exact value, so s + c is the exact sum
+// to that bound; the candidate -- (s + c) / n rounded to the storage type --
+// is the correctly rounded mean when that whole interval lies strictly
+// inside the candidate's rounding cell (between the midpoints to its
+// neighbours).  That holds for all but a vanishing share of channels (a
+// plain fp32 sum's bound, n 2^-24 sum|k|, left a few per cent of the
+// channels of N(0,1) keys undecided: the 70B-class build went from 0.17 to
+// 2.1 ms); the others (a mean on or next to a midpoint, overflow) are
+// recomputed exactly: the channel's keys re-read, summed as integers in
 // units of 2^-149 (every fp32, f16 and bf16 value is a whole number of
 // them), divided by n by long division, rounded once.
 // last_only: one item per (b, kv head), the page holding the row's last
@@ -591,28 +596,92 @@ __device__ __forceinline__ uint32_t neighbour(uint32_t bits, bool up) {
   return (up != neg) ? bits + 1u : bits - 1u;
 }
 
-// The mean of one channel from its fp32 sum s and sum of magnitudes a: the
-// correctly rounded pattern when the error bound settles it, else ~0u (the
-// exact path decides).  Patterns of the type never equal ~0u (it would be a
+// Knuth's TwoSum: s + x = t + e exactly (round to nearest, no overflow);
+// the error's bits are ORed into `inexact` (zero while every addition was
+// exact)
+__device__ __forceinline__ void two_sum(float &s, float &c, uint32_t &inexact, float x) {
+  const float t = s + x;
+  const float bp = t - s;
+  const float e = (s - (t - bp)) + (x - bp);
+  s = t;
+  c += e;
+  inexact |= __float_as_uint(e);
+}
+
+// The mean of one channel from its TwoSum pair (s, c) and sum of magnitudes
+// a: the correctly rounded pattern when the error bound settles it, else ~0u
+// (the exact path decides).  When no addition rounded (inexact == 0) s is
+// the exact sum, and a mean exactly halfway between two values -- frequent
+// for sums of a power-of-two count of 16-bit keys -- is settled here too,
+// to the even pattern.  Patterns of the type never equal ~0u (it would be a
 // NaN of fp32, and 16-bit patterns are below 2^16).
 template <class T>
-__device__ __forceinline__ uint32_t fast_mean(float s, float a, int n) {
-  if (!isfinite(s) || !isfinite(a)) return ~0u;
+__device__ __forceinline__ uint32_t fast_mean(float s, float c, float a, uint32_t inexact, int n) {
+  constexpr uint32_t kSign = sizeof(T) == 4 ? 0x80000000u : 0x8000u;
+  if (!isfinite(s) || !isfinite(c) || !isfinite(a)) return ~0u;
   if (a == 0.f) return pack_value<T>(signbit(s), 0u, 0);  // every key is a zero
-  const bool pow2 = (n & (n - 1)) == 0;
-  uint32_t r;
-  if constexpr (sizeof(T) == 4) {
-    r = __float_as_uint(pow2 ? s * (1.0f / (float)n) : (float)((double)s / n));
-  } else if constexpr (std::is_same<T, __half>::value) {
-    r = __half_as_ushort(pow2 ? __float2half_rn(s * (1.0f / (float)n))
-                              : __double2half((double)s / n));
-  } else {
-    r = __bfloat16_as_ushort(pow2 ? __float2bfloat16_rn(s * (1.0f / (float)n))
-                                  : __double2bfloat16((double)s / n));
+  if constexpr (sizeof(T) == 2) {
+    // A full page (n a power of two), in fp32 only: fp64 arithmetic is slow
+    // on this part (the build took 0.86 ms for 1 GiB of keys with it).
+    if ((n & (n - 1)) == 0) {
+      const float inv = 1.0f / (float)n;  // exact
+      auto round16 = [](float x) -> uint32_t {
+        if constexpr (std::is_same<T, __half>::value) return __half_as_ushort(__float2half_rn(x));
+        else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      };
+      // s exact: s / n is exact too, and its one rounding is the answer (ties
+      // to even; a zero keeps the sign of the mean, and keys that cancel give
+      // s = +0)
+      if (inexact == 0u) return round16(s * inv);
+      const uint32_t r = round16(fmaf(c, inv, s * inv));
+      const float rv = (float)stored_value<T>(r);
+      if (fabsf(rv) < 0x1p120f) {  // n * midpoint below fp32's overflow
+        // n * the midpoints: exact (a 16-bit value's neighbours are at most
+        // one bit more precise, n a power of two)
+        const float lo = n * ((rv + (float)stored_value<T>(neighbour<T>(r, false))) * 0.5f);
+        const float hi = n * ((rv + (float)stored_value<T>(neighbour<T>(r, true))) * 0.5f);
+        // the bound on (s, c) as below, plus an absolute floor and the
+        // roundings of this check's few fp32 operations
+        const float err = a * ((float)((n + 2) * (n + 2)) * 0x1p-48f) * (1.0f + 0x1p-10f) +
+                          0x1p-149f;
+        const float d1 = s - lo, d2 = hi - s;
+        const float margin = err + 0x1p-22f * (fabsf(d1) + fabsf(d2) + fabsf(c));
+        if (d1 + c > margin && d2 - c > margin) {
+          if (rv != 0.f) return r;
+          const float t = s + c;  // a zero: the sign of the exact mean
+          if (t > margin + 0x1p-22f * fabsf(t)) return pack_value<T>(false, 0u, 0);
+          if (t < -(margin + 0x1p-22f * fabsf(t))) return pack_value<T>(true, 0u, 0);
+        }
+        return ~0u;
+      }
+    }
   }
-  const double sd = (double)s;
-  // error bound of the fp32 sums, with room for this check's own roundings
-  const double err = (double)a * (n * 0x1p-24) * (1.0 + 0x1p-10) + fabs(sd) * 0x1p-50;
+  const double sd = (double)s + (double)c;
+  const double md = sd / n;
+  uint32_t r;
+  if constexpr (sizeof(T) == 4) r = __float_as_uint((float)md);
+  else if constexpr (std::is_same<T, __half>::value) r = __half_as_ushort(__double2half(md));
+  else r = __bfloat16_as_ushort(__double2bfloat16(md));
+  if (inexact == 0u) {  // sd is the exact sum, compared exactly below
+    if (sd == 0.0) return pack_value<T>(false, 0u, 0);  // non-zero keys cancelling: +0
+    const uint32_t dn = neighbour<T>(r, false), up = neighbour<T>(r, true);
+    const double rv = stored_value<T>(r);
+    const double lo = n * ((rv + stored_value<T>(dn)) * 0.5);
+    const double hi = n * ((rv + stored_value<T>(up)) * 0.5);
+    uint32_t pick;
+    if (sd > lo && sd < hi) pick = r;
+    else if (sd == lo) pick = (r & 1u) ? dn : r;  // a tie: the even pattern
+    else if (sd == hi) pick = (r & 1u) ? up : r;
+    else return ~0u;
+    // a zero takes the sign of the exact mean
+    if ((pick & ~kSign) == 0u) pick = sd < 0.0 ? kSign : 0u;
+    return pick;
+  }
+  // error bound of (s, c): the n + 1 error terms, each at most 2^-24 of a
+  // partial sum, accumulated in fp32 -- (n + 2)^2 2^-48 sum|k| -- with room
+  // for this check's roundings (s + c, the products and differences in fp64)
+  const double err =
+      (double)a * ((double)(n + 2) * (n + 2) * 0x1p-48) * (1.0 + 0x1p-10) + fabs(sd) * 0x1p-50;
   const double rv = stored_value<T>(r);
   const double lo = n * ((rv + stored_value<T>(neighbour<T>(r, false))) * 0.5);
   const double hi = n * ((rv + stored_value<T>(neighbour<T>(r, true))) * 0.5);
@@ -657,11 +726,14 @@ __global__ void __launch_bounds__(256)
   const int chunk = lane % C, rg = lane / C;
   const T *page = k + ((phys * Hkv + kvh) * ps) * kHeadDim;
   const uint4 *src = reinterpret_cast<const uint4 *>(page) + chunk;
-  float s[E], a[E];
+  float s[E], c[E], a[E];
+  uint32_t inexact[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     s[e] = -0.f;
+    c[e] = 0.f;
     a[e] = 0.f;
+    inexact[e] = 0u;
   }
 #pragma unroll 4
   for (int r = rg; r < n; r += RG) {
@@ -671,8 +743,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 f = unpack2(w[j], T());
-        s[2 * j] += f.x;
-        s[2 * j + 1] += f.y;
+        two_sum(s[2 * j], c[2 * j], inexact[2 * j], f.x);
+        two_sum(s[2 * j + 1], c[2 * j + 1], inexact[2 * j + 1], f.y);
         a[2 * j] += fabsf(f.x);
         a[2 * j + 1] += fabsf(f.y);
       }
@@ -681,7 +753,7 @@ __global__ void __launch_bounds__(256)
                           __uint_as_float(x.w)};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        s[j] += f[j];
+        two_sum(s[j], c[j], inexact[j], f[j]);
         a[j] += fabsf(f[j]);
       }
     }
@@ -690,7 +762,11 @@ __global__ void __launch_bounds__(256)
   if constexpr (RG == 2) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      s[e] += __shfl_xor_sync(0xFFFFFFFFu, s[e], 16);
+      const float so = __shfl_xor_sync(0xFFFFFFFFu, s[e], 16);
+      const float co = __shfl_xor_sync(0xFFFFFFFFu, c[e], 16);
+      inexact[e] |= __shfl_xor_sync(0xFFFFFFFFu, inexact[e], 16);
+      two_sum(s[e], c[e], inexact[e], so);
+      c[e] += co;
       a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
     }
   }
@@ -698,7 +774,7 @@ __global__ void __launch_bounds__(256)
   uint32_t out[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    out[e] = fast_mean<T>(s[e], a[e], n);
+    out[e] = fast_mean<T>(s[e], c[e], a[e], inexact[e], n);
     if (out[e] == ~0u) out[e] = exact_mean<T>(page, chunk * E + e, n);
   }
   T *dst = mean + (phys * Hkv + kvh) * kHeadDim + chunk * E;

@@ -21,14 +21,18 @@
 //    memory of the CTA that owns that head (distributed shared memory), so no
 //    score reaches global memory.
 //  * After a cluster barrier every CTA runs the radix select of its own head
-//    over keys already on chip, writes its selection, and marks it in a page
-//    bitmap in its shared memory.
-//  * After a second barrier CTA c builds the union over its 1/G of the pages
-//    by reading the G bitmaps remotely; the CTAs' union counts are exchanged
-//    the same way, and each writes its part of the list in page order.  An
-//    entry holds the physical page (from the block-table entries CTA c loaded
-//    for its scoring) and the page's valid tokens | head mask << 8, so the
-//    attention needs no block-table lookup.
+//    over keys already on chip, writes its selection, and ORs its head's bit
+//    into the page map (a byte of head bits per page) of the CTA that owns
+//    the page's 1/G of the pages (red.shared::cluster, no reply awaited).
+//  * After a second barrier each CTA holds the complete map of its pages:
+//    it counts their union pages, the CTAs' counts are exchanged through
+//    distributed shared memory, and after a third barrier each writes its
+//    part of the list in page order.  An entry holds the physical page (from
+//    the block-table entries CTA c loaded for its scoring) and the page's
+//    valid tokens | head mask << 8, so the attention needs no block-table
+//    lookup.  (Reading the other CTAs' bitmaps remotely instead cost a round
+//    trip; OR-ing into every CTA's map, to skip the count exchange, cost G
+//    remote atomics per selected page: 13.7 -> 19.9 us on 8-head groups.)
 #include <algorithm>
 
 #include "kv_internal.cuh"
@@ -46,10 +50,8 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_cluster(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void red_or_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -84,17 +86,16 @@ __device__ __forceinline__ uint32_t sign_half(uint32_t w, bool neg) {
   return w & m;
 }
 
-// Shared memory after the radix state: keys[maxP4] | selbits[nwords4] |
-// bt_s[PC] | cnt[16]
+// Shared memory after the radix state: keys[maxP4] | map[PC bytes: head
+// bits of this CTA's pages] | bt_s[PC] | cnt[16]
 struct SelLayout {
-  int off_sel, off_bt, off_cnt, bytes;
+  int off_map, off_bt, off_cnt, bytes;
 };
 __host__ __device__ inline SelLayout sel_layout(int maxP, int PC) {
   SelLayout l;
   const int maxP4 = (maxP + 3) & ~3;
-  const int nwords = (((maxP + 31) / 32) + 3) & ~3;
-  l.off_sel = maxP4 * 4;
-  l.off_bt = l.off_sel + nwords * 4;
+  l.off_map = maxP4 * 4;
+  l.off_bt = l.off_map + PC;  // PC is a multiple of 32
   l.off_cnt = l.off_bt + PC * 4;
   l.bytes = l.off_cnt + 16 * 4;
   return l;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : 1)
   __shared__ RadixSmem<THREADS> rs;
   const SelLayout L = sel_layout(a.maxP, a.PC);
   uint32_t *keys = reinterpret_cast<uint32_t *>(sel_smem);
-  uint32_t *selbits = reinterpret_cast<uint32_t *>(sel_smem + L.off_sel);
+  uint32_t *map = reinterpret_cast<uint32_t *>(sel_smem + L.off_map);  // 4 pages a word
   int32_t *bt_s = reinterpret_cast<int32_t *>(sel_smem + L.off_bt);
   uint32_t *cnt = reinterpret_cast<uint32_t *>(sel_smem + L.off_cnt);
 
@@ -152,10 +153,13 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : 1)
   const bool bad_len = len < 1 || len > maxP * ps;
   const int P = bad_len ? 0 : (len + ps - 1) / ps;
   if (bad_len && c == 0 && tid == 0) flag_error(a.status, KV_ERR_BOUNDS);
-  const int nwords = (maxP + 31) / 32;
-  for (int i = tid; i < nwords; i += THREADS) selbits[i] = 0u;
+  const int nmw = PC / 4;  // words of this CTA's page map
+  for (int i = tid; i < nmw; i += THREADS) map[i] = 0u;
   for (int i = tid; i < 256; i += THREADS) rs.hist[0][i] = 0;
   __syncthreads();
+  // (without the scoring below, this barrier alone orders every CTA's zeroed
+  // map before the other CTAs' ORs into it)
+  if constexpr (!SCORE) cluster_arrive();
 
   // ---- scores of this CTA's pages for every head of the group -------------
   if constexpr (!SCORE) {
@@ -215,12 +219,16 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : 1)
   }
 
   // ---- top-K of this CTA's head over the keys on chip ---------------------
+  const uint32_t map_addr = smem_u32(map);
+  const uint32_t my_bit = 1u << c;
   const int keff = min(a.K, P);
-  if (keff == P) {
+  if (keff == P) {  // every page: the map is every head's on every valid page
+    if constexpr (!SCORE) cluster_wait();
     for (int i = tid; i < a.K; i += THREADS) orow[i] = i < P ? i : -1;
-    for (int i = tid; i < nwords; i += THREADS) {
-      const int n = min(32, P - 32 * i);
-      selbits[i] = n <= 0 ? 0u : (n == 32 ? 0xFFFFFFFFu : (1u << n) - 1u);
+    const uint32_t all = (1u << G) - 1u;
+    for (int i = tid; i < nmw; i += THREADS) {
+      const int n = min(4, P - (lo + 4 * i));
+      map[i] = n <= 0 ? 0u : (all * 0x01010101u) & (n == 4 ? 0xFFFFFFFFu : (1u << (8 * n)) - 1u);
     }
   } else {
     const int f_sink = a.sink_tokens > 0 ? min(P, (a.sink_tokens + ps - 1) / ps) : 0;
@@ -237,33 +245,38 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : 1)
     int krem;
     auto key_at = [&](int p) -> uint32_t { return keys[p]; };
     radix_threshold<THREADS>(rs, key_at, P, keff, kmin, kmax, prefix, pmask, krem);
+    if constexpr (!SCORE) cluster_wait();
     radix_emit<THREADS>(rs, key_at, keys, P, prefix, pmask, krem, [&](int pos, int p) {
       if (pos < a.K) orow[pos] = p;
-      atomicOr(&selbits[p >> 5], 1u << (p & 31));
+      const int owner = p / PC;  // the CTA whose pages p is in
+      red_or_cluster(map_rank(map_addr + ((uint32_t)(p - owner * PC) & ~3u), owner),
+                     my_bit << (8 * (p & 3)));
     });
     for (int i = keff + tid; i < a.K; i += THREADS) orow[i] = -1;
   }
   cluster_arrive();
   cluster_wait();
 
-  // ---- the group's union over this CTA's pages ----------------------------
-  // one thread per 32-page word: the G heads' bits of the word, read from
-  // every CTA of the cluster
-  const int nwd = PC / 32;
-  const int w = lo / 32 + tid;
-  uint32_t hb[G], u = 0u;
-#pragma unroll
-  for (int g = 0; g < G; ++g) hb[g] = 0u;
-  if (tid < nwd && 32 * w < P) {
-    const uint32_t addr = smem_u32(&selbits[w]);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      hb[g] = ld_cluster(map_rank(addr, g));
-      u |= hb[g];
-    }
-    if (P - 32 * w < 32) u &= (1u << (P - 32 * w)) - 1u;
+  // ---- the group's union over this CTA's pages ------------------------------
+  // Each thread counts the union pages of a run of consecutive map words; a
+  // block scan places the runs; the CTAs' totals are exchanged; the list is
+  // written in page order at the CTA's offset.
+  const int per = (nmw + THREADS - 1) / THREADS;  // map words per thread
+  const int w0 = min(nmw, tid * per), w1 = min(nmw, w0 + per);
+  auto page_bits = [&](int w) -> uint32_t {  // a valid page's head bits, 4 a word
+    uint32_t m = map[w];
+    const int n = P - (lo + 4 * w);
+    if (n < 4) m &= n <= 0 ? 0u : (1u << (8 * n)) - 1u;
+    return m;
+  };
+  uint32_t n = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t t = page_bits(w);
+    t |= t >> 4;
+    t |= t >> 2;
+    t |= t >> 1;
+    n += __popc(t & 0x01010101u);
   }
-  const uint32_t n = __popc(u);
   uint32_t ni = n;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -286,21 +299,19 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 128 ? 4 : 1)
     total += cnt[g];
   }
   pdl_trigger();
-  if (tid < nwd) {
-    pos += base;
-    uint32_t rest = u;
-    while (rest) {
-      const int bit = __ffs(rest) - 1;
-      rest &= rest - 1;
-      const int p = 32 * w + bit;
-      uint32_t m = 0u;
+  pos += base;
+  for (int w = w0; w < w1; ++w) {
+    const uint32_t m4 = page_bits(w);
 #pragma unroll
-      for (int g = 0; g < G; ++g) m |= ((hb[g] >> bit) & 1u) << g;
-      const long long x = bt_s[p - lo];
-      const bool okp = x >= 0 && x < a.nphys;
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = (m4 >> (8 * e)) & 0xFFu;
+      if (m == 0u) continue;
       if (pos < (uint32_t)a.umax) {
+        const int i = 4 * w + e;  // page lo + i
+        const long long x = bt_s[i];
+        const bool okp = x >= 0 && x < a.nphys;
         a.upages[gbase * a.umax + pos] = okp ? (int32_t)x : -1;
-        a.umasks[gbase * a.umax + pos] = (uint32_t)min(ps, len - p * ps) | (m << 8);
+        a.umasks[gbase * a.umax + pos] = (uint32_t)min(ps, len - (lo + i) * ps) | (m << 8);
       }
       ++pos;
     }
