@@ -296,6 +296,15 @@ int kv_dense_decode_attn_noalloc(const kv_shape *shape, const void *q, const voi
 int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
                          int32_t sink_words, void *stream);
 
+/* The same probe with its launch shape given: `blocks` thread blocks (sink
+ * holds `blocks` words) of `threads` threads (128, 256, 512 or 1024), each
+ * thread keeping `loads_in_flight` 16-byte loads in flight (4, 8 or 16).
+ * For sweeping the shape that reads a buffer fastest.  KV_ERR_INVALID_ARG
+ * for any other shape. */
+int kv_stream_read_probe_shape(const void *src, size_t bytes, unsigned long long *sink,
+                               int32_t blocks, int32_t threads, int32_t loads_in_flight,
+                               void *stream);
+
 /* One decode step of one layer on host buffers: q and context_lens come from
  * host memory, the path runs (k > 0: kv_select_pages and
  * kv_sparse_decode_attn_selected when workspace_bytes >=

@@ -16,20 +16,26 @@
 namespace kvs {
 namespace {
 
-// Every thread streams 16-byte loads (four in flight per iteration) over a
+// Every thread streams 16-byte loads (L in flight per iteration) over a
 // grid-stride range and folds them with XOR, so the loads cannot be elided;
 // one word per thread block is written.
-__global__ void __launch_bounds__(512)
+template <int L>
+__global__ void __launch_bounds__(1024)
     stream_read_kernel(const uint4 *src, size_t n16, unsigned long long *sink) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
-    acc.x ^= a.x ^ b.x ^ c.x ^ d.x;
-    acc.y ^= a.y ^ b.y ^ c.y ^ d.y;
-    acc.z ^= a.z ^ b.z ^ c.z ^ d.z;
-    acc.w ^= a.w ^ b.w ^ c.w ^ d.w;
+  for (; i + (L - 1) * stride < n16; i += L * stride) {
+    uint4 v[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+      acc.x ^= v[u].x;
+      acc.y ^= v[u].y;
+      acc.z ^= v[u].z;
+      acc.w ^= v[u].w;
+    }
   }
   for (; i < n16; i += stride) {
     const uint4 a = src[i];
@@ -38,7 +44,7 @@ __global__ void __launch_bounds__(512)
   unsigned long long v = ((unsigned long long)(acc.x ^ acc.z) << 32) | (acc.y ^ acc.w);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v ^= __shfl_xor_sync(0xFFFFFFFFu, v, off);
-  __shared__ unsigned long long red[16];
+  __shared__ unsigned long long red[32];
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -97,12 +103,13 @@ cudaError_t launch_stage_inputs(const void *q_src, void *q_dst, size_t q_bytes,
 }
 }  // namespace kvs
 
-extern "C" int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
-                                    int32_t sink_words, void *stream) {
-  KV_API_RANGE();
+static int probe_common(const void *src, size_t bytes, unsigned long long *sink, int blocks,
+                        int threads, int loads, void *stream) {
   using namespace kvs;
   if (!src || !sink || ((uintptr_t)src & 15u) || ((uintptr_t)sink & 7u) || bytes < 16 ||
-      (bytes & 15u) || sink_words < 1)
+      (bytes & 15u) || blocks < 1 || (threads != 128 && threads != 256 && threads != 512 &&
+                                      threads != 1024) ||
+      (loads != 4 && loads != 8 && loads != 16))
     return KV_ERR_INVALID_ARG;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, src) != cudaSuccess) {
@@ -116,15 +123,33 @@ extern "C" int kv_stream_read_probe(const void *src, size_t bytes, unsigned long
   } else if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) {
     return KV_ERR_LOCATION;
   }
+  const uint4 *s16 = static_cast<const uint4 *>(dsrc);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (loads) {
+    case 4: stream_read_kernel<4><<<blocks, threads, 0, st>>>(s16, bytes / 16, sink); break;
+    case 8: stream_read_kernel<8><<<blocks, threads, 0, st>>>(s16, bytes / 16, sink); break;
+    default: stream_read_kernel<16><<<blocks, threads, 0, st>>>(s16, bytes / 16, sink); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+extern "C" int kv_stream_read_probe(const void *src, size_t bytes, unsigned long long *sink,
+                                    int32_t sink_words, void *stream) {
+  KV_API_RANGE();
+  if (sink_words < 1) return KV_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     return KV_ERR_CUDA;
   }
-  int blocks = sms * 4;
-  if (blocks > sink_words) blocks = sink_words;
-  stream_read_kernel<<<blocks, 512, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4 *>(dsrc), bytes / 16, sink);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return probe_common(src, bytes, sink, std::min(sms * 4, (int)sink_words), 512, 4, stream);
+}
+
+extern "C" int kv_stream_read_probe_shape(const void *src, size_t bytes,
+                                          unsigned long long *sink, int32_t blocks,
+                                          int32_t threads, int32_t loads_in_flight,
+                                          void *stream) {
+  KV_API_RANGE();
+  return probe_common(src, bytes, sink, blocks, threads, loads_in_flight, stream);
 }

@@ -104,6 +104,7 @@ def load(path: str = LIB_PATH):
         "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv_debug_config": (ctypes.c_int, [i32, ctypes.c_uint64]),
         "kv_stream_read_probe": (ctypes.c_int, [P, sz, P, i32, P]),
+        "kv_stream_read_probe_shape": (ctypes.c_int, [P, sz, P, i32, i32, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -308,3 +309,12 @@ def kv_stream_read_probe(src, nbytes, sink, stream=None, check=True):
     rc = load().kv_stream_read_probe(_ptr(src), int(nbytes), _ptr(sink), int(sink.numel()),
                                      _stream(stream))
     return _ret(rc, "kv_stream_read_probe", check)
+
+
+def kv_stream_read_probe_shape(src, nbytes, sink, blocks, threads, loads_in_flight, stream=None,
+                               check=True):
+    """kv_stream_read_probe with its launch shape given; sink holds one int64
+    word per block."""
+    rc = load().kv_stream_read_probe_shape(_ptr(src), int(nbytes), _ptr(sink), int(blocks),
+                                           int(threads), int(loads_in_flight), _stream(stream))
+    return _ret(rc, "kv_stream_read_probe_shape", check)

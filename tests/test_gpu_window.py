@@ -150,8 +150,8 @@ def test_window_rejects_a_window_smaller_than_one_step():
 
 def test_window_full_size_llama_128k_host_sampled():
     # the 128k-token host-resident Llama-3.1-8B layer, 6 decode steps of a
-    # drifting query; the sampled query heads run on the oracle's own
-    # selection so the oracle sees no GPU output
+    # drifting query; every query head runs on the oracle's own selection
+    # (the window's state still follows it), so the oracle sees no GPU output
     spec = W.WORKLOADS["llama3.1-8b-b1-ctx128k-host"]
     wl = W.generate(spec)
     K = spec.topk
@@ -168,12 +168,11 @@ def test_window_full_size_llama_128k_host_sampled():
         layer.select()
         ref_s = oracle.scores("bf16", q, mn, mx, wl.block_table, wl.context_lens, 16)
         ref_idx = oracle.topk(ref_s, wl.context_lens, 16, K)
-        sel = layer.indices.cpu().numpy()
-        sel[0, :spec.group] = ref_idx[0, :spec.group]       # kv head 0's group: oracle's
+        sel = ref_idx.copy()                                 # every group: the oracle's
         layer.window_attn(indices=torch.from_numpy(sel).cuda())
         torch.cuda.synchronize()
         assert kv.kv_device_status() == kv.KV_OK
-        rows = [0, 1, spec.group - 1]
+        rows = list(range(spec.num_q_heads))                 # every kv-head group
         ref = oracle.attention("bf16", q, wl.k_cache, wl.v_cache, wl.block_table,
                                wl.context_lens, wl.scale, indices=sel, rows=rows)
         out = layer.out.cpu().numpy()

@@ -2,11 +2,14 @@
 benchmark times, on outputs sampled per (sequence, head).
 
 For each workload the GPU runs the whole path (index build, page scores,
-top-K, sparse attention, dense attention) over every row; the fp64 oracle then
-recomputes, for sampled sequences, their index entries (bit-exact), score rows
-(fp32-accumulation bound), selections (boundary exemption) and, for sampled
-query heads, the sparse attention over the oracle's own selection and the
-dense attention (max-abs 2e-3 for 16-bit inputs, 1e-5 for fp32).
+top-K, sparse attention, dense attention, and the one-call selection with the
+attention over its lists) over every row; the fp64 oracle then recomputes,
+for the first and last sequence, their index entries (bit-exact), score rows
+(fp32-accumulation bound), selections (boundary exemption) and, for every
+query head of those sequences (every head chunk of every kv-head group), the
+sparse attention over the oracle's own selection and the dense attention
+(max-abs 2e-3 for 16-bit inputs, 1e-5 for fp32); the one-call path's output
+is compared on the heads whose selection equals the oracle's.
 """
 import numpy as np
 import pytest
@@ -25,10 +28,7 @@ pytestmark = pytest.mark.gpu
 
 def sample_rows(spec):
     bs = sorted({0, spec.batch - 1})
-    G = spec.group
-    H = spec.num_q_heads
-    hs = sorted({min(h, H - 1) for h in (0, G, H // 2 + 1, H - 1)})
-    return bs, hs
+    return bs, list(range(spec.num_q_heads))
 
 
 @pytest.fixture(autouse=True)
@@ -97,3 +97,22 @@ def test_full_workload_sampled(name):
             ed = np.abs(dense[b, h] - ref_d[b, h]).max()
             assert es <= ATOL[dtype], (name, b, h, "sparse", es)
             assert ed <= ATOL[dtype], (name, b, h, "dense", ed)
+
+    # the one-call selection and the attention over its lists: its selection
+    # is the separate calls' (bit for bit); its output on the sampled heads
+    # whose selection is the oracle's
+    if spec.topk:
+        layer.select_fused()
+        layer.sparse_attn_selected()
+        torch.cuda.synchronize()
+        assert kv.kv_device_status() == kv.KV_OK
+        assert np.array_equal(layer.indices.cpu().numpy(), gpu_idx)
+        fused = layer.out.cpu().numpy()
+        same = 0
+        for b in bs:
+            for h in hs:
+                if np.array_equal(gpu_idx[b, h], oracle_idx[b][h]):
+                    same += 1
+                    ef = np.abs(fused[b, h] - ref_s[b, h]).max()
+                    assert ef <= ATOL[dtype], (name, b, h, "one-call", ef)
+        assert same >= 0.9 * len(bs) * len(hs)
