@@ -129,6 +129,12 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
                 const __grid_constant__ CUtensorMap tv) {
   using Ent = PageEnt<WIN>;
   static_assert(sizeof(Ent) == attn_entry_bytes(WIN), "page-list entry size");
+  // the producer's first TMA needs the tensor maps: fetch them while the
+  // prologue runs
+  if (a.use_tma && threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+  }
   if constexpr (MMA) pdl_wait();
   constexpr int SL = (int)sizeof(T);        // 128-byte slabs per 128-element row
   constexpr int EPS = 128 / (int)sizeof(T); // elements per slab
@@ -687,28 +693,42 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
     }
   }
   __syncthreads();
+  // a thread per 4 consecutive channels of one head: 16-byte loads of the
+  // warps' partials and one 16-byte store (the stores of a CTA's last
+  // partials queue behind the other CTAs' loads at the end of the call)
   const long long rows = (long long)a.B * a.Hq;
-  for (int i = threadIdx.x; i < GC * kHeadDim; i += blockDim.x) {
-    const int g = i / kHeadDim, dd = i % kHeadDim;
+  for (int i = threadIdx.x; i < GC * (kHeadDim / 4); i += blockDim.x) {
+    const int g = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < a.nw; ++w) M = fmaxf(M, mw[w * GC + g]);
-    float o = 0.f, l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < a.nw; ++w) {
         const float m = mw[w * GC + g];
         const float f = m == -INFINITY ? 0.f : ex2(m - M);
-        o = fmaf(f, ow[(w * GC + g) * kHeadDim + dd], o);
+        const float4 x = *reinterpret_cast<const float4 *>(ow + (w * GC + g) * kHeadDim + 4 * d4);
+        o.x = fmaf(f, x.x, o.x);
+        o.y = fmaf(f, x.y, o.y);
+        o.z = fmaf(f, x.z, o.z);
+        o.w = fmaf(f, x.w, o.w);
         l = fmaf(f, lw[w * GC + g], l);
       }
     }
     const long long r = (long long)b * a.Hq + head0 + g;
     if (a.num_splits == 1) {
-      a.out[r * kHeadDim + dd] = l > 0.f ? o / l : 0.f;
+      float4 y;
+      y.x = l > 0.f ? o.x / l : 0.f;
+      y.y = l > 0.f ? o.y / l : 0.f;
+      y.z = l > 0.f ? o.z / l : 0.f;
+      y.w = l > 0.f ? o.w / l : 0.f;
+      *reinterpret_cast<float4 *>(a.out + r * kHeadDim + 4 * d4) = y;
     } else {
-      a.part_o[((long long)split * rows + r) * kHeadDim + dd] = o;
-      if (dd == 0) {
+      *reinterpret_cast<float4 *>(a.part_o + ((long long)split * rows + r) * kHeadDim + 4 * d4) =
+          o;
+      if (d4 == 0) {
         a.part_ml[((long long)split * rows + r) * 2] = M;
         a.part_ml[((long long)split * rows + r) * 2 + 1] = l;
       }
