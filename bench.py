@@ -490,12 +490,57 @@ def scores_in_memory(layer):
     return kv.kv_select_workspace_bytes(layer.shape, k) > kv.kv_attn_workspace_bytes(layer.shape, k)
 
 
-def kv_copies_for(spec):
-    """Rotating K/V copies so that one pass over them exceeds 4x the L2."""
+def kv_copies_for(spec, cap=8):
+    """Rotating K/V copies so that one pass over them exceeds 4x the L2 (at
+    most `cap`)."""
     l2_bytes = 129 * 2**20
     if spec.kv_loc != "hbm":
         return 1
-    return max(1, min(8, math.ceil(4 * l2_bytes / spec.kv_bytes())))
+    return max(1, min(cap, math.ceil(4 * l2_bytes / spec.kv_bytes())))
+
+
+def l2_note(spec, copies):
+    """How the timed steps keep K/V out of L2, for the config record."""
+    mib = spec.kv_bytes() / 2**20
+    if copies == 1:
+        return "K/V larger than L2"
+    if copies * spec.kv_bytes() >= 4 * 129 * 2**20:
+        return f"{copies} rotating K/V copies of {mib:.0f} MiB each (> 4x the 129 MB L2 in total)"
+    return (f"{copies} rotating K/V copies of {mib:.0f} MiB each stay in L2; `l2_rotated` times "
+            f"the step over enough copies to fill 4x the L2")
+
+
+def l2_rotated(spec, wl, step_fn_of, step_bytes, reps=3):
+    """For a workload whose K/V fit in L2 many times over: the step over as
+    many rotating K/V copies as fill 4x the L2, one CUDA graph with a step per
+    copy, so no step finds its pages in L2 (the main timed steps rotate over at
+    most R_GRAPH copies and so measure the L2-resident latency)."""
+    import torch
+    from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+    copies = kv_copies_for(spec, cap=256)
+    layer = DecodeLayer(wl, kv_copies=copies)
+    fn = step_fn_of(layer)
+    ms = run_graph_steps_n(layer, copies, fn, copies, reps)
+    del layer
+    torch.cuda.empty_cache()
+    return {"copies": copies, "bytes_rotated": int(copies * spec.kv_bytes()),
+            "ms_per_step": round(ms, 5), "GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 2)}
+
+
+def run_graph_steps_n(layer, copies, fn, n, reps):
+    """Device ms per call of fn over one graph of n calls rotating the K/V
+    copies, replayed reps times after one warm replay."""
+    import torch
+    g = _capture(layer, copies, fn, n)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * n)
 
 
 def cpu_model() -> str:
@@ -878,6 +923,19 @@ def main():
                        "bytes": a_bytes}
     assert kv.kv_device_status() == kv.KV_OK
 
+    # a workload whose K/V the graphs' rotation leaves in L2: the step over
+    # enough rotating copies to defeat it, as a side measurement
+    if kv_copies_for(spec, cap=256) > R_GRAPH:
+        if sparse:
+            def step_of(lay):
+                lay.build_index()
+                lay.select_fused()
+                return lambda: (lay.select_fused(), lay.sparse_attn_selected())
+        else:
+            def step_of(lay):
+                return lay.dense_step
+        extra["l2_rotated"] = l2_rotated(spec, wl, step_of, step_bytes)
+
     # other sparse workloads, shorter runs, after the default one
     side = {}
     for name in [n for n in args.side_workloads.split(",") if n and n != spec.name]:
@@ -921,9 +979,7 @@ def main():
                        "context": spec.context, "page_size": spec.page_size,
                        "topk": spec.topk, "kv_loc": spec.kv_loc, "accumulate": "f32",
                        "step": (STEP_NAME if sparse else "dense attention"),
-                       "l2": (f"{copies} rotating K/V copies of {spec.kv_bytes() / 2**20:.0f} MiB "
-                              f"each (> 4x the 129 MB L2 in total)" if copies > 1 else
-                              "K/V larger than L2"),
+                       "l2": l2_note(spec, copies),
                        "splits": splits,
                        "timing": ("CUDA events around exactly K steps replayed as CUDA graphs of "
                                   f"{R_GRAPH} steps; per-kernel times from graphs of each stage alone"),
