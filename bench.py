@@ -46,11 +46,30 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # workload (its batch in "from_batch"), applied to this launch's algorithmic
 # bytes (the traffic grows with the union bytes the launch reads).
 NCU_TRAFFIC = {
-    # attention kernel of kv_sparse_decode_attn_selected at batch 1 (two
-    # launches, 135.68 MB read + 0.52 MB written against 135.61 MB)
-    "70b-gqa-b8-ctx64k-ps64": {"per_alg_byte": 1.00431, "from_batch": 1,
-                               "src": "1a68e81670a4ced2"},
+    # attention + combine launches of kv_sparse_decode_attn_selected at batch 2
+    # (274.23 MB + 1.89 MB against 274.11 MB algorithmic; ncu empties the
+    # caches before each launch, so the combine's partials, which stay in L2
+    # between the two launches in a timed step, count as DRAM reads here)
+    "70b-gqa-b8-ctx64k-ps64": {"per_alg_byte": 1.00734, "from_batch": 2,
+                               "src": "6818ad5264681ba4"},
+    # the same two launches at full size (189.71 MB against 188.65 MB)
+    "llama3.1-8b-b4-ctx32k": {"per_alg_byte": 1.00565, "from_batch": 4,
+                              "src": "6818ad5264681ba4"},
 }
+
+
+def ncu_traffic(spec, attn_bytes, batch_override=0):
+    """(DRAM bytes of one attention call from the table above, how they were
+    obtained), or (None, None) when there is no record for this kernel."""
+    rec = NCU_TRAFFIC.get(spec.name)
+    if not rec or rec.get("src") != kernel_source_hash() or batch_override:
+        return None, None
+    if "bytes" in rec:
+        return rec["bytes"], "ncu DRAM bytes of a full-size launch"
+    how = ("full-size" if rec["from_batch"] == spec.batch else f"batch-{rec['from_batch']}")
+    return (round(rec["per_alg_byte"] * attn_bytes),
+            f"ncu DRAM bytes of a {how} call (attention + combine launches) per algorithmic "
+            "byte, times this call's algorithmic bytes")
 
 
 def kernel_source_hash() -> str:
@@ -606,6 +625,7 @@ def side_workload(name, steps, warm):
            "attention_call": {"bound": bound, "achieved": round(achieved, 1),
                               "peak": round(peak, 1), "unit": "GB/s",
                               "frac": round(achieved / peak, 4), "bytes": int(attn_bytes),
+                              "traffic": ncu_traffic(spec, attn_bytes)[0],
                               "peak_source": peak_source},
            "l2": (f"{copies} rotating K/V copies" if copies > 1 else
                   ("K/V in pinned host memory" if spec.kv_loc == "host" else "K/V larger than L2"))}
@@ -951,12 +971,9 @@ def main():
         peak, bound = link["peak"], "host-link"
         peak_source = link_source(link)
     achieved = attn_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = None
+    traffic, traffic_source = ncu_traffic(spec, attn_bytes, args.batch)
     rec = NCU_TRAFFIC.get(spec.name)
-    link_traffic = None
-    if rec and rec.get("src") == kernel_source_hash() and args.batch == 0:
-        traffic = rec["bytes"] if "bytes" in rec else round(rec["per_alg_byte"] * attn_bytes)
-        link_traffic = rec.get("link_bytes")
+    link_traffic = rec.get("link_bytes") if rec and traffic else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -988,10 +1005,7 @@ def main():
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": int(attn_bytes),
-                         **({"traffic_source": f"ncu DRAM bytes of a batch-{rec['from_batch']} "
-                                               "launch of the same kernel, scaled by algorithmic "
-                                               "bytes"} if traffic and rec and "per_alg_byte" in rec
-                            else {}),
+                         **({"traffic_source": traffic_source} if traffic else {}),
                          **({"link_traffic": link_traffic} if spec.kv_loc == "host" else {}),
                          "kernel": ("kv_sparse_decode_attn_selected (attention + combine)" if sparse
                                     else "kv_dense_decode_attn (attention"

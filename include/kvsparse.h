@@ -422,6 +422,28 @@ const char *kv_status_string(int status);
  * Returns KV_OK or KV_ERR_INVALID_ARG. */
 int kv_debug_config(int32_t skip_page, uint64_t wait_limit_ns);
 
+/* Testing hook for the attention over kv_select_pages' lists
+ * (kv_sparse_decode_attn_selected and kv_decode_step).  Its CTAs either split
+ * each (sequence, kv head) group's union list over the group's own splits, or
+ * cut the lists of all groups, laid end to end, into one equal chunk per CTA
+ * (possible when every group holds at least a chunk; a CTA then covers the
+ * tail of one group and the head of the next at most, and the combine merges
+ * the pieces).  The two give the same result up to the order of the
+ * floating-point merge.  The shapes must allow equal chunks at all: 16-bit
+ * data, 4 or 8 query heads per kv head, more than one split, at most 4096
+ * groups.
+ *   mode -1 (default): where a CTA's share of a group's list can take 100 us
+ *     or more to stream, the kernel chooses per call from the groups' list
+ *     lengths (equal chunks when the per-group split's longest CTA would
+ *     stream more K/V than an equal chunk for longer than about 2.5 us);
+ *     elsewhere the split per group, with no cost for the choice;
+ *   0: always the split per group;
+ *   1: equal chunks whenever possible;
+ *   2: the kernel chooses, as in -1, for every call the shapes allow.
+ * Process-wide; not for concurrent use with other calls.  Returns KV_OK or
+ * KV_ERR_INVALID_ARG. */
+int kv_debug_split_mode(int32_t mode);
+
 #ifdef __cplusplus
 }
 #endif

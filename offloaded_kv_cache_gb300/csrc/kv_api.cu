@@ -23,8 +23,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<int *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 
-// testing hooks (kv_debug_config)
+// testing hooks (kv_debug_config, kv_debug_split_mode)
 std::atomic<int> g_debug_skip_page{-1};
+std::atomic<int> g_split_mode{-1};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 int current_device() {
@@ -113,6 +114,11 @@ struct Plan {
   int S = 1, umax = 0, nstages = 4, nw = 4, header = 8192;
   size_t smem = 0;
   size_t off_part_o = 0, off_part_ml = 0, off_upages = 0, off_umasks = 0, off_ucount = 0;
+  // the attention over kv_select_pages' lists may cut all groups' lists into
+  // equal chunks (AttnArgs::spread) when the shapes allow it (spread_ok; its
+  // workspace is then reserved)
+  bool spread_ok = false;
+  size_t off_spa_o = 0, off_spa_ml = 0, off_gmeta = 0;
   size_t total = 0;
 };
 
@@ -138,6 +144,24 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 #ifndef KVS_SPLIT_OVERHEAD_TILES
 #define KVS_SPLIT_OVERHEAD_TILES 4  // fixed cost of a CTA, in tiles, for the split choice
 #endif
+// The attention over kv_select_pages' lists takes equal chunks of all groups'
+// lists when the longest CTA of the per-group split would stream more K/V
+// than an equal chunk for longer than this: the prefix sums' round trip
+// before the first load and the combine's lookup of where the partials are
+// (measured together at about 2.5 us on GB300)
+#ifndef KVS_SPREAD_FIXED_NS
+#define KVS_SPREAD_FIXED_NS 2500
+#endif
+// Making that choice at all costs the kernels about 1.5 us (the groups'
+// lengths and a block reduction before the first load, the combine's lookup;
+// Llama-3.1-8B 32k call 36.4 -> 37.8 us when the split per group is kept), so
+// the plan only lets the kernel choose when a CTA's share of a group's list
+// can take this long to stream with all CTAs sharing the link (70B-class
+// layer: about 300 us; Llama-3.1-8B 32k: about 38 us)
+#ifndef KVS_SPREAD_MIN_CTA_NS
+#define KVS_SPREAD_MIN_CTA_NS 100000
+#endif
+constexpr int kSpreadMaxGroups = 4096;
 
 int header_bytes(const Plan &pl, int elem, long long list_pages) {
   const long long b = attn_fixed_header(elem, pl.gc, pl.mma) +
@@ -267,6 +291,13 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device, bool win) {
     pl.smem = 1024 + pl.header + (size_t)ns * stage;
   }
   pl.umax = k > 0 ? (int)work : 0;
+  {
+    const long long ng = (long long)s->batch * pl.groups;
+    const long long ring = (long long)pl.nstages * stage;
+    pl.spread_ok = k > 0 && !win && pl.mma && pl.nchunk == 1 && pl.S > 1 &&
+                   ng <= kSpreadMaxGroups && ng * pl.umax < (1LL << 30) &&
+                   ((ng + 1 + 31) / 32 * 32 + 96) * 4 <= ring;
+  }
   size_t off = 0;
   const size_t rows = (size_t)s->batch * s->num_q_heads;
   if (pl.S > 1) {
@@ -283,6 +314,14 @@ Plan make_plan(const kv_shape *s, int k, int sms, bool have_device, bool win) {
     off = align256(off + ng * pl.umax * 4);
     pl.off_ucount = off;
     off = align256(off + ng * 4);
+    if (pl.spread_ok) {
+      pl.off_spa_o = off;
+      off = align256(off + ng * pl.nw * pl.gc * kHeadDim * 4);
+      pl.off_spa_ml = off;
+      off = align256(off + ng * pl.nw * pl.gc * 2 * 4);
+      pl.off_gmeta = off;
+      off = align256(off + ng * 16);
+    }
   }
   pl.total = off;
   return pl;
@@ -519,6 +558,26 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
   // attention kernel is the first of the call
   a.early_inputs = ready ? ready->early_inputs : indices ? 1 : 0;
   a.union_resolved = ready && ready->resolved ? 1 : 0;
+  const int split_mode = g_split_mode.load();
+  a.spread = 0;
+  if (a.union_resolved && pl.spread_ok && split_mode != 0) {
+    // a CTA's share of the link when all CTAs stream (nominal HBM 7 TB/s,
+    // host link 200 GB/s), in bytes per ns
+    const double link = as->kv_loc == KV_LOC_HBM ? 7.0e3 : 2.0e2;
+    const double ctas = (double)pl.S * s->batch * pl.groups;
+    const double share_bytes = (double)((pl.umax + pl.S - 1) / pl.S) * 2.0 * as->page_size *
+                               kHeadDim * elem_bytes(as->dtype);
+    if (split_mode == 1) a.spread = 2;
+    else if (split_mode == 2 || share_bytes / (link / ctas) >= KVS_SPREAD_MIN_CTA_NS) a.spread = 1;
+    // K/V bytes a CTA streams in KVS_SPREAD_FIXED_NS
+    a.spread_min_gain = (int)std::min(1.0e9, link / ctas * KVS_SPREAD_FIXED_NS);
+  }
+  if (a.spread) {
+    a.ngroups = s->batch * pl.groups;
+    a.spa_o = reinterpret_cast<float *>(w + pl.off_spa_o);
+    a.spa_ml = reinterpret_cast<float *>(w + pl.off_spa_ml);
+    a.gmeta = reinterpret_cast<int32_t *>(w + pl.off_gmeta);
+  }
   if (pl.S > 1) {
     a.part_o = reinterpret_cast<float *>(w + pl.off_part_o);
     a.part_ml = reinterpret_cast<float *>(w + pl.off_part_ml);
@@ -563,7 +622,10 @@ int attn_common(const kv_shape *s, const void *q, const void *k_cache, const voi
                            : launch_attn_core(s->dtype, pl.gc, a, &tk, &tv, grid, pl.smem, st);
   if (e != cudaSuccess) return KV_ERR_CUDA;
   if (pl.S > 1) {
-    e = launch_combine(a.part_o, a.part_ml, out, pl.S, s->batch, s->num_q_heads, st);
+    e = a.spread ? launch_combine_lists(a.part_o, a.part_ml, a.spa_o, a.spa_ml, a.gmeta, out,
+                                        pl.S, s->batch, s->num_q_heads, s->num_kv_heads, pl.nw,
+                                        status, st)
+                 : launch_combine(a.part_o, a.part_ml, out, pl.S, s->batch, s->num_q_heads, st);
     if (e != cudaSuccess) return KV_ERR_CUDA;
   }
   return KV_OK;
@@ -1092,6 +1154,12 @@ const char *kv_status_string(int status) {
     case KV_ERR_BOUNDS: return "KV_ERR_BOUNDS";
     default: return "KV_ERR_UNKNOWN";
   }
+}
+
+int kv_debug_split_mode(int32_t mode) {
+  if (mode < -1 || mode > 2) return KV_ERR_INVALID_ARG;
+  g_split_mode.store(mode);
+  return KV_OK;
 }
 
 int kv_debug_config(int32_t skip_page, uint64_t wait_limit_ns) {

@@ -107,6 +107,134 @@ __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uin
 struct PageRange {
   int lo, n;  // first index into the (dense or union) list, count
 };
+
+// ---------------------------------------------------------------------------
+// equal chunks of the concatenated union lists (AttnArgs::spread)
+// ---------------------------------------------------------------------------
+// With every group's list split over the same S CTAs, a group whose union is
+// larger than the others' gives its CTAs more pages, and the call ends with
+// them: rows of different context lengths in one batch, or GQA groups whose
+// heads agree less on their pages.  Instead, CTA i of N can take entries
+// [i T / N, (i + 1) T / N) of the groups' lists laid end to end (T entries,
+// groups in (sequence, kv head) order).  When every group holds at least
+// ceil(T / N) entries, a chunk meets at most two groups: the tail of one
+// (segment A) and the head of the next (segment B).
+struct SpreadShare {
+  bool on;
+  int T;                 // entries of all groups
+  int gA, offA, lenA;    // segment A: entries offA .. offA + lenA - 1 of group gA
+  int gB, lenB;          // segment B (lenB > 0): entries 0 .. lenB - 1 of group gB
+};
+
+// Step 1, every thread of the CTA after the PDL wait: the groups' list
+// lengths into pre[1 .. ngroups] (shared memory), and the decision, the same
+// in every CTA.  a.spread 2 takes equal chunks whenever they are possible; 1
+// only when the per-group split's longest CTA holds at least
+// a.spread_min_gain bytes more K/V than an equal chunk (the price of the
+// prefix sums' round trip before the first load and of the longer combine).
+// red: 96 ints of scratch.
+__device__ __forceinline__ SpreadShare spread_decide(const AttnArgs &a, long long ncta,
+                                                     int page_bytes, int32_t *pre, int *red) {
+  const int NG = a.ngroups;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+  const int per = (NG + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int g0 = min(NG, t * per), g1 = min(NG, g0 + per);
+  int sum = 0, mn = INT_MAX, mx = 0;
+  for (int g = g0; g < g1; ++g) {
+    const int l = ld_issue(a.context_lens + g / a.Hkv);
+    const int cnt = ld_issue(a.union_count + g);
+    const bool bad = l < 1 || l > a.maxP * a.ps;  // such a row's list is empty
+    const int u = bad ? 0 : min(max(cnt, 0), a.umax);
+    pre[g + 1] = u;
+    sum += u;
+    mn = min(mn, u);
+    mx = max(mx, u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  }
+  if (lane == 0) {
+    red[warp] = sum;
+    red[32 + warp] = mn;
+    red[64 + warp] = mx;
+  }
+  __syncthreads();
+  int T = 0, minU = INT_MAX, maxU = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    T += red[w];
+    minU = min(minU, red[32 + w]);
+    maxU = max(maxU, red[64 + w]);
+  }
+  SpreadShare sh{};
+  sh.T = T;
+  sh.on = T >= ncta && (long long)minU * ncta >= T;
+  if (sh.on && a.spread == 1) {
+    const int S = a.num_splits;
+    const long long chunk = (T + ncta - 1) / ncta;
+    sh.on = ((long long)(maxU + S - 1) / S - chunk) * page_bytes >= a.spread_min_gain;
+  }
+  return sh;
+}
+
+// Step 2, when sh.on: prefix sums of the lengths in pre[0 .. ngroups] and this
+// CTA's chunk.  Every thread; red: 32 ints of scratch (reused).
+__device__ __forceinline__ void spread_share(const AttnArgs &a, long long cta, long long ncta,
+                                             int32_t *pre, int *red, SpreadShare &sh) {
+  const int NG = a.ngroups;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+  const int per = (NG + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int g0 = min(NG, t * per), g1 = min(NG, g0 + per);
+  int sum = 0;
+  for (int g = g0; g < g1; ++g) sum += pre[g + 1];
+  int inc = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+    if (lane >= off) inc += x;
+  }
+  __syncthreads();  // every warp has read red[] of step 1
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp && w < nwarps; ++w) base += red[w];
+  int run = base + inc - sum;
+  if (t == 0) pre[0] = 0;
+  for (int g = g0; g < g1; ++g) {
+    run += pre[g + 1];
+    pre[g + 1] = run;
+  }
+  __syncthreads();
+  const int T = sh.T;
+  const long long c0 = cta * T / ncta, c1 = (cta + 1) * T / ncta;
+  int lo = 0, hi = NG - 1;  // the group holding entry c0: the last g with pre[g] <= c0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= c0) lo = mid;
+    else hi = mid - 1;
+  }
+  const long long endA = min(c1, (long long)pre[lo + 1]);
+  sh.gA = lo;
+  sh.offA = (int)(c0 - pre[lo]);
+  sh.lenA = (int)(endA - c0);
+  sh.gB = lo + 1;
+  sh.lenB = (int)(c1 - endA);
+}
+
+// gmeta of group g, written by the CTA whose chunk holds the group's first
+// entry: the CTAs first..last whose chunks meet g, and whether the last one
+// goes on past g's end (then g is its segment A).  Chunk of entry e: the last
+// i with i T / N <= e, that is ((e + 1) N - 1) / T.
+__device__ __forceinline__ void spread_meta(const AttnArgs &a, const int32_t *pre, int g,
+                                            long long cta, long long ncta, int T) {
+  const long long end = pre[g + 1];  // one past g's last entry
+  const long long last = (end * ncta - 1) / T;
+  const long long next = (last + 1) * T / ncta;  // where that chunk ends
+  reinterpret_cast<int4 *>(a.gmeta)[g] =
+      make_int4(kSplitSpread, (int)cta, (int)last, next > end ? 1 : 0);
+}
 // one page of the list, resolved once in the prologue: physical page (-1 when
 // the entry is out of range) and (valid tokens | head mask << 8); the window
 // instantiations add the source page to fetch (-1: the window slot holds it)
@@ -211,6 +339,14 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   const int S = a.num_splits;
   int32_t sp_page[kSpec];
   uint32_t sp_mask[kSpec];
+  PageRange rng;
+  // equal chunks of all groups' lists (spread): segment A of group (bA, kvhA)
+  // is entries 0 .. segB - 1 of this CTA's list, segment B of (bB, kvhB) the
+  // rest; the split per group has one segment, this CTA's own group
+  bool spread = false;
+  int segB = INT_MAX, gA = (int)gidx;
+  int bA = b, kvhA = kvh, bB = b, kvhB = kvh;
+  const int len = ld_issue(a.context_lens + b);  // in flight with the entries below
   if (sparse) {
 #pragma unroll
     for (int u = 0; u < kSpec; ++u) {
@@ -219,16 +355,62 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       sp_page[u] = -1;
       sp_mask[u] = 0u;
       if (j < kMaxListPages && e < a.umax) {
-        sp_page[u] = a.union_pages[gidx * a.umax + e];
-        sp_mask[u] = a.union_masks[gidx * a.umax + e];
+        sp_page[u] = ld_issue(a.union_pages + gidx * a.umax + e);
+        sp_mask[u] = ld_issue(a.union_masks + gidx * a.umax + e);
       }
     }
   }
-  const int len = a.context_lens[b];
+  if constexpr (MMA && !WIN) {
+    if (a.spread) {
+      // the groups' lengths load together with the entries above (the split
+      // per group's), so keeping that split costs no extra round trip
+      const long long ncta = (long long)gridDim.x * a.ngroups;
+      const long long cta = (long long)split * a.ngroups + gidx;
+      int32_t *pre = reinterpret_cast<int32_t *>(stages);  // the idle ring
+      int *red = pre + ((a.ngroups + 1 + 31) & ~31);
+      SpreadShare sh = spread_decide(a, ncta, (int)(2 * ps * kHeadDim * sizeof(T)), pre, red);
+      spread = sh.on;
+      if (spread) {
+        spread_share(a, cta, ncta, pre, red, sh);
+        if (threadIdx.x == 0) {
+          if (sh.offA == 0) spread_meta(a, pre, sh.gA, cta, ncta, sh.T);
+          if (sh.lenB > 0) spread_meta(a, pre, sh.gB, cta, ncta, sh.T);
+        }
+        const int n = sh.lenA + sh.lenB;  // at most ceil(T / N) <= kMaxListPages
+#pragma unroll
+        for (int u = 0; u < kSpec; ++u) {
+          const int j = threadIdx.x + u * blockDim.x;
+          sp_page[u] = -1;
+          sp_mask[u] = 0u;
+          if (j < n && j < kMaxListPages) {
+            const long long e = j < sh.lenA ? (long long)sh.gA * a.umax + sh.offA + j
+                                            : (long long)sh.gB * a.umax + (j - sh.lenA);
+            sp_page[u] = a.union_pages[e];
+            sp_mask[u] = a.union_masks[e];
+          }
+        }
+        rng.lo = 0;
+        rng.n = min(n, kMaxListPages);
+        gA = sh.gA;
+        bA = bB = gA / a.Hkv;
+        kvhA = kvhB = gA % a.Hkv;
+        if (sh.lenB > 0) {
+          segB = sh.lenA;
+          bB = sh.gB / a.Hkv;
+          kvhB = sh.gB % a.Hkv;
+        }
+      } else if (split == 0 && threadIdx.x == 0) {
+        reinterpret_cast<int4 *>(a.gmeta)[gidx] = make_int4(kSplitPerGroup, 0, 0, 0);
+      }
+      // the ring that held the lengths is next written by TMA
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+  }
   const bool bad_len = len < 1 || len > a.maxP * ps;
   const int P = bad_len ? 0 : (len + ps - 1) / ps;
-  PageRange rng;
-  if (sparse) {
+  if (spread) {
+    // rng set above
+  } else if (sparse) {
     const int total = bad_len ? 0 : min(a.union_count[gidx], a.umax);
     rng.lo = split;
     rng.n = total > split ? min((total - split + S - 1) / S, kMaxListPages) : 0;
@@ -368,7 +550,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
           if (j == a.debug_skip_page) continue;
           const uint32_t fb = smem_u32(&full[s]);
           const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
-          const int row0 = (int)((phys * a.Hkv + kvh) * ps) + (j % UPP) * TT;
+          const int kh = j / UPP < segB ? kvhA : kvhB;
+          const int row0 = (int)((phys * a.Hkv + kh) * ps) + (j % UPP) * TT;
           mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
           tma_load_3d(dst, &tk, 0, row0, 0, fb);  // every slab of the K tile
           tma_load_3d(dst + kv_off, &tv, 0, row0, 0, fb);
@@ -388,8 +571,9 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
         const long long phys = max(plist[j / UPP].phys, 0);
         issued = j + 1;
         if (j == a.debug_skip_page) continue;
+        const int kh = j / UPP < segB ? kvhA : kvhB;
         const size_t src0 =
-            ((size_t)((phys * a.Hkv + kvh) * ps) + (size_t)(j % UPP) * TT) * (SL * 128);
+            ((size_t)((phys * a.Hkv + kh) * ps) + (size_t)(j % UPP) * TT) * (SL * 128);
         const uint32_t dst = smem_u32(stages + (size_t)s * stage_bytes);
         for (int i = lane; i < chunks; i += 32) {
           const int row = i / (SL * 8), rem = i % (SL * 8);
@@ -434,23 +618,60 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
   const int gid = lane >> 2, tig = lane & 3;
   if (warp > 0) {
     uint32_t qb[8][2];
-    if constexpr (MMA) {
-      // q as the B operand (k = channel, n = head): b0 = channels 16j+2tig..+1,
-      // b1 = channels 16j+8+2tig..+1 of head gid; heads >= GC are zero.
+    // q as the B operand (k = channel, n = head): b0 = channels 16j+2tig..+1,
+    // b1 = channels 16j+8+2tig..+1 of head gid; heads >= GC are zero.
+    auto load_q = [&](int bq, int h0q) {
 #pragma unroll
       for (int j8 = 0; j8 < 8; ++j8) {
         qb[j8][0] = qb[j8][1] = 0u;
         if (gid < GC) {
           const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-              static_cast<const T *>(a.q) + ((long long)b * a.Hq + head0 + gid) * kHeadDim);
+              static_cast<const T *>(a.q) + ((long long)bq * a.Hq + h0q + gid) * kHeadDim);
           qb[j8][0] = qrow[(16 * j8 + 2 * tig) >> 1];
           qb[j8][1] = qrow[(16 * j8 + 8 + 2 * tig) >> 1];
         }
       }
-    }
+    };
+    // spread: this warp's state for segment A goes out as one of the group's
+    // nw warp partials, and the warp starts segment B afresh
+    const int jB = segB == INT_MAX ? INT_MAX : segB * UPP;  // first tile of segment B
+    bool in_b = false;
+    auto finish_a = [&]() {
+      if constexpr (MMA) {
+        float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+          l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+        }
+        const long long slot = ((long long)gA * a.nw + cw) * GC;
+        float *po = a.spa_o + slot * kHeadDim;
+        float *pml = a.spa_ml + slot * 2;
+        const int h0 = 2 * tig, h1 = h0 + 1;
+        if (gid == 0) {
+          if (h0 < GC) { pml[2 * h0] = m_run[0]; pml[2 * h0 + 1] = l0; }
+          if (h1 < GC) { pml[2 * h1] = m_run[1]; pml[2 * h1 + 1] = l1; }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int d0 = 16 * mt + gid, d1 = d0 + 8;
+          if (h0 < GC) { po[h0 * kHeadDim + d0] = acc[mt][0]; po[h0 * kHeadDim + d1] = acc[mt][2]; }
+          if (h1 < GC) { po[h1 * kHeadDim + d0] = acc[mt][1]; po[h1 * kHeadDim + d1] = acc[mt][3]; }
+          acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        }
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+      }
+      in_b = true;
+    };
+    if constexpr (MMA) load_q(bA, kvhA * a.G + chunk * GC);
     const float sl = a.scale_log2;
 #pragma unroll 1
     for (int j = cw; j < ntiles; j += a.nw) {
+      if (j >= jB && !in_b) {
+        finish_a();
+        if constexpr (MMA) load_q(bB, kvhB * a.G);
+      }
       const int s = j % NS;
       if (!mbar_wait(smem_u32(&full[s]), (j / NS) & 1, a.wait_limit_ns)) {
         if (lane == 0) flag_error(a.status, KV_ERR_DEVICE_TIMEOUT);
@@ -648,6 +869,8 @@ __global__ void __launch_bounds__(kAttnMaxThreads)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     }
+    // a warp with no tile of segment B still hands in its segment A
+    if (segB != INT_MAX && !in_b) finish_a();
   }
 
   // ======================= merge the consumer warps =======================

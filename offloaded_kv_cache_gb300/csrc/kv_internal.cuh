@@ -161,6 +161,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Global loads issued where they stand: volatile asm keeps their order
+// among themselves and against barriers, so a load meant to be in flight
+// beside others (speculatively, its result used only on one branch) is not
+// sunk by the compiler into that branch, behind a decision that needs its
+// own round trip.  The result is waited for at its first use, as usual.
+__device__ __forceinline__ int32_t ld_issue(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_issue(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_issue(const float *p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int4 ld_issue(const int4 *p) {
+  int4 v;
+  asm volatile("ld.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -259,7 +288,28 @@ struct AttnArgs {
   // sparse: 1 when the union lists hold resolved entries (physical page;
   // valid tokens | head mask << 8), as the fused selection writes them
   int union_resolved;
+  // Resolved lists, one head chunk per group, num_splits > 1: 1 lets the
+  // kernel cut the concatenation of every group's list into equal chunks, one
+  // per CTA, when every group is at least a chunk long (so a CTA covers the
+  // tail of one group and the head of the next at most) and the longest CTA of
+  // the split per group would hold spread_min_gain bytes more; 2 whenever
+  // every group is a chunk long (testing); otherwise (and with 0) each group's
+  // list is split over its own num_splits CTAs.  Either way the CTAs record in
+  // gmeta[g] where the combine finds group g's partials.
+  int spread;
+  int spread_min_gain;
+  int ngroups;      // B * Hkv
+  float *spa_o;     // [ngroups][nw][GC][d]: per consumer warp, a group's tail
+  float *spa_ml;    // [ngroups][nw][GC][2]   segment in a CTA that goes on to the next group
+  int32_t *gmeta;   // [ngroups][4]: see kSpreadMeta*
 };
+
+// gmeta[g] = {mode, first CTA, last CTA, tail}: mode kSplitPerGroup (group g's
+// partials are splits 0..S-1 of g), or kSplitSpread (the merged partials of
+// CTAs first..last, except that with tail = 1 the last CTA's part of g is its
+// first of two segments and sits in spa_o/spa_ml[g] as nw warp partials).
+constexpr int kSplitPerGroup = 0;
+constexpr int kSplitSpread = 1;
 
 // Arguments of the fused selection kernel (page score + top-K + union).
 struct SelectArgs {

@@ -72,5 +72,9 @@ size_t select_fused_smem(int G, int maxP);
 cudaError_t launch_select_fused(int dtype, const SelectArgs &a, int B, cudaStream_t st);
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st);
+// the combine after an attention over kv_select_pages' lists (AttnArgs::spread)
+cudaError_t launch_combine_lists(const float *part_o, const float *part_ml, const float *spa_o,
+                                 const float *spa_ml, const int32_t *gmeta, float *out, int S,
+                                 int B, int Hq, int Hkv, int nw, int *status, cudaStream_t st);
 
 }  // namespace kvs

@@ -218,6 +218,120 @@ cudaError_t launch_union(const int32_t *indices, const int32_t *ctx, int B, int 
                     maxP, k, umax, upages, umasks, ucount, status);
 }
 
+// ---------------------------------------------------------------------------
+// split combine of the attention over kv_select_pages' lists
+// ---------------------------------------------------------------------------
+// The attention kernel records per group g (gmeta[g]) whether its partials
+// are the S splits of g (kSplitPerGroup: partial s of row r at s * rows + r)
+// or come from the equal chunks of all groups' lists (kSplitSpread): the
+// merged partials of CTAs first..last (CTA i's at i * G + head), where with
+// tail = 1 the last CTA's share of g is instead nw warp partials in spa_*.
+// One CTA per (b, q head), one thread per output channel; the merge is the
+// one of combine_kernel over that list of partials.
+template <int kPre>
+__global__ void __launch_bounds__(kHeadDim)
+    combine_lists_kernel(const float *part_o, const float *part_ml, const float *spa_o,
+                         const float *spa_ml, const int32_t *gmeta, float *out, int S, int Hq,
+                         int Hkv, int nw, int *status) {
+  pdl_wait();
+  constexpr int R = (kPre + 31) / 32;  // rounds of 32 partials whose values stay in registers
+  const int r = blockIdx.x, c = threadIdx.x, lane = c & 31;
+  const int G = Hq / Hkv, b = r / Hq, h = r % Hq;
+  const int NG = (int)(gridDim.x / Hq) * Hkv;
+  const int g = b * Hkv + h / G, hl = h % G;
+  const long long ncta = (long long)S * NG;
+  // partial k: merged partial k (k < nm) at base + k * stride, else warp
+  // partial k - nm of the group's tail in spa_*
+  int nm = S, na = 0;
+  const long long rows = (long long)NG * G;
+  const float *ob = part_o + ((long long)g * G + hl) * kHeadDim + c;  // per group: split k
+  const float *mb = part_ml + ((long long)g * G + hl) * 2;
+  long long os = rows * kHeadDim, ms = rows * 2;
+  const float *tob = spa_o + ((long long)g * nw * G + hl) * kHeadDim + c;
+  const float *tmb = spa_ml + ((long long)g * nw * G + hl) * 2;
+  auto po = [&](int k) -> const float * {
+    return k < nm ? ob + k * os : tob + (long long)(k - nm) * G * kHeadDim;
+  };
+  auto pml = [&](int k) -> const float * {
+    return k < nm ? mb + k * ms : tmb + (long long)(k - nm) * G * 2;
+  };
+  // the per-group split's first partials load with the record, as in
+  // combine_kernel (so that split costs no extra round trip); equal chunks
+  // load theirs once the record is read
+  const int4 m = ld_issue(reinterpret_cast<const int4 *>(gmeta) + g);
+  float pre[kPre], mr[R], lr[R];
+  auto load_first = [&](int n) {
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) pre[s] = s < n ? ld_issue(po(s)) : 0.f;
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      const int k = 32 * q + lane;
+      mr[q] = k < n ? ld_issue(pml(k)) : -INFINITY;
+      lr[q] = k < n ? ld_issue(pml(k) + 1) : 0.f;
+    }
+  };
+  load_first(S);
+  if (m.x == kSplitSpread && m.y >= 0 && m.y <= m.z && m.z < ncta && (m.w == 0 || m.w == 1)) {
+    // merged partials of CTAs m.y .. (row CTA * G + head)
+    ob = part_o + ((long long)m.y * G + hl) * kHeadDim + c;
+    mb = part_ml + ((long long)m.y * G + hl) * 2;
+    os = (long long)G * kHeadDim;
+    ms = (long long)G * 2;
+    nm = m.z - m.y + (m.w ? 0 : 1);
+    na = m.w ? nw : 0;
+    load_first(nm + na);
+  } else if (m.x != kSplitPerGroup) {
+    if (c == 0) flag_error(status, KV_ERR_BOUNDS);
+    out[(long long)r * kHeadDim + c] = 0.f;
+    return;
+  }
+  // from here the merge of combine_kernel, over partials 0 .. n - 1
+  const int n = nm + na;
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < R; ++q) M = fmaxf(M, mr[q]);
+  for (int k = 32 * R + lane; k < n; k += 32) M = fmaxf(M, pml(k)[0]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  auto weight = [M](float x) { return (M == -INFINITY || x == -INFINITY) ? 0.f : ex2(x - M); };
+  float l = 0.f, o = 0.f, fr[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    fr[q] = weight(mr[q]);
+    l = fmaf(fr[q], lr[q], l);
+  }
+#pragma unroll
+  for (int s = 0; s < kPre; ++s) {
+    const float ft = __shfl_sync(0xFFFFFFFFu, fr[s / 32], s % 32);
+    if (s < n) o = fmaf(ft, pre[s], o);
+  }
+  for (int s = kPre; s < min(n, 32 * R); ++s)
+    o = fmaf(__shfl_sync(0xFFFFFFFFu, fr[R - 1], s & 31), *po(s), o);
+  for (int s0 = 32 * R; s0 < n; s0 += 32) {
+    const int k = s0 + lane;
+    float f = 0.f;
+    if (k < n) {
+      f = weight(pml(k)[0]);
+      l = fmaf(f, pml(k)[1], l);
+    }
+    const int cnt = min(32, n - s0);
+    for (int t = 0; t < cnt; ++t) o = fmaf(__shfl_sync(0xFFFFFFFFu, f, t), *po(s0 + t), o);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, off);
+  pdl_trigger();
+  out[(long long)r * kHeadDim + c] = l > 0.f ? o / l : 0.f;
+}
+
+cudaError_t launch_combine_lists(const float *part_o, const float *part_ml, const float *spa_o,
+                                 const float *spa_ml, const int32_t *gmeta, float *out, int S,
+                                 int B, int Hq, int Hkv, int nw, int *status, cudaStream_t st) {
+  const long long rows = (long long)B * Hq;
+  auto kern = S <= 16 ? combine_lists_kernel<16> : combine_lists_kernel<64>;
+  return launch_pdl(kern, dim3((unsigned)rows), dim3(kHeadDim), 0, st, part_o, part_ml, spa_o,
+                    spa_ml, gmeta, out, S, Hq, Hkv, nw, status);
+}
+
 cudaError_t launch_combine(const float *part_o, const float *part_ml, float *out, int S, int B,
                            int Hq, cudaStream_t st) {
   const long long rows = (long long)B * Hq;

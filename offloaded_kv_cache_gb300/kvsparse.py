@@ -103,6 +103,7 @@ def load(path: str = LIB_PATH):
         "kv_device_status": (ctypes.c_int, [P]),
         "kv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kv_debug_config": (ctypes.c_int, [i32, ctypes.c_uint64]),
+        "kv_debug_split_mode": (ctypes.c_int, [i32]),
         "kv_stream_read_probe": (ctypes.c_int, [P, sz, P, i32, P]),
         "kv_stream_read_probe_shape": (ctypes.c_int, [P, sz, P, i32, i32, i32, P]),
     }
@@ -301,6 +302,14 @@ def kv_status_string(code: int) -> str:
 def kv_debug_config(skip_page: int, wait_limit_ns: int, check=True):
     rc = load().kv_debug_config(int(skip_page), int(wait_limit_ns))
     return _ret(rc, "kv_debug_config", check)
+
+
+def kv_debug_split_mode(mode: int, check=True):
+    """Attention over kv_select_pages' lists: -1 the plan chooses; 0 per-group
+    splits; 1 equal chunks of all groups' lists where possible; 2 the kernel
+    chooses for every call the shapes allow."""
+    rc = load().kv_debug_split_mode(int(mode))
+    return _ret(rc, "kv_debug_split_mode", check)
 
 
 def kv_stream_read_probe(src, nbytes, sink, stream=None, check=True):

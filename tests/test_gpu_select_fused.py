@@ -189,12 +189,177 @@ def test_selection_workspace_too_small_is_refused():
     assert rc == kv.KV_ERR_WORKSPACE
 
 
+# ---------------------------------------------------------------------------
+# the attention over the lists: each group's list split over its own CTAs, or
+# all groups' lists cut into equal chunks (kv_debug_split_mode)
+# ---------------------------------------------------------------------------
+
+def union_sizes(idx, ctx, spec):
+    G = spec.group
+    U = []
+    for b in range(spec.batch):
+        P = -(-int(ctx[b]) // spec.page_size)
+        for h in range(spec.num_kv_heads):
+            sel = idx[b, h * G:(h + 1) * G].reshape(-1)
+            U.append(len(np.unique(sel[(sel >= 0) & (sel < P)])))
+    return U
+
+
+def expect_equal_chunks(layer, idx, ctx, spec, k, adaptive=False):
+    """Whether the kernel cuts the lists into equal chunks: every group
+    (sequence, kv head) holds at least ceil(T / N) union pages, T their sum,
+    N = splits x groups, T >= N; and, when it chooses (adaptive), the
+    per-group split's longest CTA holds at least the K/V a CTA streams in
+    2.5 us at 7 TB/s / N more than an equal chunk."""
+    S = kv.kv_attn_num_splits(layer.shape, k)
+    U = union_sizes(idx, ctx, spec)
+    T, N = sum(U), S * len(U)
+    ok = S > 1 and T >= N and min(U) * N >= T
+    if ok and adaptive:
+        page_bytes = 2 * spec.page_size * spec.head_dim * spec.elem_bytes
+        gain = (-(-max(U) // S) - (-(-T // N))) * page_bytes
+        ok = gain >= int(7.0e3 / N * 2500)
+    return ok
+
+
+def attn_in_both_modes(wl, k, kv_loc=None):
+    layer = DecodeLayer(wl, topk=k, kv_loc=kv_loc)
+    layer.build_index()
+    layer.select_fused()
+    torch.cuda.synchronize()
+    outs = {}
+    try:
+        for mode in (0, 1):
+            kv.kv_debug_split_mode(mode)
+            layer.out.fill_(float("nan"))
+            layer.sparse_attn_selected()
+            torch.cuda.synchronize()
+            assert kv.kv_device_status() == kv.KV_OK
+            outs[mode] = layer.out.cpu().numpy().copy()
+    finally:
+        kv.kv_debug_split_mode(-1)
+    return layer, layer.indices.cpu().numpy(), outs
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,ps,batch,ctx,k", [
+    ("bf16", 16, 2, 64, 3, [300 * 64 + 17, 120 * 64, 41 * 64 + 63], 24),
+    ("f16", 8, 2, 16, 4, [900 * 16 + 3, 700 * 16, 650 * 16 + 9, 999 * 16], 40),
+    ("bf16", 32, 4, 16, 2, [2000 * 16, 1500 * 16 + 5], 64),
+    ("bf16", 8, 1, 64, 5, [90 * 64, 80 * 64 + 1, 200 * 64, 33 * 64, 150 * 64 + 40], 10),
+    # one row far shorter than the others: its groups hold fewer pages than
+    # a chunk, so the kernel keeps the split per group
+    ("bf16", 8, 2, 16, 3, [1200 * 16, 1100 * 16, 5], 30),
+])
+def test_equal_chunks_match_per_group_split(dtype, hq, hkv, ps, batch, ctx, k):
+    if hq // hkv not in (4, 8):
+        pytest.skip("the one-call selection covers 4 or 8 heads per kv head")
+    spec = W.tiny_spec(dtype=dtype, batch=batch, hq=hq, hkv=hkv, context=max(ctx), ps=ps, topk=k,
+                       index=5800 + hq + hkv + ps + batch)
+    wl = W.generate(spec, context_lens=ctx)
+    layer, idx, outs = attn_in_both_modes(wl, k)
+    assert np.isfinite(outs[1]).all()
+    if expect_equal_chunks(layer, idx, wl.context_lens, spec, k):
+        # the same softmax merged in another order
+        np.testing.assert_allclose(outs[1], outs[0], rtol=0, atol=1e-5)
+        assert not np.array_equal(outs[1], outs[0])
+    else:
+        # the list combine merges the per-group splits in combine_kernel's order
+        assert np.array_equal(outs[1], outs[0])
+    check_against_oracle(wl, k, idx, outs[1])
+
+
+def test_equal_chunks_cover_both_decisions():
+    # the parametrization above reaches both branches
+    seen = set()
+    for ctx, k in [([1200 * 16, 1100 * 16, 5], 30), ([900 * 16, 700 * 16, 650 * 16], 40)]:
+        spec = W.tiny_spec(dtype="bf16", batch=len(ctx), hq=8, hkv=2, context=max(ctx), ps=16,
+                           topk=k, index=5900 + k)
+        wl = W.generate(spec, context_lens=ctx)
+        layer = DecodeLayer(wl, topk=k)
+        layer.build_index()
+        layer.select_fused()
+        torch.cuda.synchronize()
+        seen.add(expect_equal_chunks(layer, layer.indices.cpu().numpy(), wl.context_lens, spec, k))
+    assert seen == {True, False}
+
+
+def test_equal_chunks_host_resident_kv():
+    ctx = [700 * 16 + 7, 500 * 16, 640 * 16]
+    spec = W.tiny_spec(dtype="bf16", batch=3, hq=8, hkv=2, context=max(ctx), ps=16, topk=32,
+                       index=5950)
+    wl = W.generate(spec, context_lens=ctx)
+    layer, idx, outs = attn_in_both_modes(wl, 32, kv_loc="host")
+    assert expect_equal_chunks(layer, idx, wl.context_lens, spec, 32)
+    np.testing.assert_allclose(outs[1], outs[0], rtol=0, atol=1e-5)
+    check_against_oracle(wl, 32, idx, outs[1])
+
+
+@pytest.mark.parametrize("hq,hkv,ps,k,ctx", [
+    # rows of very different lengths: the long rows' groups hold far more
+    # pages, so the kernel takes equal chunks
+    (16, 2, 64, 64, [600 * 64, 75 * 64 + 3, 600 * 64 - 1, 80 * 64]),
+    (8, 2, 16, 256, [2400 * 16, 100 * 16 + 3, 2400 * 16 - 1, 110 * 16]),
+    # equal lengths: the groups differ by a few pages, so it keeps the split
+    # per group (bit for bit the per-group result)
+    (8, 2, 16, 256, [2400 * 16, 2400 * 16, 2400 * 16, 2400 * 16]),
+])
+def test_kernel_chooses_the_split(hq, hkv, ps, k, ctx):
+    spec = W.tiny_spec(dtype="bf16", batch=len(ctx), hq=hq, hkv=hkv, context=max(ctx), ps=ps,
+                       topk=k, index=6000 + hq + ps + ctx[1])
+    wl = W.generate(spec, context_lens=ctx)
+    layer = DecodeLayer(wl, topk=k)
+    layer.build_index()
+    layer.select_fused()
+    torch.cuda.synchronize()
+    outs = {}
+    try:
+        for mode in (0, 2):
+            kv.kv_debug_split_mode(mode)
+            layer.out.fill_(float("nan"))
+            layer.sparse_attn_selected()
+            torch.cuda.synchronize()
+            assert kv.kv_device_status() == kv.KV_OK
+            outs[mode] = layer.out.cpu().numpy().copy()
+    finally:
+        kv.kv_debug_split_mode(-1)
+    idx = layer.indices.cpu().numpy()
+    chunks = expect_equal_chunks(layer, idx, wl.context_lens, spec, k, adaptive=True)
+    assert chunks == (ctx[0] != ctx[1])
+    if chunks:
+        np.testing.assert_allclose(outs[2], outs[0], rtol=0, atol=1e-5)
+        assert not np.array_equal(outs[2], outs[0])
+    else:
+        assert np.array_equal(outs[2], outs[0])
+    check_against_oracle(wl, k, idx, outs[2])
+
+
+def test_split_mode_hook_refuses_bad_modes():
+    for m in (-2, 3, 7):
+        assert kv.kv_debug_split_mode(m, check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_debug_split_mode(-1) == kv.KV_OK
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["llama3.1-8b-b4-ctx32k", "70b-gqa-b8-ctx64k-ps64",
                                   "llama3.1-8b-b1-ctx128k-host"])
 def test_fused_selection_full_size(name):
     spec = W.WORKLOADS[name]
     wl = W.generate(spec)
-    _, idx, idx_sep, out, out_sep = fused_vs_separate(wl, spec.topk)
+    kv.kv_debug_split_mode(0)
+    try:
+        layer, idx, idx_sep, out, out_sep = fused_vs_separate(wl, spec.topk)
+    finally:
+        kv.kv_debug_split_mode(-1)
     assert np.array_equal(idx, idx_sep)
     assert np.array_equal(out, out_sep)
+    # the plan's own choice, and equal chunks forced, against the per-group split
+    for mode in (-1, 1):
+        kv.kv_debug_split_mode(mode)
+        try:
+            layer.out.fill_(float("nan"))
+            layer.sparse_attn_selected()
+            torch.cuda.synchronize()
+        finally:
+            kv.kv_debug_split_mode(-1)
+        assert kv.kv_device_status() == kv.KV_OK
+        np.testing.assert_allclose(layer.out.cpu().numpy(), out_sep, rtol=0, atol=1e-5)
