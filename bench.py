@@ -46,15 +46,16 @@ METRIC = "decode-attn KV GB/s and % of HBM (or pinned-host) roofline; queries/se
 # workload (its batch in "from_batch"), applied to this launch's algorithmic
 # bytes (the traffic grows with the union bytes the launch reads).
 NCU_TRAFFIC = {
-    # attention + combine launches of kv_sparse_decode_attn_selected at batch 2
-    # (274.23 MB + 1.89 MB against 274.11 MB algorithmic; ncu empties the
-    # caches before each launch, so the combine's partials, which stay in L2
-    # between the two launches in a timed step, count as DRAM reads here)
-    "70b-gqa-b8-ctx64k-ps64": {"per_alg_byte": 1.00734, "from_batch": 2,
-                               "src": "6818ad5264681ba4"},
-    # the same two launches at full size (189.71 MB against 188.65 MB)
-    "llama3.1-8b-b4-ctx32k": {"per_alg_byte": 1.00565, "from_batch": 4,
-                              "src": "6818ad5264681ba4"},
+    # attention + combine launches of kv_sparse_decode_attn_selected at batch 4
+    # (543.56 + 0.52 MB attention, 2.41 MB combine, against 543.39 MB
+    # algorithmic; ncu empties the caches before each launch, so the
+    # combine's partials, which stay in L2 between the two launches in a
+    # timed step, count as DRAM reads here)
+    "70b-gqa-b8-ctx64k-ps64": {"per_alg_byte": 1.00568, "from_batch": 4,
+                               "src": "ea6a1e573e38cb3c"},
+    # the same two launches at full size (189.88 MB against 188.65 MB)
+    "llama3.1-8b-b4-ctx32k": {"per_alg_byte": 1.00653, "from_batch": 4,
+                              "src": "ea6a1e573e38cb3c"},
 }
 
 
@@ -636,6 +637,45 @@ def side_workload(name, steps, warm):
     torch.cuda.empty_cache()
     return res
 
+def mixed_lengths(name, steps, warm):
+    """The workload with every other row at an eighth of its context (a batch
+    of sequences of different lengths): the sparse step with the plan's own
+    split of the attention work over the CTAs, and with each (sequence, kv
+    head) group's list split over its own CTAs (kv_debug_split_mode 0)."""
+    import torch
+    from offloaded_kv_cache_gb300 import kvsparse as kv
+    from offloaded_kv_cache_gb300 import workloads as W
+    from offloaded_kv_cache_gb300.pipeline import DecodeLayer
+    spec = W.WORKLOADS[name]
+    ctx = [spec.context if b % 2 == 0 else spec.context // 8 for b in range(spec.batch)]
+    wl = W.generate(spec, context_lens=ctx)
+    copies = kv_copies_for(spec)
+    layer = DecodeLayer(wl, kv_copies=copies)
+    layer.build_index()
+    layer.select_fused()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    step_bytes, attn_bytes = sparse_bytes(spec, wl.context_lens, layer.indices.cpu().numpy(),
+                                          lists=True, scores_in_memory=scores_in_memory(layer))
+    stages = [("select_pages", layer.select_fused), ("sparse_attn", layer.sparse_attn_selected)]
+    res = {"context_lens": f"rows alternate {spec.context} and {spec.context // 8} tokens",
+           "steps": steps, "step_bytes": int(step_bytes), "attention_bytes": int(attn_bytes)}
+    for label, mode in (("plan", -1), ("per_group_split", 0)):
+        kv.kv_debug_split_mode(mode)
+        try:
+            total, per = timed_stages(layer, copies, stages, steps, warm)
+        finally:
+            kv.kv_debug_split_mode(-1)
+        ms = total / steps
+        res[label] = {"ms_per_step": round(ms, 5),
+                      "GB_s": round(step_bytes / (ms * 1e-3) / 1e9, 2),
+                      "attention_ms": round(per["sparse_attn"], 5),
+                      "attention_GB_s": round(attn_bytes / (per["sparse_attn"] * 1e-3) / 1e9, 2)}
+    assert kv.kv_device_status() == kv.KV_OK
+    del layer
+    torch.cuda.empty_cache()
+    return res
+
 # ---------------------------------------------------------------------------
 
 def run_reference(args, spec_name):
@@ -687,6 +727,8 @@ def main():
     ap.add_argument("--side-workloads", default=",".join(SIDE_WORKLOADS),
                     help="comma-separated sparse workloads also timed (shorter) and reported "
                          "under `workloads`; empty for none")
+    ap.add_argument("--no-mixed", action="store_true",
+                    help="skip the side measurement of a batch of mixed context lengths")
     ap.add_argument("--window-steps", type=int, default=0,
                     help="profiling aid: run this many eager page-window decode steps "
                          "(x1 window, drifting queries) on the workload and exit")
@@ -962,6 +1004,9 @@ def main():
         side[name] = side_workload(name, max(10, min(args.steps, 200)), args.warmup)
     if side:
         extra["workloads"] = side
+    if sparse and spec.batch >= 2 and not args.no_mixed:
+        extra["mixed_lengths"] = mixed_lengths(spec.name, max(10, min(args.steps, 200)),
+                                               args.warmup)
 
     peak, peak_kind = measured_peaks()
     bound = "hbm"
