@@ -119,3 +119,30 @@ def test_host_step_rejects_missing_sparse_buffers():
     assert kv.kv_decode_step(layer.shape, io, check=False) == kv.KV_OK
     torch.cuda.synchronize()
     assert kv.kv_device_status() == kv.KV_OK
+
+
+@pytest.mark.parametrize("kv_loc", ["hbm", "host"])
+def test_host_step_equal_chunks(kv_loc):
+    # the step's attention with all groups' lists cut into equal chunks
+    # (kv_debug_split_mode 1) against the per-group split (mode 0)
+    ctx = [16 * 60 + 5, 16 * 44, 16 * 52 + 9]
+    spec = W.tiny_spec(dtype="bf16", batch=3, hq=16, hkv=2, context=max(ctx), ps=16, topk=8,
+                       index=131)
+    wl = W.generate(spec, context_lens=ctx)
+    layer = DecodeLayer(wl, kv_loc=kv_loc, topk=8)
+    layer.build_index()
+    q_host = layer.q.cpu().pin_memory()
+    ctx_host = layer.context_lens.cpu().pin_memory()
+    outs = {}
+    try:
+        for mode in (0, 1):
+            kv.kv_debug_split_mode(mode)
+            out_host = torch.full(layer.out.shape, np.nan, dtype=torch.float32).pin_memory()
+            layer.host_step(layer.host_io(q_host, ctx_host, out_host, True))
+            torch.cuda.synchronize()
+            assert kv.kv_device_status() == kv.KV_OK
+            outs[mode] = out_host.numpy().copy()
+    finally:
+        kv.kv_debug_split_mode(-1)
+    assert np.isfinite(outs[1]).all()
+    np.testing.assert_allclose(outs[1], outs[0], rtol=0, atol=1e-5)
