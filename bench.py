@@ -1047,6 +1047,7 @@ def main():
                                   f"{R_GRAPH} steps; per-kernel times from graphs of each stage alone"),
                        "parallelism": f"replicas x{ws}"},
             "queries_per_s": round(qps, 1),
+            "sequence_steps_per_s": round(qps / spec.num_q_heads, 1),
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": int(attn_bytes),

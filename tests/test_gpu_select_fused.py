@@ -268,6 +268,21 @@ def test_equal_chunks_match_per_group_split(dtype, hq, hkv, ps, batch, ctx, k):
     check_against_oracle(wl, k, idx, outs[1])
 
 
+def test_equal_chunks_many_groups():
+    # 24 sequences x 8 kv heads = 192 groups, more than a CTA's 160 threads:
+    # each thread sums the lengths of two groups in the prefix scan
+    rng = np.random.default_rng(77)
+    ctx = [int(x) for x in rng.integers(60 * 16, 200 * 16, size=24)]
+    spec = W.tiny_spec(dtype="bf16", batch=24, hq=32, hkv=8, context=max(ctx), ps=16, topk=16,
+                       index=5990)
+    wl = W.generate(spec, context_lens=ctx)
+    layer, idx, outs = attn_in_both_modes(wl, 16)
+    assert expect_equal_chunks(layer, idx, wl.context_lens, spec, 16)
+    np.testing.assert_allclose(outs[1], outs[0], rtol=0, atol=1e-5)
+    assert not np.array_equal(outs[1], outs[0])
+    check_against_oracle(wl, 16, idx, outs[1])
+
+
 def test_equal_chunks_cover_both_decisions():
     # the parametrization above reaches both branches
     seen = set()
