@@ -4,8 +4,9 @@ Each case draws a dtype, batch, kv heads, GQA group size (odd ones too, so
 that head chunking takes every form), page size, ragged per-row lengths, a
 page budget K (sometimes beyond the row's pages) and the K/V location, then
 checks the min/max index, the scores, the top-K selection, sparse and dense
-attention (as in test_gpu_parity), and in half of the cases also the
-forced-page selection and two page-window steps.  Same bars as the parity
+attention (as in test_gpu_parity), the one-call selection and the attention
+over its lists (both splits of the attention work), and in half of the cases
+also the forced-page selection and two page-window steps.  Same bars as the parity
 tests; the oracle never sees a GPU value.
 """
 import os
@@ -56,11 +57,43 @@ def test_random_shape_through_the_path(i):
                        context=max(c["ctx"]), ps=c["ps"], topk=c["k"], index=c["index"])
     wl = W.generate(spec, context_lens=c["ctx"])
     layer = run_pipeline_and_check(wl, c["k"], kv_loc=c["kv_loc"])
-    if not c["extras"]:
-        return
     ps, k, dtype = c["ps"], c["k"], c["dtype"]
     mn, mx = oracle.minmax_build(dtype, wl.k_cache, wl.block_table, wl.context_lens)
     s = oracle.scores(dtype, wl.q, mn, mx, wl.block_table, wl.context_lens, ps)
+
+    # the one-call selection gives the separate calls' selection; the
+    # attention over its lists, with each group's list over its own splits
+    # and with equal chunks of all groups' lists where the shape allows, gives
+    # the oracle's attention on every row whose selection is the oracle's
+    sel_sep = layer.indices.cpu().numpy().copy()
+    layer.select_fused()
+    torch.cuda.synchronize()
+    assert kv.kv_device_status() == kv.KV_OK
+    assert np.array_equal(layer.indices.cpu().numpy(), sel_sep)
+    outs = {}
+    try:
+        for mode in (0, 1):
+            kv.kv_debug_split_mode(mode)
+            layer.out.fill_(float("nan"))
+            layer.sparse_attn_selected()
+            torch.cuda.synchronize()
+            assert kv.kv_device_status() == kv.KV_OK
+            outs[mode] = layer.out.cpu().numpy().copy()
+    finally:
+        kv.kv_debug_split_mode(-1)
+    np.testing.assert_allclose(outs[1], outs[0], rtol=0, atol=1e-5)
+    ref_idx = oracle.topk(s, wl.context_lens, ps, k)
+    same = np.all(sel_sep == ref_idx, axis=-1)
+    rows = [b * spec.num_q_heads + h for b in range(spec.batch) for h in range(spec.num_q_heads)
+            if same[b, h]]
+    if rows:
+        ref_o = oracle.attention(dtype, wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                                 wl.context_lens, wl.scale, indices=ref_idx, rows=rows)
+        got = outs[1].reshape(-1, spec.head_dim)[rows]
+        err = np.abs(got - ref_o.reshape(-1, spec.head_dim)[rows]).max()
+        assert err <= ATOL[dtype], err
+    if not c["extras"]:
+        return
 
     # forced pages: the oracle's own fp32 scores fed to the GPU selection
     s32 = s.astype(np.float32)
