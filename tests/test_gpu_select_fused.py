@@ -348,6 +348,64 @@ def test_kernel_chooses_the_split(hq, hkv, ps, k, ctx):
     check_against_oracle(wl, k, idx, outs[2])
 
 
+def test_equal_chunks_bad_length_keeps_the_per_group_split():
+    # a row whose length is out of range has an empty list, so no group is a
+    # chunk long: the kernel keeps the split per group, flags the length and
+    # writes zeros for that row; the other rows are the per-group results
+    ctx = [300 * 16 + 5, 250 * 16, 280 * 16 + 9]
+    spec = W.tiny_spec(dtype="bf16", batch=3, hq=8, hkv=2, context=max(ctx), ps=16, topk=24,
+                       index=6100)
+    wl = W.generate(spec, context_lens=ctx)
+    layer = DecodeLayer(wl, topk=24)
+    layer.build_index()
+    layer.select_fused()
+    kv.kv_debug_split_mode(0)
+    try:
+        layer.sparse_attn_selected()
+        torch.cuda.synchronize()
+        good = layer.out.cpu().numpy().copy()
+        assert kv.kv_device_status() == kv.KV_OK
+        bad = layer.context_lens.clone()
+        bad[1] = 0
+        layer.context_lens.copy_(bad)
+        kv.kv_debug_split_mode(1)
+        layer.out.fill_(float("nan"))
+        layer.sparse_attn_selected()
+        torch.cuda.synchronize()
+    finally:
+        kv.kv_debug_split_mode(-1)
+    assert kv.kv_device_status() == kv.KV_ERR_BOUNDS
+    out = layer.out.cpu().numpy()
+    assert (out[1] == 0).all()
+    assert np.array_equal(out[[0, 2]], good[[0, 2]])
+
+
+def test_equal_chunks_bounded_wait_times_out_and_context_survives():
+    # a tile no producer fills (testing hook): the waits give up after 50 ms,
+    # the call's kernels finish, the status says so, and the next call is right
+    ctx = [400 * 16, 380 * 16 + 7]
+    spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=2, context=max(ctx), ps=16, topk=32,
+                       index=6200)
+    wl = W.generate(spec, context_lens=ctx)
+    layer, idx, outs = attn_in_both_modes(wl, 32)
+    assert expect_equal_chunks(layer, idx, wl.context_lens, spec, 32)
+    kv.kv_debug_split_mode(1)
+    kv.kv_debug_config(3, 50_000_000)
+    try:
+        layer.sparse_attn_selected()
+        torch.cuda.synchronize()
+        assert kv.kv_device_status() == kv.KV_ERR_DEVICE_TIMEOUT
+        kv.kv_debug_config(-1, 2_000_000_000)
+        layer.out.fill_(float("nan"))
+        layer.sparse_attn_selected()
+        torch.cuda.synchronize()
+    finally:
+        kv.kv_debug_config(-1, 2_000_000_000)
+        kv.kv_debug_split_mode(-1)
+    assert kv.kv_device_status() == kv.KV_OK
+    assert np.array_equal(layer.out.cpu().numpy(), outs[1])
+
+
 def test_split_mode_hook_refuses_bad_modes():
     for m in (-2, 3, 7):
         assert kv.kv_debug_split_mode(m, check=False) == kv.KV_ERR_INVALID_ARG
