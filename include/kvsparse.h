@@ -247,8 +247,15 @@ int kv_select_pages(const kv_shape *shape, const void *q, const void *minmax,
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /* Sparse decode attention over the pages the preceding kv_select_pages call
- * chose: the same out as kv_sparse_decode_attn with that call's indices.
- * The workspace is the one kv_select_pages filled, unchanged since. */
+ * chose: the out of kv_sparse_decode_attn with that call's indices.  It is
+ * the same bit for bit when each (sequence, kv head) group's list is split
+ * over the group's own CTAs; where a CTA's share can take 100 us or more to
+ * stream (long shares, e.g. 64-token pages over 64k tokens), the kernel may
+ * instead cut all groups' lists into equal chunks, chosen per call from the
+ * lists' lengths (a batch of rows of different lengths), and then the result
+ * differs only in the order of the floating-point merge (kv_debug_split_mode
+ * fixes the choice).  The workspace is the one kv_select_pages filled,
+ * unchanged since. */
 int kv_sparse_decode_attn_selected(const kv_shape *shape, const void *q, const void *k_cache,
                                    const void *v_cache, const int32_t *block_table,
                                    const int32_t *context_lens, int32_t k, float scale,
