@@ -325,8 +325,9 @@ int kv_stream_read_probe_shape(const void *src, size_t bytes, unsigned long long
  * those are given, else (and for a dense step) the kernels read them in
  * place.  Any other host buffer is copied through the matching device buffer
  * with cudaMemcpyAsync (q, context_lens, out may be NULL only for mapped
- * buffers).  The same outputs as the separate calls.  The index (minmax) must
- * be built. */
+ * buffers).  The same outputs as those calls (kv_sparse_decode_attn_selected
+ * says when its merge order may differ from kv_sparse_decode_attn's).  The
+ * index (minmax) must be built. */
 typedef struct {
   const void *q_host;               /* [B][Hq][d] dtype, host                  */
   const int32_t *context_lens_host; /* [B], host                               */
