@@ -164,6 +164,16 @@ int main(int argc, char **argv) {
   CHECK(kv_dense_decode_attn(&s, q, kc, vc, bt, ctx, scale, out, ws, ws_max, NULL));
   CHECK(kv_device_status(NULL));
   save(dir, "dense.out", out, (size_t)B * Hq * 128 * 4);
+  /* the one-call selection and the attention over its lists */
+  const size_t ws_sel = kv_select_workspace_bytes(&s, k);
+  void *ws2 = dalloc(ws_sel);
+  int32_t *idx2 = (int32_t *)dalloc((size_t)B * Hq * k * 4);
+  CHECK(kv_select_pages(&s, q, mm, bt, ctx, k, 0, 0, idx2, ws2, ws_sel, NULL));
+  CHECK(kv_sparse_decode_attn_selected(&s, q, kc, vc, bt, ctx, k, scale, out, ws2, ws_sel,
+                                       NULL));
+  CHECK(kv_device_status(NULL));
+  save(dir, "indices_sel.out", idx2, (size_t)B * Hq * k * 4);
+  save(dir, "selected.out", out, (size_t)B * Hq * 128 * 4);
   printf("ok\n");
   return 0;
 }
@@ -219,6 +229,11 @@ def test_c_program_runs_the_path_and_matches_the_binding(kvlib):
     assert np.array_equal(rd("indices.out", np.int32), layer.indices.cpu().numpy().reshape(-1))
     assert np.array_equal(rd("sparse.out", np.float32), sparse_py.reshape(-1))
     assert np.array_equal(rd("dense.out", np.float32), dense_py.reshape(-1))
+    # the one-call selection chose the same pages, and the attention over its
+    # lists (each group's list over its own splits on this shape) gives the
+    # same bits as the sparse call
+    assert np.array_equal(rd("indices_sel.out", np.int32), layer.indices.cpu().numpy().reshape(-1))
+    assert np.array_equal(rd("selected.out", np.float32), sparse_py.reshape(-1))
     # and the dense output against the oracle
     ref = oracle.attention("bf16", wl.q, wl.k_cache, wl.v_cache, wl.block_table,
                            wl.context_lens, wl.scale)
