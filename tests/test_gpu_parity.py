@@ -97,6 +97,18 @@ def test_topk_sizes_including_k_beyond_pages(k):
     run_pipeline_and_check(wl, k)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_large_logits_peaked_softmax(dtype):
+    # q, K, V ~ N(0, 16^2): scaled logits of a few hundred, so the softmax is
+    # dominated by a handful of tokens and every tile's and split's running
+    # maximum moves by large amounts (rescale factors far below 2^-100)
+    ctx = [16 * 300 + 5, 16 * 137 + 11]
+    spec = W.tiny_spec(dtype=dtype, batch=2, hq=8, hkv=2, context=max(ctx), ps=16, topk=40,
+                       scale=16.0, index=2900)
+    wl = W.generate(spec, context_lens=ctx)
+    run_pipeline_and_check(wl, 40)
+
+
 def test_single_token_context_returns_its_value():
     spec = W.tiny_spec(dtype="bf16", batch=2, hq=8, hkv=1, context=1, ps=16, topk=2, index=2200)
     wl = W.generate(spec)
