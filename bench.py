@@ -1,9 +1,14 @@
 """Decode-attention benchmark: KV GB/s, % of the bandwidth roofline, queries/s.
 
 One step = one pass of the decode path of one layer over one batch of the
-workload: dense attention for a dense-only workload; page scoring, top-K
-selection and sparse attention for a workload with a page budget (the dense
-pass and the index build are timed beside it and reported as sub-objects).
+workload: dense attention for a dense-only workload; for a workload with a
+page budget, kv_select_pages (page scoring, top-K selection and the group
+unions in one call) and kv_sparse_decode_attn_selected (sparse attention and
+the split combine).  The same step through the separate calls, the dense
+pass, the index builds, the decode append, two other sparse workloads and a
+batch of mixed context lengths are timed beside it and reported as
+sub-objects.  The default workload is the largest that fits one GPU, a
+70B-class GQA layer with 2 GiB of K/V.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference]
